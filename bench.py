@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Mixed-step attention throughput on GB300: tokens/s and fraction of the step roofline.
+
+One timed step is one pass of the whole hot path -- ms_kv_append_rope then
+ms_mixed_step_attention -- over every batch of the workload.  The default
+workload is the 7B-like MHA layer at token budget 512: 64 running decodes
+(c ~ U[512, 4096]) next to a 448-token chunk of a 4096-token prompt, at each of
+the prompt's nine prefix offsets 0, 448, ..., 3584 (nine batches per step,
+4608 tokens).  Inputs are seeded synthetic bf16 (N(0,1)); the KV pool (~2.5 GB)
+is larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica (weak scaling); timing is the
+max over ranks.  --impl reference times the fp64 CPU oracle on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+# the CPU oracle runs single-threaded (its reported core count is 1)
+for _var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_var, "1")
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "mixed-step attention tokens/s on 1 GB300; % of step roofline (HBM GB/s | TFLOP/s)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, dist=None, device=None) -> float:
+    """Max of a float over ranks (identity without a process group)."""
+    if dist is None or not dist.is_initialized():
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, dist=None, device=None) -> float:
+    if dist is None or not dist.is_initialized():
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- workload
+
+def load_workload(name: str):
+    wls = workloads.CONFIGS[name]()
+    return wls if isinstance(wls, list) else [wls]
+
+
+def describe(name: str, wls) -> str:
+    wl = wls[0]
+    n_dec = sum(1 for r in wl.requests if r.remaining == 0)
+    return (f"{name}: H_q {wl.H_q}, H_kv {wl.H_kv}, D {wl.D}, page 16, budget {wl.token_budget}, "
+            f"{n_dec} decodes + prefill chunk(s), {len(wls)} batch(es) per step")
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        load = [s for s, p in zip(sm, power) if p > 200.0] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import chunked_prefill_mixed_decode_gb300 as ms
+    from chunked_prefill_mixed_decode_gb300 import build as msbuild
+    from chunked_prefill_mixed_decode_gb300 import roofline, step
+
+    msbuild.build()
+    dist = None
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist = dist_init("nccl")
+    wls = load_workload(args.config)
+    wl0 = wls[0]
+    peaks, peak_src = read_peaks()
+
+    # ---- setup (untimed): metadata, device buffers, one shared KV pool
+    subs = []
+    pool = workloads.kv_pool(wl0, 1000 + rank, device)
+    max_pos = max(wl.max_pos for wl in wls) + 1
+    cos, sin = step.rope_tables_device(max_pos, wl0.D, device)
+    for i, wl in enumerate(wls):
+        states = [(r.cached_len, r.remaining) for r in wl.requests]
+        tables = [r.block_table for r in wl.requests]
+        meta = ms.build_batch_metadata(states, tables, wl.token_budget, wl.max_chunk)
+        batch = step.to_device(meta, device)
+        T = meta["num_tokens"]
+        q, k, v = workloads.step_tensors(wl, T, 50 + i + 1000 * rank, device)
+        rows = [(int(meta["q_start_pos"][s]), int(meta["cu_seqlens_q"][s + 1] - meta["cu_seqlens_q"][s]))
+                for s in range(meta["num_rows"])]
+        counts = roofline.step_counts(rows, wl.H_q, wl.H_kv, wl.D, meta["bt_stride"])
+        subs.append(dict(wl=wl, states=states, tables=tables, meta=meta, batch=batch, q=q, k=k, v=v,
+                         q_rot=torch.empty_like(q), out=torch.empty_like(q), counts=counts))
+    ws_bytes = max(ms.attention_workspace_size(max(s["meta"]["num_rows"], 1), max(s["meta"]["num_tokens"], 1),
+                                               s["batch"].context_total, wl0.H_q, wl0.H_kv, wl0.D) for s in subs)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    k_cache, v_cache = pool
+
+    def one_step(events=None):
+        for j, s in enumerate(subs):
+            b = s["batch"]
+            ms.kv_append_rope(s["q"], s["k"], s["v"], b.positions, b.slot_mapping, cos, sin, k_cache, v_cache,
+                              q_rot=s["q_rot"], dev_status=status, stream=stream)
+            if events is not None:
+                events[j][0].record(stream)
+            ms.mixed_step_attention(s["q_rot"], k_cache, v_cache, b.cu_seqlens_q, b.q_start_pos, b.context_lens,
+                                    b.block_tables, b.context_total, s["out"], ws, stream=stream)
+            if events is not None:
+                events[j][1].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    if ms.read_status(status) or ms.read_status(ws):
+        raise RuntimeError("device status set during warm-up")
+
+    # ---- timed device region
+    n_sub = len(subs)
+    attn_events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(n_sub)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device.index if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    sampler.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for it in range(args.steps):
+        one_step(attn_events[it])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if ms.read_status(status) or ms.read_status(ws):
+        raise RuntimeError("device status set during the timed region")
+    attn_ms = [[attn_events[it][j][0].elapsed_time(attn_events[it][j][1]) for it in range(args.steps)]
+               for j in range(n_sub)]
+    tokens_per_step = sum(s["meta"]["num_tokens"] for s in subs)
+    max_ms = reduce_max(elapsed_ms, dist, device)
+    total_tokens = reduce_sum(tokens_per_step * args.steps, dist, device)
+    value = total_tokens / (max_ms / 1e3)
+    ms_per_step = max_ms / args.steps
+
+    # ---- roofline of the attention call (the dominant launch group) and of the whole step
+    attn_bytes = sum(s["counts"]["attn_bytes"] for s in subs)
+    attn_flops = sum(s["counts"]["flops"] for s in subs)
+    attn_avg_ms = sum(statistics.mean(a) for a in attn_ms) / n_sub  # mean over batches of the mean duration
+    attn_bytes_avg = attn_bytes / n_sub
+    attn_flops_avg = attn_flops / n_sub
+    t_mem = attn_bytes_avg / (peaks["hbm_gbs"] * 1e9)
+    t_flop = attn_flops_avg / (peaks["bf16_tflops_sustained"] * 1e12)
+    if t_mem >= t_flop:
+        achieved = attn_bytes_avg / (attn_avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None}
+    else:
+        achieved = attn_flops_avg / (attn_avg_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4), "traffic": None}
+    roof["kernel"] = "ms_mixed_step_attention (prologue + chunk + decode + combine launches)"
+    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    roof["per_launch"] = {"alg_bytes": int(attn_bytes_avg), "alg_flops": int(attn_flops_avg),
+                          "avg_ms": round(attn_avg_ms, 4)}
+    step_bytes = sum(s["counts"]["step_bytes"] for s in subs)
+    step_flops = attn_flops
+    t_roof = max(step_bytes / (peaks["hbm_gbs"] * 1e9), step_flops / (peaks["bf16_tflops_sustained"] * 1e12))
+    step_roof = {"alg_bytes": int(step_bytes), "alg_flops": int(step_flops),
+                 "t_roof_ms": round(t_roof * 1e3, 4), "t_meas_ms": round(ms_per_step, 4),
+                 "frac_of_roofline": round(t_roof * 1e3 / ms_per_step, 4),
+                 "vs_nominal_8TBps": round(step_bytes / (8000e9) * 1e3 / ms_per_step, 4)}
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, ms, step, subs, cos, sin, k_cache, v_cache, ws, status, device, stream, dist)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16; KV pool larger than L2)",
+        "config": {"workload": describe(args.config, wls), "tokens_per_step": tokens_per_step,
+                   "batches_per_step": n_sub, "l2": "inputs larger than L2 (KV pool "
+                   f"{2 * k_cache.numel() * 2 / 1e9:.2f} GB); no flush", "parallelism": f"replicas x{world}"},
+        "roofline": roof, "step_roofline": step_roof, "e2e": e2e,
+        "gpu_launches": 5 * n_sub * args.steps, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(args, ms, step, subs, cos, sin, k_cache, v_cache, ws, status, device, stream, dist):
+    """Same metric through the public API from host buffers: per batch, the C++ scheduler
+    builds the metadata, which goes H2D with q/k/v from pinned memory; the output comes back."""
+    import torch
+    host = []
+    for s in subs:
+        host.append(dict(q=s["q"].cpu().pin_memory(), k=s["k"].cpu().pin_memory(), v=s["v"].cpu().pin_memory(),
+                         out=torch.empty_like(s["out"], device="cpu").pin_memory()))
+    n = max(1, min(args.steps, args.e2e_steps))
+    h2d = d2h = 0
+
+    def e2e_step():
+        nonlocal h2d, d2h
+        h2d = d2h = 0
+        for s, hb in zip(subs, host):
+            wl = s["wl"]
+            meta = ms.build_batch_metadata(s["states"], s["tables"], wl.token_budget, wl.max_chunk)
+            b = step.to_device(meta, device, non_blocking=True)
+            q = hb["q"].to(device, non_blocking=True)
+            k = hb["k"].to(device, non_blocking=True)
+            v = hb["v"].to(device, non_blocking=True)
+            q_rot = s["q_rot"]
+            ms.kv_append_rope(q, k, v, b.positions, b.slot_mapping, cos, sin, k_cache, v_cache, q_rot=q_rot,
+                              dev_status=status, stream=stream)
+            ms.mixed_step_attention(q_rot, k_cache, v_cache, b.cu_seqlens_q, b.q_start_pos, b.context_lens,
+                                    b.block_tables, b.context_total, s["out"], ws, stream=stream)
+            hb["out"].copy_(s["out"], non_blocking=True)
+            h2d += b.h2d_bytes + (q.numel() + k.numel() + v.numel()) * 2
+            d2h += s["out"].numel() * 2
+        torch.cuda.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    if dist is not None:
+        dist.barrier()
+    t = time.perf_counter()
+    for _ in range(n):
+        e2e_step()
+    el = time.perf_counter() - t
+    el = reduce_max(el, dist, device)
+    tokens = reduce_sum(sum(s["meta"]["num_tokens"] for s in subs) * n, dist, device)
+    return {"value": round(tokens / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n}
+
+
+# ---------------------------------------------------------------------------- oracle (CPU) timing
+
+def _oracle_sample_workload(wl, n_dec: int, n_chunk: int, seed: int):
+    """The same step shape restricted to its first n_dec decodes and an n_chunk-token chunk."""
+    rng = np.random.default_rng(seed)
+    dec = [(r.cached_len, 0) for r in wl.requests if r.remaining == 0][:n_dec]
+    prm = [(r.cached_len, r.remaining) for r in wl.requests if r.remaining > 0][:1]
+    states = dec + ([(prm[0][0], min(prm[0][1], n_chunk))] if prm and n_chunk > 0 else [])
+    reqs, total = workloads.assign_pages(states, rng)
+    return workloads.Workload(wl.name + "_sample", wl.H_q, wl.H_kv, wl.D, len(dec) + n_chunk, reqs, total,
+                              seed=seed)
+
+
+def _oracle_prepare(sub, seed):
+    """Seeded inputs of one sampled step, as the oracle takes them (bf16 bit arrays)."""
+    states = [(r.cached_len, r.remaining) for r in sub.requests]
+    tables = [r.block_table for r in sub.requests]
+    q, k, v = workloads.step_tensors(sub, sub.token_budget, seed, "cpu")
+    kc, vc = workloads.kv_pool(sub, seed, "cpu")
+    return dict(sub=sub, states=states, tables=tables, q=workloads.bf16_bits(q), k=workloads.bf16_bits(k),
+                v=workloads.bf16_bits(v), kp=workloads.bf16_bits(kc), vp=workloads.bf16_bits(vc))
+
+
+def _oracle_run(prep):
+    """Time the oracle's whole path (schedule, metadata, append, attention) on one sampled step."""
+    import oracle
+    sub = prep["sub"]
+    t = time.perf_counter()
+    rows, _ = oracle.schedule(prep["states"], sub.token_budget)
+    meta = oracle.batch_metadata(rows, prep["tables"], len(prep["states"]))
+    T = meta["num_tokens"]
+    q_rot, kp2, vp2 = oracle.kv_append(prep["q"][:T], prep["k"][:T], prep["v"][:T], meta["positions"],
+                                       meta["slot_mapping"], prep["kp"], prep["vp"])
+    oracle.attention_all(q_rot, kp2, vp2, meta, sub.H_kv)
+    return T, time.perf_counter() - t
+
+
+def _sample_size(wl, seconds):
+    n_dec_all = sum(1 for r in wl.requests if r.remaining == 0)
+    tok, sec = _oracle_run(_oracle_prepare(_oracle_sample_workload(wl, 2, 2, 7), 7))
+    n = int(max(2, min(seconds / max(sec / max(tok, 1), 1e-6), n_dec_all + 448)))
+    n_dec = min(n_dec_all, max(1, n // 2))
+    return n_dec, max(2, n - n_dec)
+
+
+def cpu_baseline(config: str, budget_s: float = 15.0) -> dict:
+    wl = load_workload(config)[0]
+    n_dec, n_chunk = _sample_size(wl, budget_s)
+    tok, sec = _oracle_run(_oracle_prepare(_oracle_sample_workload(wl, n_dec, n_chunk, 8), 8))
+    return {"value": round(tok / sec, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_dec} decodes + a {n_chunk}-token chunk of {config} (all {wl.H_q} heads), "
+                      f"fp64 numpy, one thread, {sec:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    wl = load_workload(args.config)[0]
+    per_step = args.cpu_seconds * 6.0 / max(args.steps + args.warmup, 1)  # whole run within a few minutes
+    n_dec, n_chunk = _sample_size(wl, per_step)
+    prep = _oracle_prepare(_oracle_sample_workload(wl, n_dec, n_chunk, 8), 8)
+    for _ in range(args.warmup):
+        _oracle_run(prep)
+    tot_tok = tot_s = 0.0
+    for _ in range(args.steps):
+        tk, s = _oracle_run(prep)
+        tot_tok += tk
+        tot_s += s
+    value = tot_tok / tot_s
+    sample = (f"{n_dec} decodes + a {n_chunk}-token chunk of {args.config} per step (all {wl.H_q} heads), "
+              f"fp64 numpy, one thread")
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(args.config, load_workload(args.config))}, "impl": "reference",
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="mha7b_b512", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

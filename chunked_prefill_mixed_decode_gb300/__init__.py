@@ -1,0 +1,224 @@
+"""Python binding of the mixed-batch attention step (libmixed_step.so).
+
+Argument marshalling only: every step of the path runs in the C++ scheduler
+and the sm_103a kernels behind the C ABI declared in include/mixed_step.h.
+The functions keep the C names without the ``ms_`` prefix.  Device tensors
+are torch tensors (used for memory and streams only); host metadata is numpy.
+
+There is no fallback: if the shared library is missing or cannot be loaded,
+every call raises.  Build it with ``chunked_prefill_mixed_decode_gb300.build.build()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import numpy as np
+
+from .build import LIB as _LIB_PATH
+
+MS_OK, MS_ERR_ARG, MS_ERR_BUDGET, MS_ERR_NO_PAGES, MS_ERR_CUDA, MS_ERR_DEVICE = 0, -1, -2, -3, -4, -5
+STATUS_BAD_SLOT, STATUS_BAD_POSITION, STATUS_BAD_PAGE, STATUS_TIMEOUT, STATUS_BAD_META = 1, 2, 4, 8, 16
+PAGE_SIZE = 16
+
+_ERR_NAMES = {MS_ERR_ARG: "MS_ERR_ARG", MS_ERR_BUDGET: "MS_ERR_BUDGET", MS_ERR_NO_PAGES: "MS_ERR_NO_PAGES",
+              MS_ERR_CUDA: "MS_ERR_CUDA", MS_ERR_DEVICE: "MS_ERR_DEVICE"}
+
+
+class MixedStepError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what} failed: {_ERR_NAMES.get(code, code)}")
+        self.code = code
+
+
+class Request(ctypes.Structure):
+    _fields_ = [("cached_len", ctypes.c_int32), ("remaining_prompt", ctypes.c_int32),
+                ("block_table", ctypes.POINTER(ctypes.c_int32)), ("num_pages", ctypes.c_int32)]
+
+
+class SchedConfig(ctypes.Structure):
+    _fields_ = [("token_budget", ctypes.c_int32), ("max_chunk_per_request", ctypes.c_int32)]
+
+
+class BatchInfo(ctypes.Structure):
+    _fields_ = [("num_rows", ctypes.c_int32), ("num_decodes", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
+                ("bt_stride", ctypes.c_int32), ("unused_tokens", ctypes.c_int32)]
+
+
+_lib_handle = None
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_VP = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib_handle
+    if _lib_handle is not None:
+        return _lib_handle
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: run chunked_prefill_mixed_decode_gb300.build.build() first")
+    h = ctypes.CDLL(_LIB_PATH)
+    h.ms_build_batch_metadata.restype = ctypes.c_int
+    h.ms_build_batch_metadata.argtypes = [
+        ctypes.POINTER(Request), ctypes.c_int32, ctypes.POINTER(SchedConfig), ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int64, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P, ctypes.POINTER(BatchInfo)]
+    h.ms_rope_table.restype = ctypes.c_int
+    h.ms_rope_table.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_double, _VP, _VP]
+    h.ms_kv_append_rope.restype = ctypes.c_int
+    h.ms_kv_append_rope.argtypes = [_VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP, ctypes.c_int32, _VP, _VP,
+                                    ctypes.c_int32, _VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.c_int32, _VP, _VP]
+    h.ms_attention_workspace_size.restype = ctypes.c_size_t
+    h.ms_attention_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32]
+    h.ms_mixed_step_attention.restype = ctypes.c_int
+    h.ms_mixed_step_attention.argtypes = [_VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP, _VP, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _VP, _VP,
+                                          ctypes.c_size_t, _VP]
+    h.ms_read_status.restype = ctypes.c_int
+    h.ms_read_status.argtypes = [_VP, _VP, _I32P]
+    h.ms_num_sms.restype = ctypes.c_int
+    h.ms_num_sms.argtypes = []
+    _lib_handle = h
+    return h
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != MS_OK:
+        raise MixedStepError(rc, what)
+
+
+def _i32(a: np.ndarray):
+    return a.ctypes.data_as(_I32P)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+# ---------------------------------------------------------------------------- host
+
+def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndarray], token_budget: int,
+                         max_chunk_per_request: int = 0) -> dict:
+    """Decode-first token-budget packing + varlen metadata (ms_build_batch_metadata).
+
+    ``states[i] = (cached_len, remaining_prompt)``; ``block_tables[i]`` is an
+    int32 array of that request's physical pages.  Returns numpy int32 arrays
+    and the batch summary.
+    """
+    n = len(states)
+    tables = [np.ascontiguousarray(bt, dtype=np.int32) for bt in block_tables]
+    reqs = (Request * max(n, 1))()
+    for i, ((c, rem), bt) in enumerate(zip(states, tables)):
+        reqs[i].cached_len = int(c)
+        reqs[i].remaining_prompt = int(rem)
+        reqs[i].block_table = _i32(bt) if len(bt) else None
+        reqs[i].num_pages = len(bt)
+    cfg = SchedConfig(int(token_budget), int(max_chunk_per_request))
+    cap_rows = max(n, 1)
+    cap_tokens = max(int(token_budget), 1)
+    max_pages = max([len(bt) for bt in tables] + [1])
+    cap_bt = cap_rows * max_pages
+    out = {k: np.zeros(sz, dtype=np.int32) for k, sz in (
+        ("cu_seqlens_q", cap_rows + 1), ("q_start_pos", cap_rows), ("context_lens", cap_rows),
+        ("positions", cap_tokens), ("slot_mapping", cap_tokens), ("block_tables", cap_bt),
+        ("row_req", cap_rows), ("num_scheduled", max(n, 1)))}
+    info = BatchInfo()
+    rc = lib().ms_build_batch_metadata(reqs, n, ctypes.byref(cfg), cap_rows, cap_tokens, cap_bt,
+                                       _i32(out["cu_seqlens_q"]), _i32(out["q_start_pos"]),
+                                       _i32(out["context_lens"]), _i32(out["positions"]),
+                                       _i32(out["slot_mapping"]), _i32(out["block_tables"]), _i32(out["row_req"]),
+                                       _i32(out["num_scheduled"]), ctypes.byref(info))
+    _check(rc, "ms_build_batch_metadata")
+    S, T, stride = info.num_rows, info.num_tokens, info.bt_stride
+    return {
+        "cu_seqlens_q": out["cu_seqlens_q"][: S + 1].copy(),
+        "q_start_pos": out["q_start_pos"][:S].copy(),
+        "context_lens": out["context_lens"][:S].copy(),
+        "positions": out["positions"][:T].copy(),
+        "slot_mapping": out["slot_mapping"][:T].copy(),
+        "block_tables": out["block_tables"][: S * stride].reshape(S, stride).copy(),
+        "bt_stride": stride,
+        "row_req": out["row_req"][:S].copy(),
+        "num_scheduled": out["num_scheduled"][:n].copy(),
+        "num_rows": S,
+        "num_decodes": info.num_decodes,
+        "num_tokens": T,
+        "unused_tokens": info.unused_tokens,
+    }
+
+
+def rope_table(max_pos: int, D: int, base: float = 10000.0):
+    """fp32 cos/sin tables [max_pos, D/2] on the host (ms_rope_table)."""
+    cos = np.empty((max_pos, D // 2), dtype=np.float32)
+    sin = np.empty((max_pos, D // 2), dtype=np.float32)
+    _check(lib().ms_rope_table(int(max_pos), int(D), float(base), cos.ctypes.data, sin.ctypes.data),
+           "ms_rope_table")
+    return cos, sin
+
+
+def attention_workspace_size(max_rows: int, max_tokens: int, max_context_total: int, H_q: int, H_kv: int,
+                             D: int) -> int:
+    return int(lib().ms_attention_workspace_size(int(max_rows), int(max_tokens), int(max_context_total), int(H_q),
+                                                 int(H_kv), int(D)))
+
+
+def num_sms() -> int:
+    n = lib().ms_num_sms()
+    _check(n if n < 0 else 0, "ms_num_sms")
+    return n
+
+
+# ---------------------------------------------------------------------------- device
+
+def kv_append_rope(q, k, v, positions, slot_mapping, cos_tab, sin_tab, k_cache, v_cache, q_rot=None,
+                   dev_status=None, stream=None) -> None:
+    """Rotate q, k at absolute positions; append k, v into the paged pools (ms_kv_append_rope)."""
+    T, H_q, D = q.shape
+    H_kv = k.shape[1]
+    if q_rot is None:
+        q_rot = q
+    rc = lib().ms_kv_append_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(slot_mapping), T, _ptr(cos_tab),
+                                 _ptr(sin_tab), cos_tab.shape[0], _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                 _ptr(q_rot), H_q, H_kv, D, PAGE_SIZE, _ptr(dev_status), _stream(stream))
+    _check(rc, "ms_kv_append_rope")
+
+
+def mixed_step_attention(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables,
+                         context_total: int, out, workspace, scale: float = None, stream=None) -> None:
+    """Causal attention of every packed row over its paged context (ms_mixed_step_attention).
+
+    Metadata arguments are device int32 tensors; ``block_tables`` is [rows, stride].
+    ``context_total`` is the host-side sum of context_lens (bounds the workspace).
+    """
+    T, H_q, D = q_rot.shape
+    H_kv = k_cache.shape[1]
+    S = cu_seqlens_q.shape[0] - 1
+    stride = block_tables.shape[1] if block_tables.dim() == 2 else block_tables.shape[0] // max(S, 1)
+    if scale is None:
+        scale = float(D) ** -0.5
+    rc = lib().ms_mixed_step_attention(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                       _ptr(cu_seqlens_q), _ptr(q_start_pos), _ptr(context_lens),
+                                       _ptr(block_tables), stride, S, T, int(context_total), H_q, H_kv, D,
+                                       PAGE_SIZE, float(scale), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "ms_mixed_step_attention")
+
+
+def read_status(dev_status, stream=None) -> int:
+    """Read and clear a device status word (ms_read_status); returns the status bits."""
+    import torch  # noqa: F401
+    v = ctypes.c_int32(0)
+    rc = lib().ms_read_status(_ptr(dev_status), _stream(stream), ctypes.byref(v))
+    if rc not in (MS_OK, MS_ERR_DEVICE):
+        _check(rc, "ms_read_status")
+    return int(v.value)

@@ -1,0 +1,1208 @@
+// Mixed-batch attention over a paged KV cache, sm_103a.
+//
+// A step packs single-token decodes next to prefill chunks ("Chunked Prefill:
+// Ending the Great Stall", sections 03-04).  Row s has d_s new tokens at
+// absolute positions [c_s, c_s + d_s); its query at position p attends keys
+// 0..p ("Chunked Prefill 的 Token 预算" (zwjcode.cn), sections 02 and 07):
+// the cached prefix [0, c) plus its own chunk causally.  The two row kinds sit
+// on opposite sides of the roofline ("Chunked Prefill: Ending the Great
+// Stall", section 03; "Splitting Prefill From Decode Inside a Step", "Two
+// kernels with different limiting resources"), so they take two paths:
+//
+//   decode rows (d = 1): split-KV on CUDA cores.  One warp owns a work item
+//     (row, KV head, span of pages) and streams its pages through a private
+//     ring in shared memory with bulk async copies; the G query heads of the
+//     KV head share every page read.  Lanes hold 8 (D = 128) or 4 (D = 64)
+//     columns of two token rows per 16-byte load; dot products finish with
+//     warp shuffles.  Each item leaves a partial (max, sum, accumulator);
+//     a combine kernel merges the splits.
+//   chunk rows (d > 1): tcgen05 tensor cores.  One CTA owns a 128-row query
+//     tile (128/G tokens x G heads of one KV head) and walks 128-key tiles of
+//     the prefix and its own chunk.  TMA loads Q and K/V pages (one 16-row box
+//     per page and 64-column slab, 128-byte swizzle), S = Q K^T lands in TMEM,
+//     four softmax warps own one row each, write P (bf16) to shared memory, and
+//     O += P V accumulates in TMEM, rescaled only when a row's max grows.
+//
+// A one-CTA prologue validates the metadata, chooses the split size, orders
+// rows longest-first and lays out the work lists in the workspace; both paths
+// pull work from atomic counters with no inter-CTA waiting.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "mixed_step.h"
+#include "ptx.cuh"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+using namespace ms;
+
+constexpr int kPage = 16;
+constexpr int kMinSplitPages = 16;
+constexpr int kMaxSplitPages = 256;
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kChunkThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kPrologueThreads = 1024;
+constexpr int kSortLimit = 2048;    // rows sorted longest-first up to this count
+
+// workspace header (int32 words)
+enum {
+  H_STATUS = 0,
+  H_DEC_CTR = 1,
+  H_CH_CTR = 2,
+  H_NDEC = 3,
+  H_NDEC_ITEMS = 4,
+  H_NCH = 5,
+  H_NCH_ITEMS = 6,
+  H_SPLIT = 7,
+  H_NPART = 8,
+  H_WORDS = 64
+};
+
+struct AttnParams {
+  const bf16* q_rot;
+  const bf16* k_cache;
+  const bf16* v_cache;
+  const int32_t* cu;
+  const int32_t* q_start;
+  const int32_t* ctx_lens;
+  const int32_t* bt;
+  bf16* out;
+  int32_t* hdr;
+  int32_t* dec_rows;
+  int32_t* dec_item_prefix;
+  int32_t* dec_part_base;
+  int32_t* dec_nsplit;
+  int32_t* ch_rows;
+  int32_t* ch_item_prefix;
+  float* part_ml;
+  float* part_acc;
+  int64_t max_partials;
+  int64_t context_total;
+  int32_t bt_stride, num_rows, num_tokens, num_pages;
+  int32_t H_q, H_kv, D, G;
+  int32_t dec_workers;
+  float scale_log2;
+};
+
+__host__ __device__ inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ----------------------------------------------------------------------------
+// prologue: validate, classify, sort longest-first, lay out work lists
+// ----------------------------------------------------------------------------
+
+// exclusive scan of one int64 per thread over the block; returns the total
+__device__ int64_t block_exclusive_scan(int64_t v, int64_t* s_warp, int64_t& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int64_t t = lane < (blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    s_warp[lane] = t;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int64_t before = (w > 0 ? s_warp[w - 1] : 0) + x - v;
+  total = s_warp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParams p) {
+  __shared__ int64_t s_warp[32];
+  __shared__ int s_bad;
+  __shared__ unsigned long long s_ctx_sum, s_dec_pages;
+  __shared__ int64_t s_key[kSortLimit];
+  __shared__ int32_t s_idx[kSortLimit];
+  const int tid = threadIdx.x;
+  const int S = p.num_rows;
+  int32_t* hdr = p.hdr;
+  if (tid == 0) {
+    s_bad = 0;
+    s_ctx_sum = 0;
+    s_dec_pages = 0;
+  }
+  __syncthreads();
+  // 1. validate rows and count work
+  for (int s = tid; s < S; s += blockDim.x) {
+    const int32_t a = p.cu[s], b = p.cu[s + 1];
+    const int32_t d = b - a, c = p.q_start[s], ctx = p.ctx_lens[s];
+    const bool ok = a >= 0 && b <= p.num_tokens && d >= 1 && c >= 0 && ctx == c + d &&
+                    cdiv64(ctx, kPage) <= p.bt_stride;
+    if (!ok) {
+      atomicOr(&s_bad, 1);
+      continue;
+    }
+    atomicAdd(&s_ctx_sum, static_cast<unsigned long long>(ctx));
+    if (d == 1) atomicAdd(&s_dec_pages, static_cast<unsigned long long>(cdiv64(ctx, kPage)));
+  }
+  __syncthreads();
+  const bool bad = s_bad != 0 || static_cast<int64_t>(s_ctx_sum) > p.context_total;
+  if (bad) {
+    if (tid == 0) {
+      atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
+      hdr[H_DEC_CTR] = hdr[H_CH_CTR] = 0;
+      hdr[H_NDEC] = hdr[H_NDEC_ITEMS] = hdr[H_NCH] = hdr[H_NCH_ITEMS] = hdr[H_NPART] = 0;
+      hdr[H_SPLIT] = kMinSplitPages;
+      p.dec_item_prefix[0] = 0;
+      p.ch_item_prefix[0] = 0;
+    }
+    return;
+  }
+  // 2. split size: about 16 items per decode worker, clamped
+  int64_t split = cdiv64(static_cast<int64_t>(s_dec_pages) * p.H_kv, static_cast<int64_t>(p.dec_workers) * 16);
+  split = split < kMinSplitPages ? kMinSplitPages : (split > kMaxSplitPages ? kMaxSplitPages : split);
+  // 3. stable compaction of decode rows and chunk rows
+  int64_t n_dec = 0, n_ch = 0;
+  for (int base = 0; base < S; base += blockDim.x) {
+    const int s = base + tid;
+    int is_dec = 0, is_ch = 0;
+    if (s < S) {
+      const int d = p.cu[s + 1] - p.cu[s];
+      is_dec = d == 1;
+      is_ch = d > 1;
+    }
+    int64_t tot_dec, tot_ch;
+    const int64_t o_dec = block_exclusive_scan(is_dec, s_warp, tot_dec);
+    const int64_t o_ch = block_exclusive_scan(is_ch, s_warp, tot_ch);
+    if (is_dec) p.dec_rows[n_dec + o_dec] = s;
+    if (is_ch) p.ch_rows[n_ch + o_ch] = s;
+    n_dec += tot_dec;
+    n_ch += tot_ch;
+  }
+  __syncthreads();
+  // 4. longest first (stable): decodes by context, chunks by causal pairs
+  for (int kind = 0; kind < 2; ++kind) {
+    int32_t* rows = kind == 0 ? p.dec_rows : p.ch_rows;
+    const int n = static_cast<int>(kind == 0 ? n_dec : n_ch);
+    if (n <= 1 || n > kSortLimit) continue;
+    for (int i = tid; i < n; i += blockDim.x) {
+      const int s = rows[i];
+      const int64_t c = p.q_start[s], d = p.cu[s + 1] - p.cu[s];
+      const int64_t cost = kind == 0 ? c + 1 : d * (2 * c + d + 1) / 2;
+      s_key[i] = (cost << 16) | (0xffff - (i & 0xffff));  // ties keep input order
+      s_idx[i] = s;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += blockDim.x) {
+      int rank = 0;
+      const int64_t k = s_key[i];
+      for (int j = 0; j < n; ++j) rank += s_key[j] > k;
+      rows[rank] = s_idx[i];
+    }
+    __syncthreads();
+  }
+  // 5. item prefixes and partial bases
+  int64_t dec_items = 0, parts = 0;
+  for (int base = 0; base < n_dec; base += blockDim.x) {
+    const int k = base + tid;
+    int64_t ns = 0;
+    if (k < n_dec) ns = cdiv64(cdiv64(p.ctx_lens[p.dec_rows[k]], kPage), split);
+    int64_t tot;
+    const int64_t o = block_exclusive_scan(ns, s_warp, tot);
+    if (k < n_dec) {
+      p.dec_nsplit[k] = static_cast<int32_t>(ns);
+      p.dec_item_prefix[k] = static_cast<int32_t>((dec_items + o) * p.H_kv);
+      p.dec_part_base[k] = static_cast<int32_t>((parts + o) * p.H_q);
+    }
+    dec_items += tot;
+    parts += tot;
+  }
+  int64_t ch_items = 0;
+  const int tpt = 128 / p.G;
+  for (int base = 0; base < n_ch; base += blockDim.x) {
+    const int k = base + tid;
+    int64_t nq = 0;
+    if (k < n_ch) {
+      const int s = p.ch_rows[k];
+      nq = cdiv64(p.cu[s + 1] - p.cu[s], tpt);
+    }
+    int64_t tot;
+    const int64_t o = block_exclusive_scan(nq, s_warp, tot);
+    if (k < n_ch) p.ch_item_prefix[k] = static_cast<int32_t>((ch_items + o) * p.H_kv);
+    ch_items += tot;
+  }
+  if (tid == 0) {
+    const bool overflow = parts * p.H_q > p.max_partials;
+    p.dec_item_prefix[n_dec] = static_cast<int32_t>(dec_items * p.H_kv);
+    p.ch_item_prefix[n_ch] = static_cast<int32_t>(ch_items * p.H_kv);
+    hdr[H_DEC_CTR] = 0;
+    hdr[H_CH_CTR] = 0;
+    hdr[H_NDEC] = static_cast<int32_t>(n_dec);
+    hdr[H_NDEC_ITEMS] = overflow ? 0 : static_cast<int32_t>(dec_items * p.H_kv);
+    hdr[H_NCH] = static_cast<int32_t>(n_ch);
+    hdr[H_NCH_ITEMS] = static_cast<int32_t>(ch_items * p.H_kv);
+    hdr[H_SPLIT] = static_cast<int32_t>(split);
+    hdr[H_NPART] = static_cast<int32_t>(parts * p.H_q);
+    if (overflow) {
+      atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
+      hdr[H_NDEC] = 0;
+    }
+  }
+}
+
+// index k with prefix[k] <= item < prefix[k + 1]; prefix has n + 1 entries
+__device__ __forceinline__ int find_row(const int32_t* prefix, int n, int item) {
+  int lo = 0, hi = n;  // invariant: prefix[lo] <= item < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(prefix + mid) <= item)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// ----------------------------------------------------------------------------
+// decode rows: split-KV on CUDA cores
+// ----------------------------------------------------------------------------
+
+template <int D, int G>
+struct DecCfg {
+  static constexpr int EPL = D / 16;               // columns per lane of one token row
+  static constexpr int NST = D == 128 ? (G >= 8 ? 2 : 3) : (G >= 8 ? 5 : 6);
+  static constexpr int PAGE_BYTES = kPage * D * 2;  // one page of one KV head
+  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
+  static constexpr int Q_BYTES = G * D * 2;
+  static constexpr int Q_OFF = NST * STAGE_BYTES;
+  static constexpr int P_OFF = Q_OFF + 2 * Q_BYTES;
+  static constexpr int BAR_OFF = P_OFF + G * 16 * 4;
+  static constexpr int WARP_BYTES = (BAR_OFF + NST * 8 + 127) / 128 * 128;
+  static constexpr int SMEM = kDecWarps * WARP_BYTES;
+};
+
+
+struct DecItem {
+  int row;     // row index s
+  int k;       // index among decode rows
+  int hk;      // KV head
+  int p0, np;  // logical pages [p0, p0 + np)
+  int ctx;     // keys of the row (c + 1)
+  int tok;     // packed token index of the row's query
+  int part;    // partial record of query head hk * G (+ g for the others)
+};
+
+__device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, int n_dec, int split) {
+  DecItem it;
+  const int k = find_row(p.dec_item_prefix, n_dec, item);
+  const int local = item - __ldg(p.dec_item_prefix + k);
+  const int sp = local / p.H_kv;
+  it.hk = local - sp * p.H_kv;
+  it.k = k;
+  it.row = __ldg(p.dec_rows + k);
+  it.ctx = __ldg(p.ctx_lens + it.row);
+  it.tok = __ldg(p.cu + it.row);
+  const int n_pages = (it.ctx + kPage - 1) / kPage;
+  it.p0 = sp * split;
+  it.np = min(split, n_pages - it.p0);
+  it.part = __ldg(p.dec_part_base + k) + sp * p.H_q + it.hk * p.G;
+  return it;
+}
+
+// load EPL bf16 columns of one token row from shared memory as fp32
+template <int EPL>
+__device__ __forceinline__ void lds_row(const bf16* src, float (&f)[EPL]) {
+  if constexpr (EPL == 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
+    const float2 a = bf2_to_f2(u.x), b = bf2_to_f2(u.y), c = bf2_to_f2(u.z), d = bf2_to_f2(u.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    const float2 a = bf2_to_f2(u.x), b = bf2_to_f2(u.y);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(AttnParams p) {
+  using C = DecCfg<D, G>;
+  constexpr int EPL = C::EPL, NST = C::NST;
+  extern __shared__ __align__(128) uint8_t dsmem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint8_t* wbase = dsmem + warp * C::WARP_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(wbase + C::BAR_OFF);
+  float* pbuf = reinterpret_cast<float*>(wbase + C::P_OFF);  // [G][2 halves][8]
+  const int n_items = p.hdr[H_NDEC_ITEMS];
+  const int n_dec = p.hdr[H_NDEC];
+  const int split = p.hdr[H_SPLIT];
+  if (lane == 0) {
+    for (int i = 0; i < NST; ++i) mbar_init(full + i, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const int h = lane >> 4, sub = lane & 15;  // token parity of this lane, column chunk
+  const int64_t head_stride = static_cast<int64_t>(kPage) * D;
+
+  auto dequeue = [&]() -> int {
+    int v = 0;
+    if (lane == 0) v = atomicAdd(p.hdr + H_DEC_CTR, 1);
+    return __shfl_sync(0xffffffffu, v, 0);
+  };
+
+  // issue stream: pages of `cur`, then of `nxt` (one item ahead at most)
+  DecItem cur, nxt;
+  int cur_id = dequeue();
+  if (cur_id >= n_items) return;
+  cur = describe_dec(p, cur_id, n_dec, split);
+  int nxt_id = dequeue();
+  bool nxt_valid = nxt_id < n_items;
+  if (nxt_valid) nxt = describe_dec(p, nxt_id, n_dec, split);
+  uint32_t seq_iss = 0, seq_con = 0;
+  int iss_in_nxt = 0, iss_page = 0;
+  uint32_t item_par = 0;  // q buffer of the current item
+  bool failed = false;
+
+  auto issue_page = [&](const DecItem& it, int pi, uint32_t qpar) {
+    if (lane == 0) {
+      const int st = seq_iss % NST;
+      uint8_t* stage = wbase + st * C::STAGE_BYTES;
+      int phys = __ldg(p.bt + static_cast<int64_t>(it.row) * p.bt_stride + it.p0 + pi);
+      if (phys < 0 || phys >= p.num_pages) {
+        atomicOr(p.hdr + H_STATUS, MS_STATUS_BAD_PAGE);
+        phys = 0;
+      }
+      const int64_t off = (static_cast<int64_t>(phys) * p.H_kv + it.hk) * head_stride;
+      const uint32_t bytes = 2 * C::PAGE_BYTES + (pi == 0 ? C::Q_BYTES : 0);
+      mbar_arrive_expect_tx(full + st, bytes);
+      bulk_g2s(stage, p.k_cache + off, C::PAGE_BYTES, full + st);
+      bulk_g2s(stage + C::PAGE_BYTES, p.v_cache + off, C::PAGE_BYTES, full + st);
+      if (pi == 0)
+        bulk_g2s(wbase + C::Q_OFF + qpar * C::Q_BYTES,
+                 p.q_rot + (static_cast<int64_t>(it.tok) * p.H_q + it.hk * G) * D, C::Q_BYTES, full + st);
+    }
+    ++seq_iss;
+  };
+  auto pump = [&]() {
+    while (seq_iss - seq_con < static_cast<uint32_t>(NST)) {
+      if (!iss_in_nxt) {
+        if (iss_page < cur.np) {
+          issue_page(cur, iss_page++, item_par);
+          continue;
+        }
+        iss_in_nxt = 1;
+        iss_page = 0;
+      }
+      if (!nxt_valid || iss_page >= nxt.np) break;
+      issue_page(nxt, iss_page++, item_par ^ 1u);
+    }
+  };
+  pump();
+
+  while (true) {
+    float q[G][EPL], acc[G][EPL], m[G], l[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
+    }
+    for (int pi = 0; pi < cur.np; ++pi) {
+      const int st = seq_con % NST;
+      if (!mbar_wait(full + st, (seq_con / NST) & 1u, nullptr)) {
+        failed = true;
+        break;
+      }
+      const bf16* Ks = reinterpret_cast<const bf16*>(wbase + st * C::STAGE_BYTES);
+      const bf16* Vs = Ks + kPage * D;
+      if (pi == 0) {
+        const bf16* qs = reinterpret_cast<const bf16*>(wbase + C::Q_OFF + item_par * C::Q_BYTES);
+#pragma unroll
+        for (int g = 0; g < G; ++g) lds_row<EPL>(qs + g * D + sub * EPL, q[g]);
+      }
+      const int tok0 = (cur.p0 + pi) * kPage;
+      const int nv = min(kPage, cur.ctx - tok0);  // valid keys in this page (>= 1)
+      float kf[8][EPL];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) lds_row<EPL>(Ks + (2 * i + h) * D + sub * EPL, kf[i]);
+      float alpha[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float part[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float s = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) s = fmaf(q[g][e], kf[i][e], s);
+          part[i] = s;
+        }
+        // reduce-scatter over the 16 lanes of this half: lane ends with token i = sub >> 1
+        const bool b3 = sub & 8, b2 = sub & 4, b1 = sub & 2;
+        float w4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float send = b3 ? part[j] : part[j + 4];
+          const float keep = b3 ? part[j + 4] : part[j];
+          w4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        float w2[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float send = b2 ? w4[j] : w4[j + 2];
+          const float keep = b2 ? w4[j + 2] : w4[j];
+          w2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        float y = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
+        y += __shfl_xor_sync(0xffffffffu, y, 1);
+        const int ti = sub >> 1;  // this lane's token: 2 * ti + h
+        const float s = (2 * ti + h < nv) ? y * p.scale_log2 : -INFINITY;
+        float mx = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(m[g], mx);
+        alpha[g] = ex2(m[g] - m_new);
+        const float pr = ex2(s - m_new);
+        l[g] = l[g] * alpha[g] + ((lane & 1) ? 0.f : pr);
+        m[g] = m_new;
+        if ((lane & 1) == 0) pbuf[(g * 2 + h) * 8 + ti] = pr;
+      }
+      __syncwarp();
+      float vf[8][EPL];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        lds_row<EPL>(Vs + (2 * i + h) * D + sub * EPL, vf[i]);
+        if (2 * i + h >= nv) {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) vf[i][e] = 0.f;  // keys past the context may hold stale data
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float4 pa = *reinterpret_cast<const float4*>(pbuf + (g * 2 + h) * 8);
+        const float4 pb = *reinterpret_cast<const float4*>(pbuf + (g * 2 + h) * 8 + 4);
+        const float pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          float a = acc[g][e] * alpha[g];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a = fmaf(pw[i], vf[i][e], a);
+          acc[g][e] = a;
+        }
+      }
+      __syncwarp();
+      ++seq_con;
+      pump();
+    }
+    if (failed) break;
+    // partial record of each query head: (max, sum) and the unnormalised accumulator
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float lt = l[g];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+      float a[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) a[e] = acc[g][e] + __shfl_xor_sync(0xffffffffu, acc[g][e], 16);
+      const int64_t rec = cur.part + g;
+      if (h == 0) {
+        float* dst = p.part_acc + rec * D + sub * EPL;
+        if constexpr (EPL == 8) {
+          *reinterpret_cast<float4*>(dst) = make_float4(a[0], a[1], a[2], a[3]);
+          *reinterpret_cast<float4*>(dst + 4) = make_float4(a[4], a[5], a[6], a[7]);
+        } else {
+          *reinterpret_cast<float4*>(dst) = make_float4(a[0], a[1], a[2], a[3]);
+        }
+      }
+      if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + rec * 2) = make_float2(m[g], lt);
+    }
+    if (!nxt_valid) break;
+    // advance: the next item becomes current; dequeue one more
+    cur = nxt;
+    item_par ^= 1u;
+    iss_in_nxt = 0;  // the issue cursor (iss_page) already points into the new current item
+    nxt_id = dequeue();
+    nxt_valid = nxt_id < n_items;
+    if (nxt_valid) nxt = describe_dec(p, nxt_id, n_dec, split);
+    pump();
+  }
+  if (failed) {
+    if (lane == 0) atomicOr(p.hdr + H_STATUS, MS_STATUS_TIMEOUT);
+    // let copies already in flight land before the CTA's shared memory is released
+    while (seq_con < seq_iss) {
+      mbar_wait(full + seq_con % NST, (seq_con / NST) & 1u, nullptr, 200000000ull);
+      ++seq_con;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// split combine for decode rows
+// ----------------------------------------------------------------------------
+
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
+  constexpr int EPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int n_dec = p.hdr[H_NDEC];
+  if (gw >= n_dec * p.H_q) return;
+  const int k = gw / p.H_q, hq = gw - k * p.H_q;
+  const int row = p.dec_rows[k];
+  const int ns = p.dec_nsplit[k];
+  const int64_t base = p.dec_part_base[k] + hq;
+  float M = -INFINITY;
+  for (int j = 0; j < ns; ++j) M = fmaxf(M, p.part_ml[(base + static_cast<int64_t>(j) * p.H_q) * 2]);
+  float L = 0.f, o[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+  for (int j = 0; j < ns; ++j) {
+    const int64_t rec = base + static_cast<int64_t>(j) * p.H_q;
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + rec * 2);
+    const float w = ex2(ml.x - M);
+    L += w * ml.y;
+    const float* src = p.part_acc + rec * D + lane * EPL;
+    if constexpr (EPL == 4) {
+      const float4 a = *reinterpret_cast<const float4*>(src);
+      o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
+    } else {
+      const float2 a = *reinterpret_cast<const float2*>(src);
+      o[0] += w * a.x; o[1] += w * a.y;
+    }
+  }
+  const float inv = 1.f / L;
+  bf16* dst = p.out + (static_cast<int64_t>(p.cu[row]) * p.H_q + hq) * D + lane * EPL;
+  if constexpr (EPL == 4) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(o[0] * inv, o[1] * inv);
+    __nv_bfloat162 b = __floats2bfloat162_rn(o[2] * inv, o[3] * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = u;
+  } else {
+    __nv_bfloat162 a = __floats2bfloat162_rn(o[0] * inv, o[1] * inv);
+    *reinterpret_cast<__nv_bfloat162*>(dst) = a;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// chunk rows: tcgen05 tensor cores, TMEM accumulators, TMA-staged pages
+// ----------------------------------------------------------------------------
+
+constexpr int kSlab = 128 * 128;  // bytes of one 128-row x 64-column bf16 slab (128-byte rows)
+
+template <int D>
+struct ChCfg {
+  static constexpr int NSL = D / 64;                 // 64-column slabs per row
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = NSL * kSlab;         // stage b: K at KV_OFF + b*2*NSL*kSlab, V after K
+  static constexpr int P_OFF = KV_OFF + 4 * NSL * kSlab;
+  static constexpr int BAR_OFF = P_OFF + 4 * kSlab;  // two P buffers of 128 rows x 128 keys
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int TMEM_COLS = 512;              // S0, S1 (128 each), O (D)
+};
+
+struct ChItem {
+  int row, tb, d, c, tok0, ntok, hk, kv_end, n_kt, tile0;  // tile0: CTA-global index of its first KV tile
+};
+
+struct ChBars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t item_full[2], item_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem;
+  int abort;
+  ChItem items[2];
+};
+
+// K-major, 128-byte-swizzled operand: slab-major 64-column blocks of 128-byte rows;
+// k-step kk (16 columns) lives in slab kk / 4 at byte offset (kk % 4) * 32.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
+  return smem_desc_sw128(base + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+}
+
+// wait by lane 0, result and ordering shared with the whole warp
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kChunkThreads, 1)
+    chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, AttnParams p) {
+  using C = ChCfg<D>;
+  constexpr int NSL = C::NSL;
+  constexpr int TPT = 128 / G;  // query tokens per 128-row tile
+  extern __shared__ uint8_t csmem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(csmem_raw) + 1023) & ~uintptr_t(1023));
+  ChBars* bars = reinterpret_cast<ChBars*>(smem + C::BAR_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.hdr[H_NCH_ITEMS];
+  if (n_items == 0) return;
+  const int n_ch = p.hdr[H_NCH];
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + C::Q_OFF;
+  auto kv_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kSlab; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->kv_full[b], 1);
+      mbar_init(&bars->kv_empty[b], 1);
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 128);
+      mbar_init(&bars->o_done[b], 1);
+      mbar_init(&bars->item_full[b], 1);
+      mbar_init(&bars->item_empty[b], 1 + 128);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  const uint32_t tS0 = tmem, tO = tmem + 256;
+  volatile int* abort_flag = &bars->abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer + work queue
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      int g = 0;       // CTA-global KV tile counter
+      int n_done = 0;  // items taken by this CTA
+      bool ok = true;
+      while (ok) {
+        const int item = atomicAdd(p.hdr + H_CH_CTR, 1);
+        const int slot = n_done & 1;
+        if (n_done >= 2 && !mbar_wait(&bars->item_empty[slot], ((n_done >> 1) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ChItem it;
+        it.row = -1;
+        if (item < n_items) {
+          const int k = find_row(p.ch_item_prefix, n_ch, item);
+          const int local = item - __ldg(p.ch_item_prefix + k);
+          it.row = __ldg(p.ch_rows + k);
+          it.tb = __ldg(p.cu + it.row);
+          it.d = __ldg(p.cu + it.row + 1) - it.tb;
+          it.c = __ldg(p.q_start + it.row);
+          const int n_qt = (it.d + TPT - 1) / TPT;
+          const int qt = n_qt - 1 - local / p.H_kv;  // later tiles see more keys: run them first
+          it.hk = local % p.H_kv;
+          it.tok0 = qt * TPT;
+          it.ntok = min(TPT, it.d - it.tok0);
+          it.kv_end = it.c + it.tok0 + it.ntok;
+          it.n_kt = (it.kv_end + 127) / 128;
+          it.tile0 = g;
+        }
+        bars->items[slot] = it;
+        mbar_arrive(&bars->item_full[slot]);
+        ++n_done;
+        if (it.row < 0) break;
+        // Q tile: previous item's S MMAs must be done with it
+        if (n_done >= 2 && !mbar_wait(&bars->q_empty, (n_done - 2) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->q_full, 128 * D * 2);
+        for (int s = 0; s < NSL; ++s)
+          tma_load_3d(smem + C::Q_OFF + s * kSlab, &tm_q, s * 64, it.hk * G, it.tb + it.tok0, &bars->q_full);
+        const int32_t* btrow = p.bt + static_cast<int64_t>(it.row) * p.bt_stride;
+        for (int kt = 0; kt < it.n_kt; ++kt, ++g) {
+          const int b = g & 1;
+          if (g >= 2 && !mbar_wait(&bars->kv_empty[b], ((g >> 1) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int keys = min(128, it.kv_end - kt * 128);
+          const int npg = (keys + kPage - 1) / kPage;
+          mbar_arrive_expect_tx(&bars->kv_full[b], 2 * npg * kPage * D * 2);
+          for (int pg = 0; pg < npg; ++pg) {
+            int phys = __ldg(btrow + kt * 8 + pg);
+            if (phys < 0 || phys >= p.num_pages) {
+              atomicOr(p.hdr + H_STATUS, MS_STATUS_BAD_PAGE);
+              phys = 0;
+            }
+            const int r0 = (phys * p.H_kv + it.hk) * kPage;
+            for (int s = 0; s < NSL; ++s) {
+              tma_load_2d(smem + kv_off(b) + s * kSlab + pg * 2048, &tm_k, s * 64, r0, &bars->kv_full[b]);
+              tma_load_2d(smem + kv_off(b) + (NSL + s) * kSlab + pg * 2048, &tm_v, s * 64, r0, &bars->kv_full[b]);
+            }
+          }
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      // copies still in flight must land before the CTA exits
+      for (int t = (g > 2 ? g - 2 : 0); t < g; ++t)
+        mbar_wait(&bars->kv_full[t & 1], (t >> 1) & 1, nullptr, 200000000ull);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
+      bool ok = true;
+      for (int n = 0; ok; ++n) {
+        const int slot = n & 1;
+        if (!mbar_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const ChItem it = bars->items[slot];
+        if (it.row < 0) break;
+        if (!mbar_wait(&bars->q_full, n & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        for (int kt = 0; kt <= it.n_kt; ++kt) {
+          if (kt < it.n_kt) {
+            const int g = it.tile0 + kt, b = g & 1;
+            if (!mbar_wait(&bars->kv_full[b], (g >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int keys = min(128, it.kv_end - kt * 128);
+            const int n_cols = (keys + 15) & ~15;
+            if (keys != n_cols) {
+              // rows past the context in the last page may hold stale (even non-finite)
+              // data: zero them in V so that P = 0 times V stays 0
+              uint8_t* v0 = smem + kv_off(b) + NSL * kSlab;
+              for (int r = keys; r < n_cols; ++r)
+                for (int s = 0; s < NSL; ++s)
+                  for (int q16 = 0; q16 < 8; ++q16)
+                    *reinterpret_cast<uint4*>(v0 + s * kSlab + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+              fence_proxy_async_smem();
+            }
+            const uint32_t idesc_s = idesc_bf16_f32(128, n_cols, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_bf16_ss(tS0 + b * 128, kmajor_desc(sQ, kk), kmajor_desc(sbase + kv_off(b), kk), idesc_s,
+                          kk > 0 ? 1u : 0u);
+            mma_commit(&bars->s_full[b]);
+            if (kt == it.n_kt - 1) mma_commit(&bars->q_empty);
+          }
+          if (kt >= 1) {
+            const int j = kt - 1, gj = it.tile0 + j, bj = gj & 1;
+            if (!mbar_wait(&bars->p_full[bj], (gj >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int keys = min(128, it.kv_end - j * 128);
+            const int nk = (keys + 15) >> 4;
+            const uint32_t vbase = sbase + kv_off(bj) + NSL * kSlab;
+            for (int kk = 0; kk < nk; ++kk) {
+              // V is the MN-major B operand: 64-column slabs one slab apart (LBO),
+              // 8-key row groups 1024 B apart (SBO), 16 keys = 2048 B per k-step
+              const uint64_t vdesc = smem_desc_sw128(vbase + kk * 2048, kSlab, 1024);
+              mma_bf16_ss(tO, kmajor_desc(sbase + C::P_OFF + bj * 2 * kSlab, kk), vdesc, idesc_pv,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->o_done[bj]);
+            mma_commit(&bars->kv_empty[bj]);
+          }
+        }
+        if (!ok) break;
+        mbar_arrive(&bars->item_empty[slot]);
+      }
+      if (!ok) *abort_flag = 1;
+      // every MMA this thread issued must finish before TMEM is released
+      mma_commit(&bars->mma_done);
+      mbar_wait(&bars->mma_done, 0, nullptr, 200000000ull);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax: one query row per thread
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int slot = n & 1;
+      if (!warp_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const ChItem it = bars->items[slot];
+      if (it.row < 0) break;
+      const int tl = it.tok0 + r / G;  // token of this row within the chunk
+      const bool valid = (r / G) < it.ntok;
+      const int pos = it.c + (valid ? tl : it.tok0 + it.ntok - 1);
+      float m = -INFINITY, l = 0.f;
+      for (int kt = 0; kt < it.n_kt; ++kt) {
+        const int g = it.tile0 + kt, b = g & 1;
+        if (!warp_wait(&bars->s_full[b], (g >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[128];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(tS0 + b * 128 + lane_off + cc * 32, rr);
+          tmem_wait_ld();
+          reg_fence32(rr);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sv[cc * 32 + j] = __uint_as_float(rr[j]);
+        }
+        const int key0 = kt * 128;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+          const float x = (key0 + j <= pos) ? sv[j] * p.scale_log2 : -INFINITY;
+          sv[j] = x;
+          mx = fmaxf(mx, x);
+        }
+        const float m_new = fmaxf(m, mx);
+        const float alpha = ex2(m - m_new);
+        float rs = 0.f;
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+          const float e = ex2(sv[j] - m_new);
+          sv[j] = e;
+          rs += e;
+        }
+        l = l * alpha + rs;
+        m = m_new;
+        // rescale the running O when a row's max grew (TMEM access is warp-wide)
+        if (kt > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+          if (!warp_wait(&bars->o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t rr[32];
+            tmem_ld32(tO + lane_off + cc * 32, rr);
+            tmem_wait_ld();
+            reg_fence32(rr);
+            float o[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(rr[j]) * alpha;
+            tmem_st32(tO + lane_off + cc * 32, o);
+          }
+          tmem_wait_st();
+        }
+        // P buffer b was last read by the PV MMA of tile g - 2
+        if (g >= 2 && !warp_wait(&bars->o_done[b], ((g - 2) >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* prow = smem + C::P_OFF + b * 2 * kSlab + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          __nv_bfloat162 h0 = __floats2bfloat162_rn(sv[cc * 8 + 0], sv[cc * 8 + 1]);
+          __nv_bfloat162 h1 = __floats2bfloat162_rn(sv[cc * 8 + 2], sv[cc * 8 + 3]);
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[cc * 8 + 4], sv[cc * 8 + 5]);
+          __nv_bfloat162 h3 = __floats2bfloat162_rn(sv[cc * 8 + 6], sv[cc * 8 + 7]);
+          uint4 u;
+          u.x = *reinterpret_cast<uint32_t*>(&h0);
+          u.y = *reinterpret_cast<uint32_t*>(&h1);
+          u.z = *reinterpret_cast<uint32_t*>(&h2);
+          u.w = *reinterpret_cast<uint32_t*>(&h3);
+          const int slab = cc >> 3, chunk = (cc & 7) ^ (r & 7);
+          *reinterpret_cast<uint4*>(prow + slab * kSlab + chunk * 16) = u;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[b]);
+      }
+      if (!ok) break;
+      const int gl = it.tile0 + it.n_kt - 1;
+      if (!warp_wait(&bars->o_done[gl & 1], (gl >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float inv = 1.f / l;
+      bf16* dst = p.out + (static_cast<int64_t>(it.tb + tl) * p.H_q + it.hk * G + r % G) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tO + lane_off + cc * 32, rr);
+        tmem_wait_ld();
+        reg_fence32(rr);
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 u;
+            __nv_bfloat162 h0 =
+                __floats2bfloat162_rn(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv);
+            __nv_bfloat162 h1 =
+                __floats2bfloat162_rn(__uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
+            __nv_bfloat162 h2 =
+                __floats2bfloat162_rn(__uint_as_float(rr[j + 4]) * inv, __uint_as_float(rr[j + 5]) * inv);
+            __nv_bfloat162 h3 =
+                __floats2bfloat162_rn(__uint_as_float(rr[j + 6]) * inv, __uint_as_float(rr[j + 7]) * inv);
+            u.x = *reinterpret_cast<uint32_t*>(&h0);
+            u.y = *reinterpret_cast<uint32_t*>(&h1);
+            u.z = *reinterpret_cast<uint32_t*>(&h2);
+            u.w = *reinterpret_cast<uint32_t*>(&h3);
+            *reinterpret_cast<uint4*>(dst + cc * 32 + j) = u;
+          }
+        }
+      }
+      // O has been read: the next item's first PV may overwrite it
+      tc_fence_before();
+      mbar_arrive(&bars->item_empty[slot]);
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      if (lane == 0) atomicOr(p.hdr + H_STATUS, MS_STATUS_TIMEOUT);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+
+namespace {
+
+struct WsLayout {
+  size_t hdr, dec_rows, dec_item_prefix, dec_part_base, dec_nsplit, ch_rows, ch_item_prefix, part_ml, part_acc,
+      total;
+  int64_t max_partials;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WsLayout ws_layout(int64_t max_rows, int64_t max_context_total, int64_t H_q, int64_t D) {
+  WsLayout w;
+  size_t off = 0;
+  w.hdr = off;
+  off += H_WORDS * 4;
+  w.dec_rows = off;
+  off = align_up(off + max_rows * 4, 16);
+  w.dec_item_prefix = off;
+  off = align_up(off + (max_rows + 1) * 4, 16);
+  w.dec_part_base = off;
+  off = align_up(off + max_rows * 4, 16);
+  w.dec_nsplit = off;
+  off = align_up(off + max_rows * 4, 16);
+  w.ch_rows = off;
+  off = align_up(off + max_rows * 4, 16);
+  w.ch_item_prefix = off;
+  off = align_up(off + (max_rows + 1) * 4, 256);
+  // every decode split covers >= kMinSplitPages pages: sum of splits <= ctx/256 + rows/16 + rows
+  w.max_partials = H_q * (cdiv64(max_context_total, kPage * kMinSplitPages) + 2 * max_rows);
+  w.part_ml = off;
+  off = align_up(off + w.max_partials * 2 * 4, 256);
+  w.part_acc = off;
+  off = align_up(off + w.max_partials * D * 4, 256);
+  w.total = off;
+  return w;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+bool encode_bf16(EncodeTiledFn fn, CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                 const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_num_sms = 0;
+
+int num_sms() {
+  if (g_num_sms > 0) return g_num_sms;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  g_num_sms = n;
+  return n;
+}
+
+template <int D, int G>
+int launch_paths(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                 int n_chunk_ctas, int n_dec_ctas, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecCfg<D, G>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(chunk_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, ChCfg<D>::SMEM) !=
+            cudaSuccess)
+      return MS_ERR_CUDA;
+    configured = true;
+  }
+  if (n_chunk_ctas > 0) chunk_kernel<D, G><<<n_chunk_ctas, kChunkThreads, ChCfg<D>::SMEM, st>>>(tq, tk, tv, p);
+  if (n_dec_ctas > 0) decode_kernel<D, G><<<n_dec_ctas, kDecThreads, DecCfg<D, G>::SMEM, st>>>(p);
+  const int64_t warps = static_cast<int64_t>(p.num_rows) * p.H_q;
+  if (warps > 0) combine_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? MS_OK : MS_ERR_CUDA;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" MS_API size_t ms_attention_workspace_size(int32_t max_rows, int32_t max_tokens, int64_t max_context_total,
+                                                     int32_t H_q, int32_t H_kv, int32_t D) {
+  (void)max_tokens;
+  (void)H_kv;
+  if (max_rows < 0 || max_context_total < 0 || H_q < 1 || (D != 64 && D != 128)) return 0;
+  return ws_layout(max_rows, max_context_total, H_q, D).total;
+}
+
+extern "C" MS_API int ms_num_sms(void) {
+  const int n = num_sms();
+  return n > 0 ? n : MS_ERR_CUDA;
+}
+
+extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_cache, const void* v_cache,
+                                              int32_t num_pages, const int32_t* cu_seqlens_q,
+                                              const int32_t* q_start_pos, const int32_t* context_lens,
+                                              const int32_t* block_tables, int32_t bt_stride, int32_t num_rows,
+                                              int32_t num_tokens, int64_t context_total, int32_t H_q, int32_t H_kv,
+                                              int32_t D, int32_t page_size, float scale, void* out, void* workspace,
+                                              size_t ws_bytes, ms_stream_t stream) {
+  if (num_rows < 0 || num_tokens < 0 || context_total < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 ||
+      (D != 64 && D != 128) || page_size != kPage || bt_stride < 0 || num_pages < 0 || !(scale > 0.f))
+    return MS_ERR_ARG;
+  const int G = H_q / H_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return MS_ERR_ARG;
+  if (num_rows == 0) return MS_OK;
+  if (!q_rot || !k_cache || !v_cache || !cu_seqlens_q || !q_start_pos || !context_lens || !block_tables || !out ||
+      !workspace || num_pages < 1 || num_tokens < num_rows || bt_stride < 1)
+    return MS_ERR_ARG;
+  if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MS_ERR_ARG;
+  const WsLayout w = ws_layout(num_rows, context_total, H_q, D);
+  if (ws_bytes < w.total) return MS_ERR_ARG;
+  const int sms = num_sms();
+  if (sms <= 0) return MS_ERR_CUDA;
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return MS_ERR_CUDA;
+
+  CUtensorMap tq, tk, tv;
+  {
+    const cuuint64_t dq[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_q),
+                              static_cast<cuuint64_t>(num_tokens)};
+    const cuuint64_t sq[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H_q) * D * 2};
+    const cuuint32_t bq[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+    const cuuint64_t dk[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_pages) * H_kv * kPage};
+    const cuuint64_t sk[1] = {static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t bk[2] = {64, static_cast<cuuint32_t>(kPage)};
+    if (!encode_bf16(enc, &tq, q_rot, 3, dq, sq, bq) || !encode_bf16(enc, &tk, k_cache, 2, dk, sk, bk) ||
+        !encode_bf16(enc, &tv, v_cache, 2, dk, sk, bk))
+      return MS_ERR_ARG;
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  AttnParams p;
+  p.q_rot = static_cast<const bf16*>(q_rot);
+  p.k_cache = static_cast<const bf16*>(k_cache);
+  p.v_cache = static_cast<const bf16*>(v_cache);
+  p.cu = cu_seqlens_q;
+  p.q_start = q_start_pos;
+  p.ctx_lens = context_lens;
+  p.bt = block_tables;
+  p.out = static_cast<bf16*>(out);
+  p.hdr = reinterpret_cast<int32_t*>(ws + w.hdr);
+  p.dec_rows = reinterpret_cast<int32_t*>(ws + w.dec_rows);
+  p.dec_item_prefix = reinterpret_cast<int32_t*>(ws + w.dec_item_prefix);
+  p.dec_part_base = reinterpret_cast<int32_t*>(ws + w.dec_part_base);
+  p.dec_nsplit = reinterpret_cast<int32_t*>(ws + w.dec_nsplit);
+  p.ch_rows = reinterpret_cast<int32_t*>(ws + w.ch_rows);
+  p.ch_item_prefix = reinterpret_cast<int32_t*>(ws + w.ch_item_prefix);
+  p.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
+  p.part_acc = reinterpret_cast<float*>(ws + w.part_acc);
+  p.max_partials = w.max_partials;
+  p.context_total = context_total;
+  p.bt_stride = bt_stride;
+  p.num_rows = num_rows;
+  p.num_tokens = num_tokens;
+  p.num_pages = num_pages;
+  p.H_q = H_q;
+  p.H_kv = H_kv;
+  p.D = D;
+  p.G = G;
+  p.dec_workers = sms * kDecWarps;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  prologue_kernel<<<1, kPrologueThreads, 0, st>>>(p);
+  // chunk work: at most one persistent CTA per SM, and no more than the tiles there can be
+  const int64_t tpt = 128 / G;
+  const int64_t max_chunk_items = (cdiv64(num_tokens, tpt) + num_rows) * H_kv;
+  const int n_chunk_ctas = static_cast<int>(max_chunk_items < sms ? max_chunk_items : sms);
+  const int n_dec_ctas = sms;
+  int rc = MS_ERR_ARG;
+  switch (D * 100 + G) {
+    case 6401: rc = launch_paths<64, 1>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
+    case 6402: rc = launch_paths<64, 2>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
+    case 6404: rc = launch_paths<64, 4>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
+    case 6408: rc = launch_paths<64, 8>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
+    case 12801: rc = launch_paths<128, 1>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
+    case 12802: rc = launch_paths<128, 2>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
+    case 12804: rc = launch_paths<128, 4>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
+    case 12808: rc = launch_paths<128, 8>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
+    default: break;
+  }
+  return rc;
+}
+
+extern "C" MS_API int ms_read_status(int32_t* dev_status, ms_stream_t stream, int32_t* host_status) {
+  if (dev_status == nullptr || host_status == nullptr) return MS_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MS_ERR_CUDA;
+  if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return MS_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MS_ERR_CUDA;
+  *host_status = v;
+  return v == 0 ? MS_OK : MS_ERR_DEVICE;
+}

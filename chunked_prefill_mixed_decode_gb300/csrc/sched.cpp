@@ -1,0 +1,131 @@
+// Host side of the mixed step: decode-first token-budget packing, varlen
+// metadata, and the rotary cos/sin table.
+//
+// Packing follows "Chunked Prefill 的 Token 预算" (zwjcode.cn), sections 03-05
+// and 08, and "Chunked Prefill: Ending the Great Stall", sections 03-04: every
+// running decode is placed first at one token each; then prompts are visited
+// in arrival order and each takes the largest chunk that fits what is left
+// (optionally capped per request, as in "Prefill head-of-line blocking",
+// "The fix").  The metadata is the zwjcode page's section 06 list: absolute
+// positions, one physical slot per new token, the block table, and the
+// context length after the round.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "mixed_step.h"
+
+namespace {
+
+constexpr int32_t kPage = 16;
+
+inline int32_t ceil_div(int64_t a, int64_t b) { return static_cast<int32_t>((a + b - 1) / b); }
+
+struct Row {
+  int32_t req;
+  int32_t c;
+  int32_t d;
+};
+
+}  // namespace
+
+extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_req, const ms_sched_config* cfg,
+                                              int32_t cap_rows, int32_t cap_tokens, int64_t cap_bt,
+                                              int32_t* cu_seqlens_q, int32_t* q_start_pos,
+                                              int32_t* context_lens, int32_t* positions, int32_t* slot_mapping,
+                                              int32_t* block_tables, int32_t* row_req, int32_t* num_scheduled,
+                                              ms_batch_info* info) {
+  if (n_req < 0 || cfg == nullptr || info == nullptr || cu_seqlens_q == nullptr || q_start_pos == nullptr ||
+      context_lens == nullptr || row_req == nullptr || (n_req > 0 && (reqs == nullptr || num_scheduled == nullptr)))
+    return MS_ERR_ARG;
+  const int32_t budget = cfg->token_budget;
+  const int32_t cap = cfg->max_chunk_per_request;
+  if (budget < 0 || cap < 0) return MS_ERR_ARG;
+  for (int32_t i = 0; i < n_req; ++i) {
+    if (reqs[i].cached_len < 0 || reqs[i].remaining_prompt < 0 || reqs[i].num_pages < 0 ||
+        (reqs[i].num_pages > 0 && reqs[i].block_table == nullptr))
+      return MS_ERR_ARG;
+  }
+
+  // 1. running decodes first, one token each, in input order
+  std::vector<Row> rows;
+  rows.reserve(static_cast<size_t>(n_req));
+  int32_t used = 0;
+  for (int32_t i = 0; i < n_req; ++i)
+    if (reqs[i].remaining_prompt == 0) rows.push_back({i, reqs[i].cached_len, 1});
+  const int32_t num_decodes = static_cast<int32_t>(rows.size());
+  if (num_decodes > budget) return MS_ERR_BUDGET;
+  used = num_decodes;
+
+  // 2. prompts in arrival order fill the leftover budget
+  for (int32_t i = 0; i < n_req; ++i) {
+    if (reqs[i].remaining_prompt == 0) continue;
+    const int32_t leftover = budget - used;
+    if (leftover == 0) break;
+    int32_t take = reqs[i].remaining_prompt < leftover ? reqs[i].remaining_prompt : leftover;
+    if (cap > 0 && take > cap) take = cap;
+    if (take > 0) {
+      rows.push_back({i, reqs[i].cached_len, take});
+      used += take;
+    }
+  }
+
+  // 3. capacities and page coverage
+  const int32_t S = static_cast<int32_t>(rows.size());
+  int32_t stride = 0;
+  for (const Row& r : rows) {
+    const int64_t ctx = static_cast<int64_t>(r.c) + r.d;
+    if (ctx > INT32_MAX) return MS_ERR_ARG;
+    const int32_t need = ceil_div(ctx, kPage);
+    if (reqs[r.req].num_pages < need) return MS_ERR_NO_PAGES;
+    if (need > stride) stride = need;
+  }
+  if (S > cap_rows || used > cap_tokens || static_cast<int64_t>(S) * stride > cap_bt) return MS_ERR_ARG;
+  if (used > 0 && (positions == nullptr || slot_mapping == nullptr)) return MS_ERR_ARG;
+  if (static_cast<int64_t>(S) * stride > 0 && block_tables == nullptr) return MS_ERR_ARG;
+
+  // 4. metadata
+  for (int32_t i = 0; i < n_req; ++i) num_scheduled[i] = 0;
+  cu_seqlens_q[0] = 0;
+  int32_t t = 0;
+  for (int32_t s = 0; s < S; ++s) {
+    const Row& r = rows[s];
+    const int32_t* bt = reqs[r.req].block_table;
+    cu_seqlens_q[s + 1] = cu_seqlens_q[s] + r.d;
+    q_start_pos[s] = r.c;
+    context_lens[s] = r.c + r.d;
+    row_req[s] = r.req;
+    num_scheduled[r.req] = r.d;
+    for (int32_t j = 0; j < r.d; ++j, ++t) {
+      const int32_t pos = r.c + j;
+      positions[t] = pos;
+      slot_mapping[t] = bt[pos / kPage] * kPage + pos % kPage;
+    }
+    const int32_t need = ceil_div(static_cast<int64_t>(r.c) + r.d, kPage);
+    int32_t* dst = block_tables + static_cast<int64_t>(s) * stride;
+    for (int32_t p = 0; p < stride; ++p) dst[p] = p < need ? bt[p] : -1;
+  }
+  info->num_rows = S;
+  info->num_decodes = num_decodes;
+  info->num_tokens = used;
+  info->bt_stride = stride;
+  info->unused_tokens = budget - used;
+  return MS_OK;
+}
+
+extern "C" MS_API int ms_rope_table(int32_t max_pos, int32_t D, double base, float* cos_tab, float* sin_tab) {
+  if (max_pos < 1 || D < 2 || (D & 1) || !(base > 0.0) || cos_tab == nullptr || sin_tab == nullptr)
+    return MS_ERR_ARG;
+  const int32_t half = D / 2;
+  std::vector<double> inv_freq(static_cast<size_t>(half));
+  for (int32_t i = 0; i < half; ++i) inv_freq[i] = std::pow(base, -(2.0 * i) / static_cast<double>(D));
+  for (int32_t p = 0; p < max_pos; ++p) {
+    for (int32_t i = 0; i < half; ++i) {
+      const double ang = static_cast<double>(p) * inv_freq[i];
+      cos_tab[static_cast<int64_t>(p) * half + i] = static_cast<float>(std::cos(ang));
+      sin_tab[static_cast<int64_t>(p) * half + i] = static_cast<float>(std::sin(ang));
+    }
+  }
+  return MS_OK;
+}

@@ -1,0 +1,219 @@
+/*
+ * mixed_step.h -- C ABI of the GB300 (sm_103a) mixed-batch attention step.
+ *
+ * One forward step of an attention layer over a paged KV cache, for a batch
+ * that packs single-token decodes next to prefill chunks under a token budget
+ * (chunked prefill with stall-free, decode-first batching).  Three calls make
+ * the step:
+ *
+ *   ms_build_batch_metadata  host: decode-first token-budget packing and the
+ *                            varlen metadata of the packed rows;
+ *   ms_kv_append_rope        device: rotary embedding at absolute positions
+ *                            for q and k, and the paged append of k and v;
+ *   ms_mixed_step_attention  device: causal attention of every packed row
+ *                            over its cached prefix plus its own new tokens.
+ *
+ * Sources, cited by page title and section:
+ *   [zwj] "Chunked Prefill 的 Token 预算" (zwjcode.cn)
+ *   [sar] "Chunked Prefill: Ending the Great Stall" (manishklach.github.io)
+ *   [mer] "Splitting Prefill From Decode Inside a Step" (mercemay.com)
+ *   [sfe] "Prefill head-of-line blocking" (sference.com)
+ *
+ * Conventions for every call:
+ *   - All integers are int32 unless stated.  bf16 tensors are raw 16-bit
+ *     storage (void*).  Pointers marked "device" must be device memory of the
+ *     current CUDA device; "host" pointers are ordinary host memory.
+ *   - The caller owns every buffer (metadata, tensors, K/V pools, workspace,
+ *     stream).  The library allocates no memory and never synchronises, except
+ *     in ms_read_status, which waits on the given stream.
+ *   - Device calls only enqueue work on `stream`; they return MS_OK once the
+ *     launches are queued.  Launch errors are returned as MS_ERR_CUDA.
+ *   - Page size is 16 tokens.  Head dim D is 64 or 128.  H_q % H_kv == 0.
+ *   - Return value: MS_OK (0) or a negative MS_ERR_* code; on error nothing is
+ *     enqueued and no output is written.
+ */
+#ifndef MIXED_STEP_H_
+#define MIXED_STEP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MS_API __attribute__((visibility("default")))
+#else
+#define MS_API
+#endif
+
+/* CUDA stream handle (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st* ms_stream_t;
+
+enum {
+  MS_OK = 0,
+  MS_ERR_ARG = -1,       /* bad shape, size, capacity, alignment or null pointer */
+  MS_ERR_BUDGET = -2,    /* more running decodes than the token budget ([zwj] section 05) */
+  MS_ERR_NO_PAGES = -3,  /* a block table cannot address the scheduled tokens ([mer]) */
+  MS_ERR_CUDA = -4,      /* a CUDA runtime/driver call failed */
+  MS_ERR_DEVICE = -5     /* a device-side check failed (see ms_read_status) */
+};
+
+/* Device status bits, accumulated in a caller-owned int32 status word. */
+enum {
+  MS_STATUS_BAD_SLOT = 1,      /* slot_mapping entry outside the page pool */
+  MS_STATUS_BAD_POSITION = 2,  /* position outside the cos/sin table */
+  MS_STATUS_BAD_PAGE = 4,      /* block_tables entry outside the page pool */
+  MS_STATUS_TIMEOUT = 8,       /* a bounded in-kernel wait gave up */
+  MS_STATUS_BAD_META = 16      /* inconsistent row metadata (lengths, offsets) */
+};
+
+/* One request as the scheduler sees it.
+ *   cached_len        c, tokens already in the KV cache (absolute positions
+ *                     0..c-1; positions are never reset, [zwj] section 07)
+ *   remaining_prompt  0 for a running decode; > 0 prompt tokens still to prefill
+ *   block_table       host, num_pages physical page ids in logical order,
+ *                     reserved by the caller before the request's first chunk
+ *                     ([mer] "The arithmetic of chunk boundaries") */
+typedef struct {
+  int32_t cached_len;
+  int32_t remaining_prompt;
+  const int32_t* block_table;
+  int32_t num_pages;
+} ms_request;
+
+/* token_budget           B_tok, the most tokens one step may hold
+ *                        ([zwj] section 04: |D_t| + sum |c| <= B_tok)
+ * max_chunk_per_request  per-prefill cap on one round's take; 0 = no cap
+ *                        ([sfe] "The fix", [mer] build_batch's chunk_size) */
+typedef struct {
+  int32_t token_budget;
+  int32_t max_chunk_per_request;
+} ms_sched_config;
+
+/* Summary of one packed step.  bt_stride is the row stride of block_tables. */
+typedef struct {
+  int32_t num_rows;
+  int32_t num_decodes;
+  int32_t num_tokens;
+  int32_t bt_stride;
+  int32_t unused_tokens;
+} ms_batch_info;
+
+/* ms_build_batch_metadata -- pack one round, decode first ([zwj] sections
+ * 03-05 and 08, [sar] sections 03-04), and emit its varlen metadata
+ * ([zwj] section 06).  Host only; pure (reqs are not modified: the caller
+ * commits progress after the step, [zwj] section 08).
+ *
+ * Packing: every request with remaining_prompt == 0 is a decode row (c, 1), in
+ * input order; more decodes than token_budget is MS_ERR_BUDGET.  Then, in input
+ * order, each prompt takes min(remaining, leftover, cap) tokens as a chunk row
+ * (c, take); packing stops when the leftover reaches 0.
+ *
+ * Outputs (host, caller-allocated, capacities in elements):
+ *   cu_seqlens_q  [cap_rows + 1]  row token offsets, cu[0] = 0
+ *   q_start_pos   [cap_rows]      c of each row
+ *   context_lens  [cap_rows]      c + d, the row's length after the step
+ *   positions     [cap_tokens]    absolute position c + j of each new token
+ *   slot_mapping  [cap_tokens]    block_table[pos / 16] * 16 + pos % 16
+ *   block_tables  [cap_bt]        rows x bt_stride page ids, padded with -1;
+ *                                 bt_stride = max over rows of ceil((c+d)/16)
+ *   row_req       [cap_rows]      request index of each row
+ *   num_scheduled [n_req]         tokens each request got this round (0 or d)
+ *   info          summary (num_rows, num_decodes, num_tokens, bt_stride, unused)
+ * Errors: MS_ERR_ARG (null pointer, capacity too small, negative lengths),
+ * MS_ERR_BUDGET, MS_ERR_NO_PAGES (a block table shorter than ceil((c+d)/16)). */
+MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_req, const ms_sched_config* cfg,
+                                   int32_t cap_rows, int32_t cap_tokens, int64_t cap_bt,
+                                   int32_t* cu_seqlens_q, int32_t* q_start_pos, int32_t* context_lens,
+                                   int32_t* positions, int32_t* slot_mapping, int32_t* block_tables,
+                                   int32_t* row_req, int32_t* num_scheduled, ms_batch_info* info);
+
+/* ms_rope_table -- host: cos/sin of p * base^(-2i/D) for p < max_pos, i < D/2,
+ * computed in double precision and rounded to fp32.  Output layout
+ * [max_pos][D/2] row-major, caller-allocated host buffers.  The rotary phase
+ * is taken at the absolute position ([zwj] section 07).
+ * Errors: MS_ERR_ARG (null pointer, max_pos < 1, D odd or < 2, base <= 0). */
+MS_API int ms_rope_table(int32_t max_pos, int32_t D, double base, float* cos_tab, float* sin_tab);
+
+/* ms_kv_append_rope -- device: for every new token t at p = positions[t],
+ * rotate q[t] and k[t] with the rotate-half pairing (element i with i + D/2):
+ *     y_i       = x_i * cos - x_{i+D/2} * sin
+ *     y_{i+D/2} = x_{i+D/2} * cos + x_i * sin
+ * each as two fp32 products and one fp32 sum, rounded to nearest, never fused,
+ * then rounded to bf16 (nearest even); write q_rot[t], and rotated k[t] and
+ * raw v[t] into the paged pools at slot_mapping[t] ([zwj] section 06; slot -1
+ * means no write).
+ *   q      device bf16 [T, H_q, D];   q_rot device bf16 [T, H_q, D] (may alias q)
+ *   k, v   device bf16 [T, H_kv, D]
+ *   positions, slot_mapping  device int32 [T]
+ *   cos_tab, sin_tab         device fp32 [max_pos, D/2] (ms_rope_table)
+ *   k_cache, v_cache         device bf16 [num_pages, H_kv, 16, D]
+ *   dev_status               device int32 status word or NULL; out-of-range
+ *                            slots and positions are skipped and, when given,
+ *                            recorded there (MS_STATUS_BAD_SLOT / _POSITION)
+ * All tensor pointers 16-byte aligned.  T == 0 is a no-op.
+ * Errors: MS_ERR_ARG, MS_ERR_CUDA. */
+MS_API int ms_kv_append_rope(const void* q, const void* k, const void* v,
+                             const int32_t* positions, const int32_t* slot_mapping, int32_t T,
+                             const float* cos_tab, const float* sin_tab, int32_t max_pos,
+                             void* k_cache, void* v_cache, int32_t num_pages, void* q_rot,
+                             int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
+                             int32_t* dev_status, ms_stream_t stream);
+
+/* ms_attention_workspace_size -- bytes of device workspace that
+ * ms_mixed_step_attention needs for steps of at most max_rows rows,
+ * max_tokens new tokens and max_context_total = sum over rows of context_lens.
+ * The first 256 bytes of a workspace hold its status word and queue counters:
+ * zero the whole workspace once before its first use. */
+MS_API size_t ms_attention_workspace_size(int32_t max_rows, int32_t max_tokens, int64_t max_context_total,
+                                          int32_t H_q, int32_t H_kv, int32_t D);
+
+/* ms_mixed_step_attention -- device: for every packed token t of row s
+ * (absolute position p = q_start_pos[s] + t - cu_seqlens_q[s]) and query head h
+ * (KV head h / (H_q / H_kv)):
+ *     out[t, h] = softmax_j(scale * q_rot[t, h] . K[j]) V[j],   j = 0..p
+ * with K/V row j read from page block_tables[s * bt_stride + j / 16], slot
+ * j % 16.  A chunk [c, c+d) sees the cached prefix [0, c) plus its own tokens
+ * causally ([zwj] sections 02 and 07; [sar] section 05).  Rows with d == 1 run
+ * the split-KV decode path; rows with d > 1 run the tensor-core chunk path; a
+ * persistent queue orders the work longest-first.  bf16 in, fp32 accumulate,
+ * bf16 out.
+ *   q_rot        device bf16 [num_tokens, H_q, D]
+ *   k_cache, v_cache  device bf16 [num_pages, H_kv, 16, D], num_pages pages
+ *   cu_seqlens_q [num_rows + 1], q_start_pos [num_rows], context_lens [num_rows],
+ *   block_tables [num_rows * bt_stride]   device int32, as built by
+ *                ms_build_batch_metadata (context_lens[s] must equal
+ *                q_start_pos[s] + d_s)
+ *   out          device bf16 [num_tokens, H_q, D]
+ *   workspace    device, ws_bytes >= ms_attention_workspace_size(...) for
+ *                this step's sizes, zeroed before first use; its first int32 is
+ *                the status word (read it with ms_read_status)
+ * Out-of-range page ids are not read (MS_STATUS_BAD_PAGE).  Steps that share a
+ * workspace must not overlap on the GPU.
+ * Errors: MS_ERR_ARG, MS_ERR_CUDA. */
+MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_cache, const void* v_cache,
+                                   int32_t num_pages,
+                                   const int32_t* cu_seqlens_q, const int32_t* q_start_pos,
+                                   const int32_t* context_lens, const int32_t* block_tables,
+                                   int32_t bt_stride, int32_t num_rows, int32_t num_tokens,
+                                   int64_t context_total,
+                                   int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
+                                   void* out, void* workspace, size_t ws_bytes, ms_stream_t stream);
+
+/* ms_read_status -- waits for `stream`, copies the int32 device status word at
+ * dev_status (for attention: the workspace pointer) to *host_status and
+ * clears it.  Returns MS_OK, MS_ERR_DEVICE when the word was non-zero, or
+ * MS_ERR_ARG / MS_ERR_CUDA. */
+MS_API int ms_read_status(int32_t* dev_status, ms_stream_t stream, int32_t* host_status);
+
+/* ms_num_sms -- SM count of the current device (the persistent grid size), or
+ * a negative MS_ERR_* code. */
+MS_API int ms_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MIXED_STEP_H_ */

@@ -1,0 +1,148 @@
+"""Host-side checks of the C ABI (no GPU): the library builds, loads and exports
+every declared entry point; the C++ scheduler and rope table are bit-exact with
+the oracle; error codes follow the header."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def ms():
+    from chunked_prefill_mixed_decode_gb300 import build
+    build.build()
+    import chunked_prefill_mixed_decode_gb300 as ms
+    return ms
+
+
+def header_symbols():
+    syms = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            syms += re.findall(r"MS_API\s+[\w\s\*]+?\b(ms_\w+)\s*\(", text)
+    return syms
+
+
+def test_library_exports_every_declared_symbol(ms):
+    syms = header_symbols()
+    assert len(syms) >= 7
+    lib = ctypes.CDLL(ms.build.LIB)
+    for s in syms:
+        assert hasattr(lib, s), s
+
+
+def _oracle_meta(states, tables, budget, cap=0):
+    rows, unused = oracle.schedule(states, budget, cap)
+    n_dec = sum(1 for s in states if s[1] == 0)
+    m = oracle.batch_metadata(rows, tables, len(states), num_decodes=n_dec)
+    m["unused_tokens"] = unused
+    return m
+
+
+def _assert_meta_equal(got, ref):
+    for k in ("cu_seqlens_q", "q_start_pos", "context_lens", "positions", "slot_mapping", "row_req",
+              "num_scheduled"):
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+    np.testing.assert_array_equal(got["block_tables"], ref["block_tables"])
+    for k in ("bt_stride", "num_rows", "num_tokens", "num_decodes", "unused_tokens"):
+        assert got[k] == ref[k], k
+
+
+def test_worked_example_rounds_bit_exact(ms):
+    wl = workloads.worked_example()
+    tables = [r.block_table for r in wl.requests]
+    states = [(r.cached_len, r.remaining) for r in wl.requests]
+    for _ in range(4):
+        got = ms.build_batch_metadata(states, tables, wl.token_budget)
+        ref = _oracle_meta(states, tables, wl.token_budget)
+        _assert_meta_equal(got, ref)
+        rows, _ = oracle.schedule(states, wl.token_budget)
+        states = oracle.commit_round(states, rows)
+
+
+@pytest.mark.parametrize("name", ["mha7b_b512", "mha13b_b2048", "gqa8b_b8192", "long_bimodal_b4608"])
+def test_config_metadata_bit_exact(ms, name):
+    wls = workloads.CONFIGS[name]()
+    wls = wls if isinstance(wls, list) else [wls]
+    for wl in wls[:3]:
+        tables = [r.block_table for r in wl.requests]
+        states = [(r.cached_len, r.remaining) for r in wl.requests]
+        got = ms.build_batch_metadata(states, tables, wl.token_budget, wl.max_chunk)
+        _assert_meta_equal(got, _oracle_meta(states, tables, wl.token_budget, wl.max_chunk))
+
+
+def test_scheduler_fuzz_bit_exact(ms):
+    rng = np.random.default_rng(21)
+    for trial in range(400):
+        n = int(rng.integers(0, 12))
+        budget = int(rng.integers(0, 40))
+        cap = int(rng.integers(0, 3)) * int(rng.integers(1, 9))
+        states, tables = [], []
+        for _ in range(n):
+            c = int(rng.integers(0, 100))
+            rem = 0 if rng.random() < 0.5 else int(rng.integers(1, 60))
+            need = -(-(c + max(rem, 1)) // 16)
+            short = rng.random() < 0.08
+            n_pages = max(0, need - int(rng.integers(1, 3))) if short else need + int(rng.integers(0, 3))
+            tables.append(rng.integers(0, 1000, size=n_pages).astype(np.int32))
+            states.append((c, rem))
+        try:
+            ref = _oracle_meta(states, tables, budget, cap)
+            err = None
+        except oracle.BudgetError:
+            err = ms.MS_ERR_BUDGET
+        except oracle.NoPagesError:
+            err = ms.MS_ERR_NO_PAGES
+        if err is None:
+            _assert_meta_equal(ms.build_batch_metadata(states, tables, budget, cap), ref)
+        else:
+            with pytest.raises(ms.MixedStepError) as e:
+                ms.build_batch_metadata(states, tables, budget, cap)
+            assert e.value.code == err
+
+
+def test_rope_table_bit_exact_with_oracle(ms):
+    for D in (64, 128):
+        max_pos = 131073
+        cos, sin = ms.rope_table(max_pos, D)
+        pos = np.array([0, 1, 2, 5, 15, 16, 17, 448, 4095, 6000, 28672, 32767, 65536, 100003, 131072])
+        oc, os_ = oracle.rope_tables(pos, D)
+        np.testing.assert_array_equal(cos[pos], oc)
+        np.testing.assert_array_equal(sin[pos], os_)
+
+
+def test_argument_errors(ms):
+    lib = ms.lib()
+    assert lib.ms_rope_table(0, 64, 10000.0, None, None) == ms.MS_ERR_ARG
+    assert lib.ms_kv_append_rope(*([None] * 5), 1, None, None, 1, None, None, 1, None, 4, 3, 64, 16, None,
+                                 None) == ms.MS_ERR_ARG  # H_q % H_kv != 0
+    assert lib.ms_kv_append_rope(*([None] * 5), 0, None, None, 1, None, None, 1, None, 4, 2, 64, 16, None,
+                                 None) == ms.MS_OK  # T == 0 is a no-op
+    assert lib.ms_mixed_step_attention(None, None, None, 1, None, None, None, None, 1, 0, 0, 0, 4, 2, 96, 16,
+                                       0.1, None, None, 0, None) == ms.MS_ERR_ARG  # D = 96
+    assert lib.ms_mixed_step_attention(None, None, None, 1, None, None, None, None, 1, 0, 0, 0, 4, 2, 64, 16,
+                                       0.1, None, None, 0, None) == ms.MS_OK  # empty step
+    assert lib.ms_mixed_step_attention(None, None, None, 1, None, None, None, None, 1, 0, 0, 0, 12, 4, 64, 16,
+                                       0.1, None, None, 0, None) == ms.MS_ERR_ARG  # G = 3 unsupported
+    # capacity too small -> MS_ERR_ARG, budget overflow -> MS_ERR_BUDGET
+    bt = np.arange(4, dtype=np.int32)
+    with pytest.raises(ms.MixedStepError) as e:
+        ms.build_batch_metadata([(3, 0)] * 3, [bt] * 3, 2)
+    assert e.value.code == ms.MS_ERR_BUDGET
+    with pytest.raises(ms.MixedStepError) as e:
+        ms.build_batch_metadata([(60, 10)], [bt], 8)  # needs ceil(68/16) = 5 pages
+    assert e.value.code == ms.MS_ERR_NO_PAGES
+
+
+def test_workspace_size_grows_with_context(ms):
+    a = ms.attention_workspace_size(65, 512, 64 * 4096, 32, 32, 128)
+    b = ms.attention_workspace_size(65, 512, 2 * 64 * 4096, 32, 32, 128)
+    assert 0 < a < b
+    assert ms.attention_workspace_size(1, 1, 0, 4, 2, 96) == 0

@@ -1,0 +1,283 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bar: metadata, K/V pool and q_rot bit-exact; attention output within
+|gpu - oracle| <= 1e-2 + 1e-2 * |oracle| elementwise (bf16 in, fp32 accumulate,
+bf16 out); the GPU's chunked prefill matches its own full prefill within the
+same bound.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from chunked_prefill_mixed_decode_gb300 import build
+    build.build()
+    import chunked_prefill_mixed_decode_gb300 as ms
+    from chunked_prefill_mixed_decode_gb300 import step
+    return torch, ms, step
+
+
+def _states(wl):
+    return [(r.cached_len, r.remaining) for r in wl.requests]
+
+
+def _tables(wl):
+    return [r.block_table for r in wl.requests]
+
+
+class Case:
+    """One step of a workload on the GPU and its oracle inputs."""
+
+    def __init__(self, env, wl, states, seed, pool=None, dev="cuda", host_pool=True):
+        torch, ms, step = env
+        self.wl, self.states = wl, states
+        self.meta = ms.build_batch_metadata(states, _tables(wl), wl.token_budget, wl.max_chunk)
+        self.batch = step.to_device(self.meta, dev)
+        T = self.meta["num_tokens"]
+        self.q, self.k, self.v = workloads.step_tensors(wl, max(T, 1), seed, dev)
+        if pool is None:
+            pool = workloads.kv_pool(wl, seed, dev)
+        self.k_cache, self.v_cache = pool
+        if host_pool:  # host copies before the step
+            self.k_in = workloads.bf16_bits(self.k_cache)
+            self.v_in = workloads.bf16_bits(self.v_cache)
+        self.cos, self.sin = step.rope_tables_device(wl.max_pos + 1, wl.D, dev)
+        self.out = torch.zeros_like(self.q)
+        self.q_rot = torch.empty_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = step.workspace_for(self.batch, wl.H_q, wl.H_kv, wl.D, dev)
+
+    def run(self, env):
+        torch, ms, step = env
+        step.run_step(self.q, self.k, self.v, self.batch, self.cos, self.sin, self.k_cache, self.v_cache, self.out,
+                      self.ws, q_rot=self.q_rot, dev_status=self.status)
+        torch.cuda.synchronize()
+        assert ms.read_status(self.status) == 0
+        assert ms.read_status(self.ws) == 0
+        return self
+
+    def oracle_append(self):
+        T = self.meta["num_tokens"]
+        ref_meta = oracle.batch_metadata(*oracle.schedule(self.states, self.wl.token_budget, self.wl.max_chunk)[:1],
+                                         _tables(self.wl), len(self.states),
+                                         num_decodes=sum(1 for s in self.states if s[1] == 0))
+        for key in ("cu_seqlens_q", "positions", "slot_mapping", "context_lens", "q_start_pos"):
+            np.testing.assert_array_equal(self.meta[key], ref_meta[key])
+        q = workloads.bf16_bits(self.q[:T])
+        k = workloads.bf16_bits(self.k[:T])
+        v = workloads.bf16_bits(self.v[:T])
+        return ref_meta, oracle.kv_append(q, k, v, ref_meta["positions"], ref_meta["slot_mapping"], self.k_in,
+                                          self.v_in)
+
+
+def _check_attention(got_bits, ref, what=""):
+    got = oracle.bf16_to_f64(got_bits)
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), f"{what}: {bad.sum()} elements out of bound, max err {err.max():.3g}"
+    return err.max()
+
+
+def _full_parity(env, wl, states, seed):
+    case = Case(env, wl, states, seed).run(env)
+    T = case.meta["num_tokens"]
+    ref_meta, (q_rot, kp, vp) = case.oracle_append()
+    np.testing.assert_array_equal(workloads.bf16_bits(case.q_rot[:T]), q_rot)
+    np.testing.assert_array_equal(workloads.bf16_bits(case.k_cache), kp)
+    np.testing.assert_array_equal(workloads.bf16_bits(case.v_cache), vp)
+    ref = oracle.attention_all(q_rot, kp, vp, ref_meta, wl.H_kv)
+    got = workloads.bf16_bits(case.out[:T])
+    n_dec = case.meta["num_decodes"]
+    if n_dec:
+        _check_attention(got[:n_dec], ref[:n_dec], f"{wl.name} decode rows")
+    if T > n_dec:
+        _check_attention(got[n_dec:], ref[n_dec:], f"{wl.name} chunk rows")
+    return case
+
+
+def test_worked_example_four_rounds(env):
+    """The 8-token-budget walk-through (3 decodes + 12-token prompt), stepped four rounds on one pool."""
+    wl = workloads.worked_example()
+    states = _states(wl)
+    torch = env[0]
+    pool = workloads.kv_pool(wl, 1, "cuda")
+    for rnd in range(4):
+        case = Case(env, wl, states, 100 + rnd, pool=pool).run(env)
+        T = case.meta["num_tokens"]
+        ref_meta, (q_rot, kp, vp) = case.oracle_append()
+        np.testing.assert_array_equal(workloads.bf16_bits(case.k_cache), kp)
+        np.testing.assert_array_equal(workloads.bf16_bits(case.v_cache), vp)
+        ref = oracle.attention_all(q_rot, kp, vp, ref_meta, wl.H_kv)
+        _check_attention(workloads.bf16_bits(case.out[:T]), ref, f"round {rnd + 1}")
+        rows, _ = oracle.schedule(states, wl.token_budget)
+        states = oracle.commit_round(states, rows)
+    assert states[3] == (13, 0)
+
+
+@pytest.mark.parametrize("H_q,H_kv,D", [(8, 2, 128), (8, 8, 64), (4, 4, 128), (16, 2, 128), (8, 2, 64),
+                                        (4, 1, 64)])
+def test_small_mixed_all_rows(env, H_q, H_kv, D):
+    """Decodes at c = 0, page boundaries and beyond a tile; chunks of 130 (several tiles), 200 at offset 300
+    and a 5-token tail at offset 16."""
+    wl = workloads.small_mixed(seed=H_q * 100 + H_kv * 10 + D, H_q=H_q, H_kv=H_kv, D=D)
+    _full_parity(env, wl, _states(wl), seed=7)
+
+
+def test_decode_only_and_chunk_only(env):
+    wl = workloads.small_mixed(seed=31, H_q=8, H_kv=2, D=128, dec_ctx=(5, 64, 255, 256, 257, 1000, 2049),
+                               prompts=())
+    _full_parity(env, wl, _states(wl), seed=8)
+    wl = workloads.small_mixed(seed=32, H_q=8, H_kv=2, D=128, dec_ctx=(), prompts=((0, 2), (700, 129), (5, 64)))
+    _full_parity(env, wl, _states(wl), seed=9)
+
+
+def test_chunked_prefill_matches_full_prefill_on_gpu(env):
+    """zwjcode section 07: chunks [2, 3, 1] of a 6-token prompt -- and a 300-token prompt as
+    [100, 37, 163] -- give the same outputs as one full prefill (same pool, same inputs)."""
+    torch, ms, step = env
+    for chunks, H_q, H_kv, D in (([2, 3, 1], 4, 2, 64), ([100, 37, 163], 8, 2, 128), ([129, 128, 1], 8, 8, 128)):
+        L = sum(chunks)
+        rng = np.random.default_rng(L)
+        table = rng.permutation(-(-L // 16) + 2).astype(np.int32)
+        wl = workloads.Workload("chunked_vs_full", H_q, H_kv, D, L, [workloads.Request(0, L, table)],
+                                len(table))
+        qa, ka, va = workloads.step_tensors(wl, L, 5, "cuda")
+        cos, sin = step.rope_tables_device(L + 1, D, "cuda")
+
+        def run(chunk_list):
+            kc = torch.zeros((wl.num_pages, H_kv, 16, D), dtype=torch.bfloat16, device="cuda")
+            vc = torch.zeros_like(kc)
+            outs = []
+            state = [(0, L)]
+            for d in chunk_list:
+                meta = ms.build_batch_metadata(state, [table], d)
+                b = step.to_device(meta, "cuda")
+                c0 = state[0][0]
+                q = qa[c0:c0 + d].clone()
+                out = torch.zeros_like(q)
+                ws = step.workspace_for(b, H_q, H_kv, D, "cuda")
+                step.run_step(q, ka[c0:c0 + d], va[c0:c0 + d], b, cos, sin, kc, vc, out, ws)
+                outs.append(out)
+                state = [(c0 + d, L - c0 - d)]
+            torch.cuda.synchronize()
+            return torch.cat(outs).float().cpu().numpy()
+
+        full = run([L])
+        chunked = run(chunks)
+        assert np.all(np.abs(chunked - full) <= ATOL + RTOL * np.abs(full))
+
+
+def test_status_reports_bad_slot_and_page(env):
+    torch, ms, step = env
+    wl = workloads.small_mixed(seed=41, H_q=4, H_kv=2, D=64, dec_ctx=(20,), prompts=())
+    case = Case(env, wl, _states(wl), seed=3)
+    bad_slots = torch.full_like(case.batch.slot_mapping, wl.num_pages * 16 + 5)
+    ms.kv_append_rope(case.q, case.k, case.v, case.batch.positions, bad_slots, case.cos, case.sin, case.k_cache,
+                      case.v_cache, q_rot=case.q_rot, dev_status=case.status)
+    torch.cuda.synchronize()
+    assert ms.read_status(case.status) & ms.STATUS_BAD_SLOT
+    np.testing.assert_array_equal(workloads.bf16_bits(case.k_cache), case.k_in)  # nothing written
+    case.batch.block_tables.fill_(wl.num_pages + 7)
+    ms.mixed_step_attention(case.q_rot, case.k_cache, case.v_cache, case.batch.cu_seqlens_q,
+                            case.batch.q_start_pos, case.batch.context_lens, case.batch.block_tables,
+                            case.batch.context_total, case.out, case.ws)
+    torch.cuda.synchronize()
+    assert ms.read_status(case.ws) & ms.STATUS_BAD_PAGE
+    assert ms.read_status(case.ws) == 0  # cleared by the read
+
+
+def test_inconsistent_metadata_is_flagged(env):
+    torch, ms, step = env
+    wl = workloads.small_mixed(seed=42, H_q=4, H_kv=2, D=64, dec_ctx=(20, 30), prompts=((0, 9),))
+    case = Case(env, wl, _states(wl), seed=3)
+    case.batch.context_lens[0] += 1  # no longer c + d
+    ms.mixed_step_attention(case.q, case.k_cache, case.v_cache, case.batch.cu_seqlens_q, case.batch.q_start_pos,
+                            case.batch.context_lens, case.batch.block_tables, case.batch.context_total,
+                            case.out, case.ws)
+    torch.cuda.synchronize()
+    assert ms.read_status(case.ws) & ms.STATUS_BAD_META
+
+
+# ------------------------------------------------------------------ full-size configurations (sampled)
+
+def _sampled_parity(env, wl, seed, n_dec_rows=48, n_chunk_tokens=48, heads=None):
+    """Full-size step on the GPU; oracle on sampled (token, head) pairs.
+
+    The sampled rows' pages are gathered from the device pool before and after
+    the step: the oracle appends the rows' new tokens into the "before" copy,
+    which must equal the "after" copy bit for bit, then attends from it."""
+    torch, ms, step = env
+    states = _states(wl)
+    case = Case(env, wl, states, seed, host_pool=False)
+    meta = case.meta
+    T, n_dec = meta["num_tokens"], meta["num_decodes"]
+    rng = np.random.default_rng(seed)
+    H_q = wl.H_q
+    heads = heads or sorted(set(rng.integers(0, H_q, size=4).tolist()) | {0, H_q - 1})
+    dec_rows = sorted(set(rng.choice(n_dec, size=min(n_dec, n_dec_rows), replace=False).tolist())) if n_dec else []
+    chunk_tok = sorted(set(rng.choice(np.arange(n_dec, T), size=min(T - n_dec, n_chunk_tokens),
+                                      replace=False).tolist()) | ({n_dec, T - 1} if T > n_dec else set()))
+    tokens = dec_rows + chunk_tok
+    ref_meta = oracle.batch_metadata(oracle.schedule(states, wl.token_budget, wl.max_chunk)[0], _tables(wl),
+                                     len(states), num_decodes=n_dec)
+    for key in ("cu_seqlens_q", "positions", "slot_mapping", "context_lens", "q_start_pos"):
+        np.testing.assert_array_equal(meta[key], ref_meta[key])
+    cu = ref_meta["cu_seqlens_q"]
+    row_of = np.searchsorted(cu, np.arange(T), side="right") - 1
+    rows = sorted(set(row_of[tokens].tolist()))
+    bts = ref_meta["block_tables"]
+    pages = np.unique(np.concatenate([bts[s][bts[s] >= 0] for s in rows]))
+    remap = np.full(wl.num_pages, -1, dtype=np.int64)
+    remap[pages] = np.arange(len(pages))
+    pidx = torch.from_numpy(pages.astype(np.int64)).to(case.k_cache.device)
+    k_pre = workloads.bf16_bits(case.k_cache.index_select(0, pidx))
+    v_pre = workloads.bf16_bits(case.v_cache.index_select(0, pidx))
+    case.run(env)
+    k_post = workloads.bf16_bits(case.k_cache.index_select(0, pidx))
+    v_post = workloads.bf16_bits(case.v_cache.index_select(0, pidx))
+    sub_meta = {"cu_seqlens_q": cu, "q_start_pos": ref_meta["q_start_pos"],
+                "block_tables": np.where(bts >= 0, remap[np.maximum(bts, 0)], -1)}
+    tok_rows = [t for t in range(T) if row_of[t] in set(rows)]
+    q = workloads.bf16_bits(case.q[tok_rows])
+    k = workloads.bf16_bits(case.k[tok_rows])
+    v = workloads.bf16_bits(case.v[tok_rows])
+    pos = ref_meta["positions"][tok_rows]
+    slots = ref_meta["slot_mapping"][tok_rows]
+    sub_slots = remap[slots // 16] * 16 + slots % 16
+    q_rot_sub, kp_ref, vp_ref = oracle.kv_append(q, k, v, pos, sub_slots, k_pre, v_pre)
+    np.testing.assert_array_equal(k_post, kp_ref)
+    np.testing.assert_array_equal(v_post, vp_ref)
+    np.testing.assert_array_equal(workloads.bf16_bits(case.q_rot[tok_rows]), q_rot_sub)
+    q_rot_full = np.zeros((T, H_q, wl.D), np.uint16)
+    q_rot_full[tok_rows] = q_rot_sub
+    select = [(t, h) for t in tokens for h in heads]
+    ref = oracle.attention_rows(q_rot_full, kp_ref, vp_ref, sub_meta, wl.H_kv, select=select)
+    got = workloads.bf16_bits(case.out)
+    g = np.stack([got[t, h] for t, h in select])
+    r = np.stack([ref[(t, h)] for t, h in select])
+    _check_attention(g, r, wl.name)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mha7b_b512", "mha13b_b2048", "gqa8b_b8192", "long_bimodal_b4608"])
+def test_full_size_config_sampled(env, name):
+    wls = workloads.CONFIGS[name]()
+    if isinstance(wls, list):
+        wls = [wls[0], wls[-1]] + workloads.mha7b_steps(include_tail=True)[-1:]
+    else:
+        wls = [wls]
+    for i, wl in enumerate(wls):
+        _sampled_parity(env, wl, seed=17 + i)
