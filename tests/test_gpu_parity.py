@@ -53,7 +53,9 @@ class Case:
         if host_pool:  # host copies before the step
             self.k_in = workloads.bf16_bits(self.k_cache)
             self.v_in = workloads.bf16_bits(self.v_cache)
-        self.cos, self.sin = step.rope_tables_device(wl.max_pos + 1, wl.D, dev)
+        # positions of later rounds stay within the pages each request reserved
+        max_pos = max([wl.max_pos + 1] + [16 * len(r.block_table) for r in wl.requests])
+        self.cos, self.sin = step.rope_tables_device(max_pos, wl.D, dev)
         self.out = torch.zeros_like(self.q)
         self.q_rot = torch.empty_like(self.q)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
