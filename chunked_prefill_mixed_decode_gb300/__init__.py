@@ -19,11 +19,12 @@ import numpy as np
 from .build import LIB as _LIB_PATH
 
 MS_OK, MS_ERR_ARG, MS_ERR_BUDGET, MS_ERR_NO_PAGES, MS_ERR_CUDA, MS_ERR_DEVICE = 0, -1, -2, -3, -4, -5
+MS_ERR_SCRATCH = -6
 STATUS_BAD_SLOT, STATUS_BAD_POSITION, STATUS_BAD_PAGE, STATUS_TIMEOUT, STATUS_BAD_META = 1, 2, 4, 8, 16
 PAGE_SIZE = 16
 
 _ERR_NAMES = {MS_ERR_ARG: "MS_ERR_ARG", MS_ERR_BUDGET: "MS_ERR_BUDGET", MS_ERR_NO_PAGES: "MS_ERR_NO_PAGES",
-              MS_ERR_CUDA: "MS_ERR_CUDA", MS_ERR_DEVICE: "MS_ERR_DEVICE"}
+              MS_ERR_CUDA: "MS_ERR_CUDA", MS_ERR_DEVICE: "MS_ERR_DEVICE", MS_ERR_SCRATCH: "MS_ERR_SCRATCH"}
 
 
 class MixedStepError(RuntimeError):
@@ -77,6 +78,11 @@ def lib() -> ctypes.CDLL:
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _VP, _VP,
                                           ctypes.c_size_t, _VP]
+    h.ms_mixed_step_attention_noalloc.restype = ctypes.c_int
+    h.ms_mixed_step_attention_noalloc.argtypes = [_VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP, _VP,
+                                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                  ctypes.c_float, _VP, _VP, _VP]
     h.ms_read_status.restype = ctypes.c_int
     h.ms_read_status.argtypes = [_VP, _VP, _I32P]
     h.ms_num_sms.restype = ctypes.c_int
@@ -212,6 +218,30 @@ def mixed_step_attention(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, con
                                        PAGE_SIZE, float(scale), _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "ms_mixed_step_attention")
+
+
+def mixed_step_attention_noalloc(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables,
+                                 context_total: int, out, dev_status=None, scale: float = None,
+                                 stream=None) -> None:
+    """The attention step without a caller workspace (ms_mixed_step_attention_noalloc).
+
+    For callers that cannot allocate device memory on their step path; the
+    step runs out of the library's 64 MiB static scratch per device.  Calls
+    share that scratch, so they must not overlap on the GPU.  ``dev_status``
+    (device int32, optional) receives this call's status bits.
+    """
+    T, H_q, D = q_rot.shape
+    H_kv = k_cache.shape[1]
+    S = cu_seqlens_q.shape[0] - 1
+    stride = block_tables.shape[1] if block_tables.dim() == 2 else block_tables.shape[0] // max(S, 1)
+    if scale is None:
+        scale = float(D) ** -0.5
+    rc = lib().ms_mixed_step_attention_noalloc(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                               _ptr(cu_seqlens_q), _ptr(q_start_pos), _ptr(context_lens),
+                                               _ptr(block_tables), stride, S, T, int(context_total), H_q, H_kv, D,
+                                               PAGE_SIZE, float(scale), _ptr(out), _ptr(dev_status),
+                                               _stream(stream))
+    _check(rc, "ms_mixed_step_attention_noalloc")
 
 
 def read_status(dev_status, stream=None) -> int:

@@ -33,6 +33,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "mixed_step.h"
 #include "ptx.cuh"
@@ -1205,4 +1206,74 @@ extern "C" MS_API int ms_read_status(int32_t* dev_status, ms_stream_t stream, in
   if (cudaStreamSynchronize(st) != cudaSuccess) return MS_ERR_CUDA;
   *host_status = v;
   return v == 0 ? MS_OK : MS_ERR_DEVICE;
+}
+
+// ----------------------------------------------------------------------------
+// attention without a caller workspace
+// ----------------------------------------------------------------------------
+//
+// Some callers cannot hand the library a workspace: a serving process that
+// reserves nearly all device memory for its KV-cache pool at start-up and
+// leaves nothing for a second allocator, or host code that must not call
+// cudaMalloc on its per-step path (a device allocation may synchronise the
+// device and stall every other stream).  For them the step can run out of a
+// fixed scratch array that the library owns.  The array lives in device
+// memory from the moment this library's device code is loaded on a GPU until
+// the process exits, on every GPU that loads it.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB per device
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_step_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_step_scratch on the current device, looked up once per
+// device (host code must not pass the symbol itself to a kernel: on the host
+// it names a stand-in, not device memory).
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_step_scratch) != cudaSuccess || p == nullptr) return MS_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MS_OK;
+}
+
+}  // namespace
+
+extern "C" MS_API int ms_mixed_step_attention_noalloc(const void* q_rot, const void* k_cache, const void* v_cache,
+                                                      int32_t num_pages, const int32_t* cu_seqlens_q,
+                                                      const int32_t* q_start_pos, const int32_t* context_lens,
+                                                      const int32_t* block_tables, int32_t bt_stride,
+                                                      int32_t num_rows, int32_t num_tokens, int64_t context_total,
+                                                      int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
+                                                      float scale, void* out, int32_t* dev_status,
+                                                      ms_stream_t stream) {
+  if (num_rows < 0 || context_total < 0 || H_q < 1 || (D != 64 && D != 128)) return MS_ERR_ARG;
+  if (num_rows == 0) return MS_OK;
+  const size_t need = ws_layout(num_rows, context_total, H_q, D).total;
+  if (need > kNoAllocScratchBytes) return MS_ERR_SCRATCH;
+  void* scratch = nullptr;
+  const int rc0 = scratch_address(&scratch);
+  if (rc0 != MS_OK) return rc0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: its status word and queue
+  // counters must start this call at zero
+  if (cudaMemsetAsync(scratch, 0, H_WORDS * sizeof(int32_t), st) != cudaSuccess) return MS_ERR_CUDA;
+  const int rc = ms_mixed_step_attention(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos,
+                                         context_lens, block_tables, bt_stride, num_rows, num_tokens, context_total,
+                                         H_q, H_kv, D, page_size, scale, out, scratch, kNoAllocScratchBytes, stream);
+  if (rc != MS_OK) return rc;
+  if (dev_status != nullptr &&
+      cudaMemcpyAsync(dev_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MS_ERR_CUDA;
+  return MS_OK;
 }

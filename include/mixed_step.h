@@ -57,7 +57,9 @@ enum {
   MS_ERR_BUDGET = -2,    /* more running decodes than the token budget ([zwj] section 05) */
   MS_ERR_NO_PAGES = -3,  /* a block table cannot address the scheduled tokens ([mer]) */
   MS_ERR_CUDA = -4,      /* a CUDA runtime/driver call failed */
-  MS_ERR_DEVICE = -5     /* a device-side check failed (see ms_read_status) */
+  MS_ERR_DEVICE = -5,    /* a device-side check failed (see ms_read_status) */
+  MS_ERR_SCRATCH = -6    /* the step needs more than the library's static scratch
+                            (ms_mixed_step_attention_noalloc) */
 };
 
 /* Device status bits, accumulated in a caller-owned int32 status word. */
@@ -201,6 +203,41 @@ MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_cache, const
                                    int64_t context_total,
                                    int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
                                    void* out, void* workspace, size_t ws_bytes, ms_stream_t stream);
+
+/* ms_mixed_step_attention_noalloc -- the same attention step as
+ * ms_mixed_step_attention, for callers that cannot give the library a
+ * workspace.  A serving process that reserves nearly all device memory for
+ * its KV-cache pool at start-up has no room for another allocation, and host
+ * code on a per-step path should not call cudaMalloc (it may synchronise the
+ * device and stall other streams).  This call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.  It works out of a
+ * scratch array the library owns, 64 MiB per device (the step's workspace
+ * size, ms_attention_workspace_size(num_rows, num_tokens, context_total, H_q,
+ * H_kv, D), must not exceed it -- else MS_ERR_SCRATCH and nothing is
+ * enqueued).  The array is device memory that every GPU which loads this
+ * library holds until the process exits.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array per device and it keeps the last
+ * call's contents: each call clears its status word and work counters on
+ * `stream` before the kernels run, so calls that overlap on the GPU (other
+ * streams, other host threads) race and must be serialised by the caller.
+ *
+ * Arguments are those of ms_mixed_step_attention without the workspace, plus
+ * dev_status: device int32 or NULL; when given, it is overwritten on `stream`
+ * with this call's device status bits (MS_STATUS_*) after the kernels.
+ * The pages have no counterpart of this call: it only changes where the
+ * scratch lives.
+ * Errors: MS_ERR_ARG, MS_ERR_SCRATCH, MS_ERR_CUDA. */
+MS_API int ms_mixed_step_attention_noalloc(const void* q_rot, const void* k_cache, const void* v_cache,
+                                           int32_t num_pages,
+                                           const int32_t* cu_seqlens_q, const int32_t* q_start_pos,
+                                           const int32_t* context_lens, const int32_t* block_tables,
+                                           int32_t bt_stride, int32_t num_rows, int32_t num_tokens,
+                                           int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D,
+                                           int32_t page_size, float scale, void* out, int32_t* dev_status,
+                                           ms_stream_t stream);
 
 /* ms_read_status -- waits for `stream`, copies the int32 device status word at
  * dev_status (for attention: the workspace pointer) to *host_status and
