@@ -48,7 +48,7 @@ constexpr int kMinSplitPages = 16;
 constexpr int kMaxSplitPages = 256;
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kChunkThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kChunkThreads = 256;  // warp 0 K/Q TMA + queue, 1 MMA, 2-5 softmax, 6 V TMA, 7 idle
 constexpr int kPrologueThreads = 1024;
 constexpr int kSortLimit = 2048;    // rows sorted longest-first up to this count
 
@@ -82,6 +82,9 @@ struct AttnParams {
   int32_t* dec_nsplit;
   int32_t* ch_rows;
   int32_t* ch_item_prefix;
+  int2* dec_items;  // per decode item: (decode row index, item within the row)
+  int2* ch_items;   // per chunk item: (chunk row index, item within the row)
+  int64_t max_dec_items, max_ch_items;
   float* part_ml;
   float* part_acc;
   int64_t max_partials;
@@ -221,6 +224,9 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
       p.dec_nsplit[k] = static_cast<int32_t>(ns);
       p.dec_item_prefix[k] = static_cast<int32_t>((dec_items + o) * p.H_kv);
       p.dec_part_base[k] = static_cast<int32_t>((parts + o) * p.H_q);
+      const int64_t i0 = (dec_items + o) * p.H_kv, n_it = ns * p.H_kv;
+      if (i0 + n_it <= p.max_dec_items)
+        for (int64_t i = 0; i < n_it; ++i) p.dec_items[i0 + i] = make_int2(k, static_cast<int>(i));
     }
     dec_items += tot;
     parts += tot;
@@ -236,11 +242,17 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
     }
     int64_t tot;
     const int64_t o = block_exclusive_scan(nq, s_warp, tot);
-    if (k < n_ch) p.ch_item_prefix[k] = static_cast<int32_t>((ch_items + o) * p.H_kv);
+    if (k < n_ch) {
+      p.ch_item_prefix[k] = static_cast<int32_t>((ch_items + o) * p.H_kv);
+      const int64_t i0 = (ch_items + o) * p.H_kv, n_it = nq * p.H_kv;
+      if (i0 + n_it <= p.max_ch_items)
+        for (int64_t i = 0; i < n_it; ++i) p.ch_items[i0 + i] = make_int2(k, static_cast<int>(i));
+    }
     ch_items += tot;
   }
   if (tid == 0) {
-    const bool overflow = parts * p.H_q > p.max_partials;
+    const bool overflow = parts * p.H_q > p.max_partials || dec_items * p.H_kv > p.max_dec_items ||
+                          ch_items * p.H_kv > p.max_ch_items;
     p.dec_item_prefix[n_dec] = static_cast<int32_t>(dec_items * p.H_kv);
     p.ch_item_prefix[n_ch] = static_cast<int32_t>(ch_items * p.H_kv);
     hdr[H_DEC_CTR] = 0;
@@ -254,21 +266,9 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
     if (overflow) {
       atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
       hdr[H_NDEC] = 0;
+      hdr[H_NCH_ITEMS] = 0;
     }
   }
-}
-
-// index k with prefix[k] <= item < prefix[k + 1]; prefix has n + 1 entries
-__device__ __forceinline__ int find_row(const int32_t* prefix, int n, int item) {
-  int lo = 0, hi = n;  // invariant: prefix[lo] <= item < prefix[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(prefix + mid) <= item)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  return lo;
 }
 
 // ----------------------------------------------------------------------------
@@ -300,10 +300,10 @@ struct DecItem {
   int part;    // partial record of query head hk * G (+ g for the others)
 };
 
-__device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, int n_dec, int split) {
+__device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, int split) {
   DecItem it;
-  const int k = find_row(p.dec_item_prefix, n_dec, item);
-  const int local = item - __ldg(p.dec_item_prefix + k);
+  const int2 kl = __ldg(p.dec_items + item);  // (decode row index, item within the row)
+  const int k = kl.x, local = kl.y;
   const int sp = local / p.H_kv;
   it.hk = local - sp * p.H_kv;
   it.k = k;
@@ -341,7 +341,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(AttnParams p) {
   uint64_t* full = reinterpret_cast<uint64_t*>(wbase + C::BAR_OFF);
   float* pbuf = reinterpret_cast<float*>(wbase + C::P_OFF);  // [G][2 halves][8]
   const int n_items = p.hdr[H_NDEC_ITEMS];
-  const int n_dec = p.hdr[H_NDEC];
   const int split = p.hdr[H_SPLIT];
   if (lane == 0) {
     for (int i = 0; i < NST; ++i) mbar_init(full + i, 1);
@@ -362,20 +361,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(AttnParams p) {
   DecItem cur, nxt;
   int cur_id = dequeue();
   if (cur_id >= n_items) return;
-  cur = describe_dec(p, cur_id, n_dec, split);
+  cur = describe_dec(p, cur_id, split);
   int nxt_id = dequeue();
   bool nxt_valid = nxt_id < n_items;
-  if (nxt_valid) nxt = describe_dec(p, nxt_id, n_dec, split);
+  if (nxt_valid) nxt = describe_dec(p, nxt_id, split);
   uint32_t seq_iss = 0, seq_con = 0;
   int iss_in_nxt = 0, iss_page = 0;
   uint32_t item_par = 0;  // q buffer of the current item
   bool failed = false;
 
+  int iss_bt = 0;  // lane j: page id (issue-cursor item, window start + j)
   auto issue_page = [&](const DecItem& it, int pi, uint32_t qpar) {
+    if ((pi & 31) == 0) {  // one coalesced load per 32 pages of an item
+      const int w = pi + lane;
+      iss_bt = w < it.np ? __ldg(p.bt + static_cast<int64_t>(it.row) * p.bt_stride + it.p0 + w) : 0;
+    }
+    int phys = __shfl_sync(0xffffffffu, iss_bt, pi & 31);
     if (lane == 0) {
       const int st = seq_iss % NST;
       uint8_t* stage = wbase + st * C::STAGE_BYTES;
-      int phys = __ldg(p.bt + static_cast<int64_t>(it.row) * p.bt_stride + it.p0 + pi);
       if (phys < 0 || phys >= p.num_pages) {
         atomicOr(p.hdr + H_STATUS, MS_STATUS_BAD_PAGE);
         phys = 0;
@@ -532,7 +536,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(AttnParams p) {
     iss_in_nxt = 0;  // the issue cursor (iss_page) already points into the new current item
     nxt_id = dequeue();
     nxt_valid = nxt_id < n_items;
-    if (nxt_valid) nxt = describe_dec(p, nxt_id, n_dec, split);
+    if (nxt_valid) nxt = describe_dec(p, nxt_id, split);
     pump();
   }
   if (failed) {
@@ -607,7 +611,7 @@ struct ChCfg {
   static constexpr int KV_OFF = NSL * kSlab;         // stage b: K at KV_OFF + b*2*NSL*kSlab, V after K
   static constexpr int P_OFF = KV_OFF + 4 * NSL * kSlab;
   static constexpr int BAR_OFF = P_OFF + 4 * kSlab;  // two P buffers of 128 rows x 128 keys
-  static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int SMEM = BAR_OFF + 512 + 1024;  // + barriers + alignment slack
   static constexpr int TMEM_COLS = 512;              // S0, S1 (128 each), O (D)
 };
 
@@ -617,7 +621,8 @@ struct ChItem {
 
 struct ChBars {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full[2], k_empty[2];  // K stage: free once the tile's S MMA is done
+  uint64_t v_full[2], v_empty[2];  // V stage: free once the tile's PV MMA is done
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t item_full[2], item_empty[2];
   uint64_t mma_done;
@@ -625,6 +630,9 @@ struct ChBars {
   int abort;
   ChItem items[2];
 };
+
+static_assert(sizeof(ChBars) <= 512, "chunk-kernel barrier block exceeds its reserved space");
+static_assert(ChCfg<128>::SMEM <= 232448, "chunk kernel exceeds the per-CTA shared-memory limit");
 
 // K-major, 128-byte-swizzled operand: slab-major 64-column blocks of 128-byte rows;
 // k-step kk (16 columns) lives in slab kk / 4 at byte offset (kk % 4) * 32.
@@ -654,7 +662,6 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.hdr[H_NCH_ITEMS];
   if (n_items == 0) return;
-  const int n_ch = p.hdr[H_NCH];
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + C::Q_OFF;
@@ -664,13 +671,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->kv_full[b], 1);
-      mbar_init(&bars->kv_empty[b], 1);
+      mbar_init(&bars->k_full[b], 1);
+      mbar_init(&bars->k_empty[b], 1);
+      mbar_init(&bars->v_full[b], 1);
+      mbar_init(&bars->v_empty[b], 1);
       mbar_init(&bars->s_full[b], 1);
       mbar_init(&bars->p_full[b], 128);
       mbar_init(&bars->o_done[b], 1);
       mbar_init(&bars->item_full[b], 1);
-      mbar_init(&bars->item_empty[b], 1 + 128);
+      mbar_init(&bars->item_empty[b], 1 + 128 + 1);  // MMA, softmax threads, V producer
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -706,8 +715,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         ChItem it;
         it.row = -1;
         if (item < n_items) {
-          const int k = find_row(p.ch_item_prefix, n_ch, item);
-          const int local = item - __ldg(p.ch_item_prefix + k);
+          const int2 kl = __ldg(p.ch_items + item);  // (chunk row index, item within the row)
+          const int k = kl.x, local = kl.y;
           it.row = __ldg(p.ch_rows + k);
           it.tb = __ldg(p.cu + it.row);
           it.d = __ldg(p.cu + it.row + 1) - it.tb;
@@ -734,33 +743,50 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         for (int s = 0; s < NSL; ++s)
           tma_load_3d(smem + C::Q_OFF + s * kSlab, &tm_q, s * 64, it.hk * G, it.tb + it.tok0, &bars->q_full);
         const int32_t* btrow = p.bt + static_cast<int64_t>(it.row) * p.bt_stride;
+        const int n_pages = (it.kv_end + kPage - 1) / kPage;
+        int pg_cur[8], pg_nxt[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pg_cur[j] = j < n_pages ? __ldg(btrow + j) : 0;
         for (int kt = 0; kt < it.n_kt; ++kt, ++g) {
-          const int b = g & 1;
-          if (g >= 2 && !mbar_wait(&bars->kv_empty[b], ((g >> 1) - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
+          // the next tile's page ids are in flight while this tile waits for its stage
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int lp = (kt + 1) * 8 + j;
+            pg_nxt[j] = lp < n_pages ? __ldg(btrow + lp) : 0;
           }
+          const int b = g & 1;
           const int keys = min(128, it.kv_end - kt * 128);
           const int npg = (keys + kPage - 1) / kPage;
-          mbar_arrive_expect_tx(&bars->kv_full[b], 2 * npg * kPage * D * 2);
-          for (int pg = 0; pg < npg; ++pg) {
-            int phys = __ldg(btrow + kt * 8 + pg);
-            if (phys < 0 || phys >= p.num_pages) {
+          int r0[8];
+#pragma unroll
+          for (int pg = 0; pg < 8; ++pg) {
+            int phys = pg_cur[pg];
+            if (pg < npg && (phys < 0 || phys >= p.num_pages)) {
               atomicOr(p.hdr + H_STATUS, MS_STATUS_BAD_PAGE);
               phys = 0;
             }
-            const int r0 = (phys * p.H_kv + it.hk) * kPage;
-            for (int s = 0; s < NSL; ++s) {
-              tma_load_2d(smem + kv_off(b) + s * kSlab + pg * 2048, &tm_k, s * 64, r0, &bars->kv_full[b]);
-              tma_load_2d(smem + kv_off(b) + (NSL + s) * kSlab + pg * 2048, &tm_v, s * 64, r0, &bars->kv_full[b]);
-            }
+            r0[pg] = (phys * p.H_kv + it.hk) * kPage;
           }
+          // K of tile g: its stage was last read by the S MMA of tile g - 2
+          if (g >= 2 && !mbar_wait(&bars->k_empty[b], ((g >> 1) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->k_full[b], npg * kPage * D * 2);
+#pragma unroll
+          for (int pg = 0; pg < 8; ++pg)
+            if (pg < npg)
+#pragma unroll
+              for (int s = 0; s < NSL; ++s)
+                tma_load_2d(smem + kv_off(b) + s * kSlab + pg * 2048, &tm_k, s * 64, r0[pg], &bars->k_full[b]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) pg_cur[j] = pg_nxt[j];
         }
       }
       if (!ok) *abort_flag = 1;
       // copies still in flight must land before the CTA exits
       for (int t = (g > 2 ? g - 2 : 0); t < g; ++t)
-        mbar_wait(&bars->kv_full[t & 1], (t >> 1) & 1, nullptr, 200000000ull);
+        mbar_wait(&bars->k_full[t & 1], (t >> 1) & 1, nullptr, 200000000ull);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (one thread)
@@ -782,40 +808,42 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         for (int kt = 0; kt <= it.n_kt; ++kt) {
           if (kt < it.n_kt) {
             const int g = it.tile0 + kt, b = g & 1;
-            if (!mbar_wait(&bars->kv_full[b], (g >> 1) & 1, abort_flag)) {
+            if (!mbar_wait(&bars->k_full[b], (g >> 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const int keys = min(128, it.kv_end - kt * 128);
             const int n_cols = (keys + 15) & ~15;
-            if (keys != n_cols) {
-              // rows past the context in the last page may hold stale (even non-finite)
-              // data: zero them in V so that P = 0 times V stays 0
-              uint8_t* v0 = smem + kv_off(b) + NSL * kSlab;
-              for (int r = keys; r < n_cols; ++r)
-                for (int s = 0; s < NSL; ++s)
-                  for (int q16 = 0; q16 < 8; ++q16)
-                    *reinterpret_cast<uint4*>(v0 + s * kSlab + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
-              fence_proxy_async_smem();
-            }
             const uint32_t idesc_s = idesc_bf16_f32(128, n_cols, 0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
               mma_bf16_ss(tS0 + b * 128, kmajor_desc(sQ, kk), kmajor_desc(sbase + kv_off(b), kk), idesc_s,
                           kk > 0 ? 1u : 0u);
             mma_commit(&bars->s_full[b]);
+            mma_commit(&bars->k_empty[b]);
             if (kt == it.n_kt - 1) mma_commit(&bars->q_empty);
           }
           if (kt >= 1) {
             const int j = kt - 1, gj = it.tile0 + j, bj = gj & 1;
-            if (!mbar_wait(&bars->p_full[bj], (gj >> 1) & 1, abort_flag)) {
+            if (!mbar_wait(&bars->v_full[bj], (gj >> 1) & 1, abort_flag) ||
+                !mbar_wait(&bars->p_full[bj], (gj >> 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const int keys = min(128, it.kv_end - j * 128);
             const int nk = (keys + 15) >> 4;
+            if (keys != nk * 16) {
+              // rows past the context in the last page may hold stale (even non-finite)
+              // data: zero them in V so that P = 0 times V stays 0
+              uint8_t* v0 = smem + kv_off(bj) + NSL * kSlab;
+              for (int r = keys; r < nk * 16; ++r)
+                for (int s = 0; s < NSL; ++s)
+                  for (int q16 = 0; q16 < 8; ++q16)
+                    *reinterpret_cast<uint4*>(v0 + s * kSlab + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+              fence_proxy_async_smem();
+            }
             const uint32_t vbase = sbase + kv_off(bj) + NSL * kSlab;
             for (int kk = 0; kk < nk; ++kk) {
               // V is the MN-major B operand: 64-column slabs one slab apart (LBO),
@@ -825,7 +853,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                           (j > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bars->o_done[bj]);
-            mma_commit(&bars->kv_empty[bj]);
+            mma_commit(&bars->v_empty[bj]);
           }
         }
         if (!ok) break;
@@ -836,11 +864,71 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       mma_commit(&bars->mma_done);
       mbar_wait(&bars->mma_done, 0, nullptr, 200000000ull);
     }
-  } else {
+  } else if (warp == 6) {
+    // ---------------------------------------------------------------- V producer
+    if (lane == 0) {
+      int g = 0;
+      bool ok = true;
+      for (int n = 0; ok; ++n) {
+        const int slot = n & 1;
+        if (!mbar_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const ChItem it = bars->items[slot];
+        if (it.row < 0) break;
+        const int32_t* btrow = p.bt + static_cast<int64_t>(it.row) * p.bt_stride;
+        const int n_pages = (it.kv_end + kPage - 1) / kPage;
+        int pg_cur[8], pg_nxt[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pg_cur[j] = j < n_pages ? __ldg(btrow + j) : 0;
+        for (int kt = 0; kt < it.n_kt; ++kt, ++g) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int lp = (kt + 1) * 8 + j;
+            pg_nxt[j] = lp < n_pages ? __ldg(btrow + lp) : 0;
+          }
+          const int b = g & 1;
+          const int keys = min(128, it.kv_end - kt * 128);
+          const int npg = (keys + kPage - 1) / kPage;
+          // V of tile g: its stage was last read by the PV MMA of tile g - 2
+          if (g >= 2 && !mbar_wait(&bars->v_empty[b], ((g >> 1) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->v_full[b], npg * kPage * D * 2);
+#pragma unroll
+          for (int pg = 0; pg < 8; ++pg) {
+            if (pg < npg) {
+              int phys = pg_cur[pg];
+              if (phys < 0 || phys >= p.num_pages) phys = 0;  // flagged by the K producer
+              const int r0 = (phys * p.H_kv + it.hk) * kPage;
+#pragma unroll
+              for (int s = 0; s < NSL; ++s)
+                tma_load_2d(smem + kv_off(b) + (NSL + s) * kSlab + pg * 2048, &tm_v, s * 64, r0,
+                            &bars->v_full[b]);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) pg_cur[j] = pg_nxt[j];
+        }
+        if (!ok) break;
+        mbar_arrive(&bars->item_empty[slot]);
+      }
+      if (!ok) *abort_flag = 1;
+      for (int t = (g > 2 ? g - 2 : 0); t < g; ++t)
+        mbar_wait(&bars->v_full[t & 1], (t >> 1) & 1, nullptr, 200000000ull);
+    }
+  } else if (warp < 6) {
     // ---------------------------------------------------------------- softmax: one query row per thread
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = p.scale_log2;
+    // A row exponentiates against m_use, the largest scaled score seen when it
+    // was last raised; it is raised (and O rescaled) only when a tile's max
+    // exceeds it by more than 2^8, so P <= 256 and O, l stay exact in fp32.
+    constexpr float kRescaleLog2 = 8.f;
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int slot = n & 1;
@@ -853,7 +941,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       const int tl = it.tok0 + r / G;  // token of this row within the chunk
       const bool valid = (r / G) < it.ntok;
       const int pos = it.c + (valid ? tl : it.tok0 + it.ntok - 1);
-      float m = -INFINITY, l = 0.f;
+      const int warp_min_pos = it.c + it.tok0 + (quad * 32) / G;  // smallest position of this warp's rows
+      float m_use = -INFINITY, l = 0.f;
       for (int kt = 0; kt < it.n_kt; ++kt) {
         const int g = it.tile0 + kt, b = g & 1;
         if (!warp_wait(&bars->s_full[b], (g >> 1) & 1, abort_flag)) {
@@ -861,37 +950,50 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           break;
         }
         tc_fence_after();
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        const uint32_t ts = tS0 + b * 128 + lane_off;
+        tmem_ld32(ts, r0);
+        tmem_ld32(ts + 32, r1);
+        tmem_ld32(ts + 64, r2);
+        tmem_ld32(ts + 96, r3);
+        tmem_wait_ld();
+        reg_fence32(r0);
+        reg_fence32(r1);
+        reg_fence32(r2);
+        reg_fence32(r3);
         float sv[128];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t rr[32];
-          tmem_ld32(tS0 + b * 128 + lane_off + cc * 32, rr);
-          tmem_wait_ld();
-          reg_fence32(rr);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sv[cc * 32 + j] = __uint_as_float(rr[j]);
+        for (int j = 0; j < 32; ++j) {
+          sv[j] = __uint_as_float(r0[j]);
+          sv[32 + j] = __uint_as_float(r1[j]);
+          sv[64 + j] = __uint_as_float(r2[j]);
+          sv[96 + j] = __uint_as_float(r3[j]);
         }
         const int key0 = kt * 128;
-        float mx = -INFINITY;
+        if (key0 + 127 > warp_min_pos) {  // diagonal or ragged tile: causal mask (warp-uniform branch)
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          const float x = (key0 + j <= pos) ? sv[j] * p.scale_log2 : -INFINITY;
-          sv[j] = x;
-          mx = fmaxf(mx, x);
+          for (int j = 0; j < 128; ++j)
+            if (key0 + j > pos) sv[j] = -INFINITY;
         }
-        const float m_new = fmaxf(m, mx);
-        const float alpha = ex2(m - m_new);
+        float mx = sv[0];
+#pragma unroll
+        for (int j = 1; j < 128; ++j) mx = fmaxf(mx, sv[j]);
+        const float mx_s = mx * sl2;
+        const bool grow = mx_s > m_use + kRescaleLog2;
+        const float m_new = grow ? mx_s : m_use;
+        const float alpha = grow ? ex2(m_use - m_new) : 1.f;
+        const float neg_m = -m_new;
         float rs = 0.f;
 #pragma unroll
         for (int j = 0; j < 128; ++j) {
-          const float e = ex2(sv[j] - m_new);
+          const float e = ex2(fmaf(sv[j], sl2, neg_m));
           sv[j] = e;
           rs += e;
         }
         l = l * alpha + rs;
-        m = m_new;
-        // rescale the running O when a row's max grew (TMEM access is warp-wide)
-        if (kt > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+        m_use = m_new;
+        // rescale the running O when a row raised its max (TMEM access is warp-wide)
+        if (kt > 0 && __any_sync(0xffffffffu, grow)) {
           if (!warp_wait(&bars->o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag)) {
             ok = false;
             break;
@@ -995,14 +1097,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 namespace {
 
 struct WsLayout {
-  size_t hdr, dec_rows, dec_item_prefix, dec_part_base, dec_nsplit, ch_rows, ch_item_prefix, part_ml, part_acc,
-      total;
-  int64_t max_partials;
+  size_t hdr, dec_rows, dec_item_prefix, dec_part_base, dec_nsplit, ch_rows, ch_item_prefix, dec_items, ch_items,
+      part_ml, part_acc, total;
+  int64_t max_partials, max_dec_items, max_ch_items;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WsLayout ws_layout(int64_t max_rows, int64_t max_context_total, int64_t H_q, int64_t D) {
+WsLayout ws_layout(int64_t max_rows, int64_t max_tokens, int64_t max_context_total, int64_t H_q, int64_t H_kv,
+                   int64_t D) {
   WsLayout w;
   size_t off = 0;
   w.hdr = off;
@@ -1019,8 +1122,16 @@ WsLayout ws_layout(int64_t max_rows, int64_t max_context_total, int64_t H_q, int
   off = align_up(off + max_rows * 4, 16);
   w.ch_item_prefix = off;
   off = align_up(off + (max_rows + 1) * 4, 256);
-  // every decode split covers >= kMinSplitPages pages: sum of splits <= ctx/256 + rows/16 + rows
-  w.max_partials = H_q * (cdiv64(max_context_total, kPage * kMinSplitPages) + 2 * max_rows);
+  // every decode split covers >= kMinSplitPages pages: splits <= ctx/256 + rows/16 + rows
+  const int64_t max_splits = cdiv64(max_context_total, kPage * kMinSplitPages) + 2 * max_rows;
+  const int64_t G = H_q / (H_kv > 0 ? H_kv : 1);
+  w.max_dec_items = H_kv * max_splits;
+  w.max_ch_items = H_kv * (cdiv64(max_tokens * G, 128) + max_rows);
+  w.dec_items = off;
+  off = align_up(off + w.max_dec_items * 8, 256);
+  w.ch_items = off;
+  off = align_up(off + w.max_ch_items * 8, 256);
+  w.max_partials = H_q * max_splits;
   w.part_ml = off;
   off = align_up(off + w.max_partials * 2 * 4, 256);
   w.part_acc = off;
@@ -1092,10 +1203,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 extern "C" MS_API size_t ms_attention_workspace_size(int32_t max_rows, int32_t max_tokens, int64_t max_context_total,
                                                      int32_t H_q, int32_t H_kv, int32_t D) {
-  (void)max_tokens;
-  (void)H_kv;
-  if (max_rows < 0 || max_context_total < 0 || H_q < 1 || (D != 64 && D != 128)) return 0;
-  return ws_layout(max_rows, max_context_total, H_q, D).total;
+  if (max_rows < 0 || max_tokens < 0 || max_context_total < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 ||
+      (D != 64 && D != 128))
+    return 0;
+  return ws_layout(max_rows, max_tokens, max_context_total, H_q, H_kv, D).total;
 }
 
 extern "C" MS_API int ms_num_sms(void) {
@@ -1122,7 +1233,7 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
   if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return MS_ERR_ARG;
-  const WsLayout w = ws_layout(num_rows, context_total, H_q, D);
+  const WsLayout w = ws_layout(num_rows, num_tokens, context_total, H_q, H_kv, D);
   if (ws_bytes < w.total) return MS_ERR_ARG;
   const int sms = num_sms();
   if (sms <= 0) return MS_ERR_CUDA;
@@ -1160,6 +1271,10 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
   p.dec_nsplit = reinterpret_cast<int32_t*>(ws + w.dec_nsplit);
   p.ch_rows = reinterpret_cast<int32_t*>(ws + w.ch_rows);
   p.ch_item_prefix = reinterpret_cast<int32_t*>(ws + w.ch_item_prefix);
+  p.dec_items = reinterpret_cast<int2*>(ws + w.dec_items);
+  p.ch_items = reinterpret_cast<int2*>(ws + w.ch_items);
+  p.max_dec_items = w.max_dec_items;
+  p.max_ch_items = w.max_ch_items;
   p.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
   p.part_acc = reinterpret_cast<float*>(ws + w.part_acc);
   p.max_partials = w.max_partials;
@@ -1257,9 +1372,11 @@ extern "C" MS_API int ms_mixed_step_attention_noalloc(const void* q_rot, const v
                                                       int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
                                                       float scale, void* out, int32_t* dev_status,
                                                       ms_stream_t stream) {
-  if (num_rows < 0 || context_total < 0 || H_q < 1 || (D != 64 && D != 128)) return MS_ERR_ARG;
+  if (num_rows < 0 || num_tokens < 0 || context_total < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 ||
+      (D != 64 && D != 128))
+    return MS_ERR_ARG;
   if (num_rows == 0) return MS_OK;
-  const size_t need = ws_layout(num_rows, context_total, H_q, D).total;
+  const size_t need = ws_layout(num_rows, num_tokens, context_total, H_q, H_kv, D).total;
   if (need > kNoAllocScratchBytes) return MS_ERR_SCRATCH;
   void* scratch = nullptr;
   const int rc0 = scratch_address(&scratch);
