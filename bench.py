@@ -284,7 +284,7 @@ def run_ours(args, world, rank, local):
                    "batches_per_step": n_sub, "l2": "inputs larger than L2 (KV pool "
                    f"{2 * k_cache.numel() * 2 / 1e9:.2f} GB); no flush", "parallelism": f"replicas x{world}"},
         "roofline": roof, "step_roofline": step_roof, "e2e": e2e,
-        "gpu_launches": 5 * n_sub * args.steps, "clocks": clocks,
+        "gpu_launches": 4 * n_sub * args.steps, "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_seconds)

@@ -47,10 +47,16 @@ constexpr int kPage = 16;
 constexpr int kMinSplitPages = 16;
 constexpr int kMaxSplitPages = 256;
 constexpr int kDecWarps = 8;
-constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kChunkThreads = 256;  // warp 0 K/Q TMA + queue, 1 MMA, 2-5 softmax, 6 V TMA, 7 idle
 constexpr int kPrologueThreads = 1024;
 constexpr int kSortLimit = 2048;    // rows sorted longest-first up to this count
+constexpr int kMaxRows = 8192;      // rows of one step
+// Cost model that splits the SMs between the two row kinds at the start of a
+// step (CTAs then move to whichever queue still has work): one 128x128 chunk
+// tile per SM, and the decode bandwidth one SM sustains, capped by HBM.
+constexpr float kChunkTileNs = 3000.f;   // per 128x128 tile and SM, alongside decode traffic
+constexpr float kDecodeSmGBs = 62.f;    // G = 1; fewer bytes per SM-cycle as G grows
+constexpr float kHbmGBs = 6500.f;
 
 // workspace header (int32 words)
 enum {
@@ -63,6 +69,7 @@ enum {
   H_NCH_ITEMS = 6,
   H_SPLIT = 7,
   H_NPART = 8,
+  H_CHUNK_CTAS = 9,  // CTAs that start on chunk work (the rest start on decodes)
   H_WORDS = 64
 };
 
@@ -83,6 +90,7 @@ struct AttnParams {
   int32_t* ch_rows;
   int32_t* ch_item_prefix;
   int2* dec_items;  // per decode item: (decode row index, item within the row)
+  int32_t* dec_cnt; // per (decode row, KV head): splits finished, for the last one to merge
   int2* ch_items;   // per chunk item: (chunk row index, item within the row)
   int64_t max_dec_items, max_ch_items;
   float* part_ml;
@@ -128,147 +136,261 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t* s_warp, int64_t& tot
   return before;
 }
 
+// Shared memory of the prologue: sort keys and per-row values of up to
+// kSortLimit rows, and the item prefix of up to kMaxRows rows.
+struct PrologueSmem {
+  int64_t key[kSortLimit];
+  int32_t id[kSortLimit];
+  int32_t d[kSortLimit];
+  int32_t c[kSortLimit];
+  int32_t pref[kMaxRows + 1];
+};
+
+// k with pref[k] <= item < pref[k + 1] (pref has n + 1 entries, in shared memory)
+__device__ __forceinline__ int find_in_prefix(const int32_t* pref, int n, int item) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] <= item)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// One CTA: validate the rows, split them into decode rows (d = 1) and chunk
+// rows (d > 1), order each list longest-first, size the decode splits, lay
+// out the per-item tables, zero the split counters and pick how many CTAs of
+// the main kernel start on chunk work.  Every row's values are read from
+// global memory once; the rest happens in registers and shared memory.
 __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParams p) {
+  extern __shared__ __align__(16) uint8_t psm_raw[];
+  PrologueSmem& sm = *reinterpret_cast<PrologueSmem*>(psm_raw);
   __shared__ int64_t s_warp[32];
   __shared__ int s_bad;
-  __shared__ unsigned long long s_ctx_sum, s_dec_pages;
-  __shared__ int64_t s_key[kSortLimit];
-  __shared__ int32_t s_idx[kSortLimit];
+  __shared__ unsigned long long s_ctx_sum, s_dec_pages, s_tiles;
+  constexpr int R = kMaxRows / kPrologueThreads;
   const int tid = threadIdx.x;
   const int S = p.num_rows;
   int32_t* hdr = p.hdr;
-  if (tid == 0) {
-    s_bad = 0;
-    s_ctx_sum = 0;
-    s_dec_pages = 0;
-  }
-  __syncthreads();
-  // 1. validate rows and count work
-  for (int s = tid; s < S; s += blockDim.x) {
-    const int32_t a = p.cu[s], b = p.cu[s + 1];
-    const int32_t d = b - a, c = p.q_start[s], ctx = p.ctx_lens[s];
-    const bool ok = a >= 0 && b <= p.num_tokens && d >= 1 && c >= 0 && ctx == c + d &&
-                    cdiv64(ctx, kPage) <= p.bt_stride;
-    if (!ok) {
-      atomicOr(&s_bad, 1);
-      continue;
+  if (tid == 0) s_tiles = 0;
+  // 1. this thread's rows s = tid + i * 1024: load, validate, count (block sums, no atomics)
+  int rd[R], rc[R];
+  int64_t my_ctx = 0, my_pages = 0;
+  int my_bad = S > kMaxRows;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int s = tid + i * kPrologueThreads;
+    rd[i] = 0;
+    rc[i] = 0;
+    if (s < S && S <= kMaxRows) {
+      const int32_t a = p.cu[s], b = p.cu[s + 1];
+      const int32_t d = b - a, c = p.q_start[s], ctx = p.ctx_lens[s];
+      const bool ok = a >= 0 && b <= p.num_tokens && d >= 1 && c >= 0 && ctx == c + d &&
+                      cdiv64(ctx, kPage) <= p.bt_stride;
+      if (ok) {
+        rd[i] = d;
+        rc[i] = c;
+        my_ctx += ctx;
+        if (d == 1) my_pages += (ctx + kPage - 1) / kPage;
+      } else {
+        my_bad = 1;
+      }
     }
-    atomicAdd(&s_ctx_sum, static_cast<unsigned long long>(ctx));
-    if (d == 1) atomicAdd(&s_dec_pages, static_cast<unsigned long long>(cdiv64(ctx, kPage)));
   }
-  __syncthreads();
-  const bool bad = s_bad != 0 || static_cast<int64_t>(s_ctx_sum) > p.context_total;
-  if (bad) {
+  {
+    int64_t tot;
+    block_exclusive_scan(my_ctx, s_warp, tot);
+    if (tid == 0) s_ctx_sum = static_cast<unsigned long long>(tot);
+    block_exclusive_scan(my_pages, s_warp, tot);
+    if (tid == 0) s_dec_pages = static_cast<unsigned long long>(tot);
+    block_exclusive_scan(my_bad, s_warp, tot);
+    if (tid == 0) s_bad = tot != 0;
+    __syncthreads();
+  }
+  if (s_bad != 0 || static_cast<int64_t>(s_ctx_sum) > p.context_total) {
     if (tid == 0) {
       atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
       hdr[H_DEC_CTR] = hdr[H_CH_CTR] = 0;
       hdr[H_NDEC] = hdr[H_NDEC_ITEMS] = hdr[H_NCH] = hdr[H_NCH_ITEMS] = hdr[H_NPART] = 0;
       hdr[H_SPLIT] = kMinSplitPages;
+      hdr[H_CHUNK_CTAS] = 0;
       p.dec_item_prefix[0] = 0;
       p.ch_item_prefix[0] = 0;
     }
     return;
   }
-  // 2. split size: about 16 items per decode worker, clamped
+  // 2. decode split size: about 16 items per decode worker warp, clamped
   int64_t split = cdiv64(static_cast<int64_t>(s_dec_pages) * p.H_kv, static_cast<int64_t>(p.dec_workers) * 16);
   split = split < kMinSplitPages ? kMinSplitPages : (split > kMaxSplitPages ? kMaxSplitPages : split);
-  // 3. stable compaction of decode rows and chunk rows
-  int64_t n_dec = 0, n_ch = 0;
-  for (int base = 0; base < S; base += blockDim.x) {
-    const int s = base + tid;
-    int is_dec = 0, is_ch = 0;
-    if (s < S) {
-      const int d = p.cu[s + 1] - p.cu[s];
-      is_dec = d == 1;
-      is_ch = d > 1;
-    }
-    int64_t tot_dec, tot_ch;
-    const int64_t o_dec = block_exclusive_scan(is_dec, s_warp, tot_dec);
-    const int64_t o_ch = block_exclusive_scan(is_ch, s_warp, tot_ch);
-    if (is_dec) p.dec_rows[n_dec + o_dec] = s;
-    if (is_ch) p.ch_rows[n_ch + o_ch] = s;
-    n_dec += tot_dec;
-    n_ch += tot_ch;
-  }
-  __syncthreads();
-  // 4. longest first (stable): decodes by context, chunks by causal pairs
-  for (int kind = 0; kind < 2; ++kind) {
-    int32_t* rows = kind == 0 ? p.dec_rows : p.ch_rows;
-    const int n = static_cast<int>(kind == 0 ? n_dec : n_ch);
-    if (n <= 1 || n > kSortLimit) continue;
-    for (int i = tid; i < n; i += blockDim.x) {
-      const int s = rows[i];
-      const int64_t c = p.q_start[s], d = p.cu[s + 1] - p.cu[s];
-      const int64_t cost = kind == 0 ? c + 1 : d * (2 * c + d + 1) / 2;
-      s_key[i] = (cost << 16) | (0xffff - (i & 0xffff));  // ties keep input order
-      s_idx[i] = s;
-    }
-    __syncthreads();
-    for (int i = tid; i < n; i += blockDim.x) {
-      int rank = 0;
-      const int64_t k = s_key[i];
-      for (int j = 0; j < n; ++j) rank += s_key[j] > k;
-      rows[rank] = s_idx[i];
-    }
-    __syncthreads();
-  }
-  // 5. item prefixes and partial bases
-  int64_t dec_items = 0, parts = 0;
-  for (int base = 0; base < n_dec; base += blockDim.x) {
-    const int k = base + tid;
-    int64_t ns = 0;
-    if (k < n_dec) ns = cdiv64(cdiv64(p.ctx_lens[p.dec_rows[k]], kPage), split);
-    int64_t tot;
-    const int64_t o = block_exclusive_scan(ns, s_warp, tot);
-    if (k < n_dec) {
-      p.dec_nsplit[k] = static_cast<int32_t>(ns);
-      p.dec_item_prefix[k] = static_cast<int32_t>((dec_items + o) * p.H_kv);
-      p.dec_part_base[k] = static_cast<int32_t>((parts + o) * p.H_q);
-      const int64_t i0 = (dec_items + o) * p.H_kv, n_it = ns * p.H_kv;
-      if (i0 + n_it <= p.max_dec_items)
-        for (int64_t i = 0; i < n_it; ++i) p.dec_items[i0 + i] = make_int2(k, static_cast<int>(i));
-    }
-    dec_items += tot;
-    parts += tot;
-  }
-  int64_t ch_items = 0;
   const int tpt = 128 / p.G;
-  for (int base = 0; base < n_ch; base += blockDim.x) {
-    const int k = base + tid;
-    int64_t nq = 0;
-    if (k < n_ch) {
-      const int s = p.ch_rows[k];
-      nq = cdiv64(p.cu[s + 1] - p.cu[s], tpt);
+  // 3. the two row lists, each in input order first
+  int dpos[R], cpos[R];
+  int64_t n_dec = 0, n_ch = 0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    dpos[i] = -1;
+    cpos[i] = -1;
+    if (i * kPrologueThreads < S) {  // uniform
+      const int is_dec = rd[i] == 1, is_ch = rd[i] > 1;
+      int64_t tot_dec, tot_ch;
+      const int64_t o_dec = block_exclusive_scan(is_dec, s_warp, tot_dec);
+      const int64_t o_ch = block_exclusive_scan(is_ch, s_warp, tot_ch);
+      dpos[i] = is_dec ? static_cast<int>(n_dec + o_dec) : -1;
+      cpos[i] = is_ch ? static_cast<int>(n_ch + o_ch) : -1;
+      n_dec += tot_dec;
+      n_ch += tot_ch;
     }
-    int64_t tot;
-    const int64_t o = block_exclusive_scan(nq, s_warp, tot);
-    if (k < n_ch) {
-      p.ch_item_prefix[k] = static_cast<int32_t>((ch_items + o) * p.H_kv);
-      const int64_t i0 = (ch_items + o) * p.H_kv, n_it = nq * p.H_kv;
-      if (i0 + n_it <= p.max_ch_items)
-        for (int64_t i = 0; i < n_it; ++i) p.ch_items[i0 + i] = make_int2(k, static_cast<int>(i));
+  }
+  // 4. each list longest first (stable), then item counts in queue order
+  for (int kind = 0; kind < 2; ++kind) {
+    const int n = static_cast<int>(kind == 0 ? n_dec : n_ch);
+    int32_t* rows = kind == 0 ? p.dec_rows : p.ch_rows;
+    const bool sorted = n <= kSortLimit;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int s = tid + i * kPrologueThreads;
+      const int pos = kind == 0 ? dpos[i] : cpos[i];
+      if (s >= S || pos < 0) continue;
+      const int64_t c = rc[i], d = rd[i];
+      if (sorted) {
+        const int64_t cost = kind == 0 ? c + 1 : d * (2 * c + d + 1) / 2;
+        sm.key[pos] = (cost << 16) | (0xffff - (pos & 0xffff));  // ties keep input order
+        sm.id[pos] = s;
+        sm.d[pos] = static_cast<int32_t>(d);
+        sm.c[pos] = static_cast<int32_t>(c);
+      } else {
+        rows[pos] = s;
+        const int64_t items = kind == 0 ? cdiv64(cdiv64(c + 1, kPage), split) : cdiv64(d, tpt);
+        sm.pref[pos] = static_cast<int32_t>(items);
+        if (kind == 1) {
+          unsigned long long tiles = 0;
+          for (int64_t qt = 0; qt < items; ++qt) tiles += cdiv64(c + (d < (qt + 1) * tpt ? d : (qt + 1) * tpt), 128);
+          atomicAdd(&s_tiles, tiles * p.H_kv);
+        }
+      }
     }
-    ch_items += tot;
+    __syncthreads();
+    if (sorted) {
+      for (int j = tid; j < n; j += kPrologueThreads) {
+        const int64_t k = sm.key[j];
+        int rank = 0;
+        for (int m = 0; m < n; ++m) rank += sm.key[m] > k;
+        rows[rank] = sm.id[j];
+        const int64_t c = sm.c[j], d = sm.d[j];
+        const int64_t items = kind == 0 ? cdiv64(cdiv64(c + 1, kPage), split) : cdiv64(d, tpt);
+        sm.pref[rank] = static_cast<int32_t>(items);
+        if (kind == 1) {
+          unsigned long long tiles = 0;
+          for (int64_t qt = 0; qt < items; ++qt) tiles += cdiv64(c + (d < (qt + 1) * tpt ? d : (qt + 1) * tpt), 128);
+          atomicAdd(&s_tiles, tiles * p.H_kv);
+        }
+      }
+      __syncthreads();
+    }
+    // 5. exclusive prefix of the per-row item counts (times H_kv) in queue order
+    int64_t run = 0;
+    for (int base = 0; base < n; base += kPrologueThreads) {
+      const int k = base + tid;
+      const int64_t v = k < n ? sm.pref[k] : 0;
+      int64_t tot;
+      const int64_t o = block_exclusive_scan(v, s_warp, tot);
+      if (k < n) {
+        const int64_t first = (run + o) * p.H_kv;
+        sm.pref[k] = static_cast<int32_t>(first);
+        if (kind == 0) {
+          p.dec_item_prefix[k] = static_cast<int32_t>(first);
+          p.dec_part_base[k] = static_cast<int32_t>((run + o) * p.H_q);
+          p.dec_nsplit[k] = static_cast<int32_t>(v);
+        } else {
+          p.ch_item_prefix[k] = static_cast<int32_t>(first);
+        }
+      }
+      run += tot;
+    }
+    const int64_t n_items = run * p.H_kv;
+    const int64_t cap = kind == 0 ? p.max_dec_items : p.max_ch_items;
+    const bool overflow = n_items > cap || (kind == 0 && run * p.H_q > p.max_partials);
+    if (tid == 0) {
+      sm.pref[n] = static_cast<int32_t>(n_items);
+      if (kind == 0) {
+        p.dec_item_prefix[n] = static_cast<int32_t>(n_items);
+        hdr[H_NDEC] = overflow ? 0 : static_cast<int32_t>(n_dec);
+        hdr[H_NDEC_ITEMS] = overflow ? 0 : static_cast<int32_t>(n_items);
+        hdr[H_NPART] = static_cast<int32_t>(run * p.H_q);
+      } else {
+        p.ch_item_prefix[n] = static_cast<int32_t>(n_items);
+        hdr[H_NCH] = overflow ? 0 : static_cast<int32_t>(n_ch);
+        hdr[H_NCH_ITEMS] = overflow ? 0 : static_cast<int32_t>(n_items);
+      }
+      if (overflow) atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
+    }
+    __syncthreads();
+    __syncthreads();
   }
   if (tid == 0) {
-    const bool overflow = parts * p.H_q > p.max_partials || dec_items * p.H_kv > p.max_dec_items ||
-                          ch_items * p.H_kv > p.max_ch_items;
-    p.dec_item_prefix[n_dec] = static_cast<int32_t>(dec_items * p.H_kv);
-    p.ch_item_prefix[n_ch] = static_cast<int32_t>(ch_items * p.H_kv);
     hdr[H_DEC_CTR] = 0;
     hdr[H_CH_CTR] = 0;
-    hdr[H_NDEC] = static_cast<int32_t>(n_dec);
-    hdr[H_NDEC_ITEMS] = overflow ? 0 : static_cast<int32_t>(dec_items * p.H_kv);
-    hdr[H_NCH] = static_cast<int32_t>(n_ch);
-    hdr[H_NCH_ITEMS] = static_cast<int32_t>(ch_items * p.H_kv);
     hdr[H_SPLIT] = static_cast<int32_t>(split);
-    hdr[H_NPART] = static_cast<int32_t>(parts * p.H_q);
-    if (overflow) {
-      atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
-      hdr[H_NDEC] = 0;
-      hdr[H_NCH_ITEMS] = 0;
-    }
   }
+  // 7. starting split of the SMs between chunk tiles and decode pages: warp 0
+  // evaluates every split in fp32 (fp64 is slow on this part) and keeps the best
+  if (tid < 32) {
+    const int sms = p.dec_workers / kDecWarps;
+    const float t_tiles = static_cast<float>(s_tiles) * kChunkTileNs;  // SM-ns of chunk work
+    const float dec_bytes = static_cast<float>(s_dec_pages) * p.H_kv * kPage * p.D * 4.f;
+    const float sm_gbs = kDecodeSmGBs / (1.f + 0.18f * (p.G - 1));
+    float best_t = 3.0e38f;
+    int best_n = sms;
+    for (int n = tid; n <= sms; n += 32) {
+      const float tc = s_tiles == 0 ? 0.f : (n == 0 ? 3.0e38f : t_tiles / n);
+      const float bw = fminf((sms - n) * sm_gbs, kHbmGBs);
+      const float td = dec_bytes == 0.f ? 0.f : (n == sms ? 3.0e38f : dec_bytes / bw);
+      const float t = fmaxf(tc, td);
+      if (t <= best_t * 1.0001f) {  // ties: more chunk CTAs while decode stays HBM-bound
+        best_t = fminf(t, best_t);
+        best_n = n;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
+      const int on = __shfl_xor_sync(0xffffffffu, best_n, o);
+      if (ot < best_t * 0.9999f || (ot <= best_t * 1.0001f && on > best_n)) {
+        best_t = ot;
+        best_n = on;
+      }
+    }
+    if (tid == 0) hdr[H_CHUNK_CTAS] = best_n;
+  }
+}
+
+// Item tables: item i of a list -> (row index in queue order, item within the
+// row), found by binary search over the list's item prefix staged in shared
+// memory; also zeroes the per-(decode row, KV head) split counters.  Runs on
+// many CTAs right after the prologue.
+constexpr int kItemThreads = 512;
+__global__ void __launch_bounds__(kItemThreads) items_kernel(AttnParams p) {
+  __shared__ int32_t pref[kMaxRows + 1];
+  for (int kind = 0; kind < 2; ++kind) {
+    const int n = kind == 0 ? p.hdr[H_NDEC] : p.hdr[H_NCH];
+    const int n_items = kind == 0 ? p.hdr[H_NDEC_ITEMS] : p.hdr[H_NCH_ITEMS];
+    const int32_t* gp = kind == 0 ? p.dec_item_prefix : p.ch_item_prefix;
+    if (n_items == 0) continue;  // uniform
+    for (int k = threadIdx.x; k <= n; k += kItemThreads) pref[k] = __ldg(gp + k);
+    __syncthreads();
+    int2* out = kind == 0 ? p.dec_items : p.ch_items;
+    for (int it = blockIdx.x * kItemThreads + threadIdx.x; it < n_items; it += gridDim.x * kItemThreads) {
+      const int k = find_in_prefix(pref, n, it);
+      out[it] = make_int2(k, it - pref[k]);
+    }
+    __syncthreads();
+  }
+  const int64_t n_cnt = static_cast<int64_t>(p.hdr[H_NDEC]) * p.H_kv;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kItemThreads + threadIdx.x; i < n_cnt;
+       i += static_cast<int64_t>(gridDim.x) * kItemThreads)
+    p.dec_cnt[i] = 0;
 }
 
 // ----------------------------------------------------------------------------
@@ -298,6 +420,7 @@ struct DecItem {
   int ctx;     // keys of the row (c + 1)
   int tok;     // packed token index of the row's query
   int part;    // partial record of query head hk * G (+ g for the others)
+  int ns;      // splits of the row
 };
 
 __device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, int split) {
@@ -314,6 +437,7 @@ __device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, i
   it.p0 = sp * split;
   it.np = min(split, n_pages - it.p0);
   it.part = __ldg(p.dec_part_base + k) + sp * p.H_q + it.hk * p.G;
+  it.ns = __ldg(p.dec_nsplit + k);
   return it;
 }
 
@@ -331,11 +455,68 @@ __device__ __forceinline__ void lds_row(const bf16* src, float (&f)[EPL]) {
   }
 }
 
+// Merge the ns split records of decode row k for query heads h0 .. h0+nh-1
+// into bf16 output (one warp; lane owns D/32 columns).  Records written by
+// other SMs are read past L1.
+template <int D>
+__device__ __forceinline__ void merge_splits(const AttnParams& p, int k, int h0, int nh, int tok, int ns,
+                                             int lane) {
+  constexpr int EPL = D / 32;
+  const int64_t base0 = __ldcg(p.dec_part_base + k);
+  for (int hq = h0; hq < h0 + nh; ++hq) {
+    const int64_t base = base0 + hq;
+    // lanes over splits for (max, sum); then every lane walks the splits for its columns
+    float M = -INFINITY;
+    for (int j = lane; j < ns; j += 32)
+      M = fmaxf(M, __ldcg(p.part_ml + (base + static_cast<int64_t>(j) * p.H_q) * 2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f, o[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+    for (int j0 = 0; j0 < ns; j0 += 32) {
+      const int j = j0 + lane;
+      float w = 0.f;
+      if (j < ns) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (base + static_cast<int64_t>(j) * p.H_q) * 2));
+        w = ex2(ml.x - M);
+        L += w * ml.y;
+      }
+      const int nj = min(32, ns - j0);
+#pragma unroll 4
+      for (int jj = 0; jj < nj; ++jj) {
+        const float wj = __shfl_sync(0xffffffffu, w, jj);
+        const float* src = p.part_acc + (base + static_cast<int64_t>(j0 + jj) * p.H_q) * D + lane * EPL;
+        if constexpr (EPL == 4) {
+          const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+          o[0] += wj * a.x; o[1] += wj * a.y; o[2] += wj * a.z; o[3] += wj * a.w;
+        } else {
+          const float2 a = __ldcg(reinterpret_cast<const float2*>(src));
+          o[0] += wj * a.x; o[1] += wj * a.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+    const float inv = 1.f / L;
+    bf16* dst = p.out + (static_cast<int64_t>(tok) * p.H_q + hq) * D + lane * EPL;
+    if constexpr (EPL == 4) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(o[0] * inv, o[1] * inv);
+      __nv_bfloat162 b = __floats2bfloat162_rn(o[2] * inv, o[3] * inv);
+      *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(o[0] * inv, o[1] * inv);
+      *reinterpret_cast<__nv_bfloat162*>(dst) = a;
+    }
+  }
+}
+
+// Decode phase: each of the CTA's 8 warps is an independent worker over its
+// own slice of shared memory, pulling decode items until the queue is empty.
 template <int D, int G>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(AttnParams p) {
+__device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem) {
   using C = DecCfg<D, G>;
   constexpr int EPL = C::EPL, NST = C::NST;
-  extern __shared__ __align__(128) uint8_t dsmem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint8_t* wbase = dsmem + warp * C::WARP_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(wbase + C::BAR_OFF);
@@ -508,7 +689,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(AttnParams p) {
       pump();
     }
     if (failed) break;
-    // partial record of each query head: (max, sum) and the unnormalised accumulator
+    // Per query head: one split writes the normalised bf16 output itself;
+    // otherwise it leaves a partial record (max, sum, unnormalised accumulator)
+    // and the last split of the (row, KV head) to finish merges them all.
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float lt = l[g];
@@ -517,6 +700,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(AttnParams p) {
       float a[EPL];
 #pragma unroll
       for (int e = 0; e < EPL; ++e) a[e] = acc[g][e] + __shfl_xor_sync(0xffffffffu, acc[g][e], 16);
+      if (cur.ns == 1) {
+        if (h == 0) {
+          const float inv = 1.f / lt;
+          bf16* dst = p.out + (static_cast<int64_t>(cur.tok) * p.H_q + cur.hk * G + g) * D + sub * EPL;
+          uint32_t w[EPL / 2];
+#pragma unroll
+          for (int e = 0; e < EPL / 2; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(a[2 * e] * inv, a[2 * e + 1] * inv);
+            w[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          if constexpr (EPL == 8)
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+          else
+            *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+        }
+        continue;
+      }
       const int64_t rec = cur.part + g;
       if (h == 0) {
         float* dst = p.part_acc + rec * D + sub * EPL;
@@ -528,6 +728,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(AttnParams p) {
         }
       }
       if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + rec * 2) = make_float2(m[g], lt);
+    }
+    if (cur.ns > 1) {
+      __threadfence();  // this split's records are visible before it is counted
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(p.dec_cnt + cur.k * p.H_kv + cur.hk, 1) == cur.ns - 1;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        merge_splits<D>(p, cur.k, cur.hk * G, G, cur.tok, cur.ns, lane);
+      }
     }
     if (!nxt_valid) break;
     // advance: the next item becomes current; dequeue one more
@@ -546,55 +757,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(AttnParams p) {
       mbar_wait(full + seq_con % NST, (seq_con / NST) & 1u, nullptr, 200000000ull);
       ++seq_con;
     }
-  }
-}
-
-// ----------------------------------------------------------------------------
-// split combine for decode rows
-// ----------------------------------------------------------------------------
-
-template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
-  constexpr int EPL = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int n_dec = p.hdr[H_NDEC];
-  if (gw >= n_dec * p.H_q) return;
-  const int k = gw / p.H_q, hq = gw - k * p.H_q;
-  const int row = p.dec_rows[k];
-  const int ns = p.dec_nsplit[k];
-  const int64_t base = p.dec_part_base[k] + hq;
-  float M = -INFINITY;
-  for (int j = 0; j < ns; ++j) M = fmaxf(M, p.part_ml[(base + static_cast<int64_t>(j) * p.H_q) * 2]);
-  float L = 0.f, o[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-  for (int j = 0; j < ns; ++j) {
-    const int64_t rec = base + static_cast<int64_t>(j) * p.H_q;
-    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + rec * 2);
-    const float w = ex2(ml.x - M);
-    L += w * ml.y;
-    const float* src = p.part_acc + rec * D + lane * EPL;
-    if constexpr (EPL == 4) {
-      const float4 a = *reinterpret_cast<const float4*>(src);
-      o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
-    } else {
-      const float2 a = *reinterpret_cast<const float2*>(src);
-      o[0] += w * a.x; o[1] += w * a.y;
-    }
-  }
-  const float inv = 1.f / L;
-  bf16* dst = p.out + (static_cast<int64_t>(p.cu[row]) * p.H_q + hq) * D + lane * EPL;
-  if constexpr (EPL == 4) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(o[0] * inv, o[1] * inv);
-    __nv_bfloat162 b = __floats2bfloat162_rn(o[2] * inv, o[3] * inv);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(dst) = u;
-  } else {
-    __nv_bfloat162 a = __floats2bfloat162_rn(o[0] * inv, o[1] * inv);
-    *reinterpret_cast<__nv_bfloat162*>(dst) = a;
   }
 }
 
@@ -649,19 +811,23 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return ok != 0;
 }
 
+// Chunk phase: warp 0 streams Q and K (and owns the work queue), warp 1 issues
+// the MMAs, warps 2-5 run the softmax (one query row per thread), warp 6 streams
+// V.  Returns when the chunk queue is empty; the caller owns TMEM and the
+// barrier invalidation.
 template <int D, int G>
-__global__ void __launch_bounds__(kChunkThreads, 1)
-    chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, AttnParams p) {
+__device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtensorMap* tm_k_p,
+                                            const CUtensorMap* tm_v_p, const AttnParams& p, uint8_t* smem,
+                                            uint32_t tmem) {
   using C = ChCfg<D>;
   constexpr int NSL = C::NSL;
   constexpr int TPT = 128 / G;  // query tokens per 128-row tile
-  extern __shared__ uint8_t csmem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(csmem_raw) + 1023) & ~uintptr_t(1023));
+  const CUtensorMap& tm_q = *tm_q_p;
+  const CUtensorMap& tm_k = *tm_k_p;
+  const CUtensorMap& tm_v = *tm_v_p;
   ChBars* bars = reinterpret_cast<ChBars*>(smem + C::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.hdr[H_NCH_ITEMS];
-  if (n_items == 0) return;
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + C::Q_OFF;
@@ -685,14 +851,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
-    tmem_alloc(&bars->tmem, C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem;
   const uint32_t tS0 = tmem, tO = tmem + 256;
   volatile int* abort_flag = &bars->abort;
 
@@ -975,21 +1134,27 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
           for (int j = 0; j < 128; ++j)
             if (key0 + j > pos) sv[j] = -INFINITY;
         }
-        float mx = sv[0];
+        // eight independent max / sum chains: one warp per scheduler has no other latency cover
+        float mxa[8];
 #pragma unroll
-        for (int j = 1; j < 128; ++j) mx = fmaxf(mx, sv[j]);
+        for (int a = 0; a < 8; ++a) mxa[a] = sv[a];
+#pragma unroll
+        for (int j = 8; j < 128; ++j) mxa[j & 7] = fmaxf(mxa[j & 7], sv[j]);
+        const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                               fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
         const float mx_s = mx * sl2;
         const bool grow = mx_s > m_use + kRescaleLog2;
         const float m_new = grow ? mx_s : m_use;
         const float alpha = grow ? ex2(m_use - m_new) : 1.f;
         const float neg_m = -m_new;
-        float rs = 0.f;
+        float rsa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 128; ++j) {
           const float e = ex2(fmaf(sv[j], sl2, neg_m));
           sv[j] = e;
-          rs += e;
+          rsa[j & 7] += e;
         }
+        const float rs = ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3])) + ((rsa[4] + rsa[5]) + (rsa[6] + rsa[7]));
         l = l * alpha + rs;
         m_use = m_new;
         // rescale the running O when a row raised its max (TMEM access is warp-wide)
@@ -1080,13 +1245,72 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       if (lane == 0) atomicOr(p.hdr + H_STATUS, MS_STATUS_TIMEOUT);
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+  (void)n_items;
+}
+
+// barriers of one finished phase, invalidated before the memory is reused
+template <int D, int G>
+__device__ __forceinline__ void invalidate_phase_barriers(uint8_t* smem, bool chunk) {
+  if (chunk) {
+    if (threadIdx.x == 0) {
+      ChBars* bars = reinterpret_cast<ChBars*>(smem + ChCfg<D>::BAR_OFF);
+      uint64_t* b0 = &bars->q_full;
+      uint64_t* b1 = &bars->mma_done;
+      for (uint64_t* b = b0; b <= b1; ++b) mbar_inval(b);
+    }
+  } else if ((threadIdx.x & 31) == 0) {
+    using C = DecCfg<D, G>;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (threadIdx.x >> 5) * C::WARP_BYTES + C::BAR_OFF);
+    for (int i = 0; i < C::NST; ++i) mbar_inval(full + i);
   }
 }
+
+// One persistent CTA per SM.  CTAs below hdr[H_CHUNK_CTAS] start on chunk
+// tiles (tensor cores), the others on decode items (HBM), so the two kinds of
+// work run side by side; a CTA whose queue runs dry moves to the other queue.
+template <int D, int G>
+__global__ void __launch_bounds__(kChunkThreads, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, AttnParams p) {
+  extern __shared__ uint8_t asmem_raw[];
+  __shared__ uint32_t s_tmem;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(asmem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int n_ch_items = p.hdr[H_NCH_ITEMS];
+  const int n_dec_items = p.hdr[H_NDEC_ITEMS];
+  if (n_ch_items == 0 && n_dec_items == 0) return;
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, ChCfg<D>::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const bool chunk_first = static_cast<int>(blockIdx.x) < p.hdr[H_CHUNK_CTAS];
+  for (int ph = 0; ph < 2; ++ph) {
+    const bool chunk = (ph == 0) == chunk_first;
+    if (chunk && n_ch_items > 0) {
+      chunk_phase<D, G>(&tm_q, &tm_k, &tm_v, p, smem, tmem);
+      tc_fence_before();
+      __syncthreads();
+      const bool aborted = reinterpret_cast<ChBars*>(smem + ChCfg<D>::BAR_OFF)->abort != 0;
+      invalidate_phase_barriers<D, G>(smem, true);
+      __syncthreads();
+      if (aborted) break;
+    } else if (!chunk && n_dec_items > 0) {
+      decode_phase<D, G>(p, smem);
+      __syncwarp();
+      invalidate_phase_barriers<D, G>(smem, false);
+      __syncthreads();
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ChCfg<D>::TMEM_COLS);
+  }
+}
+
 
 }  // namespace
 
@@ -1097,8 +1321,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 namespace {
 
 struct WsLayout {
-  size_t hdr, dec_rows, dec_item_prefix, dec_part_base, dec_nsplit, ch_rows, ch_item_prefix, dec_items, ch_items,
-      part_ml, part_acc, total;
+  size_t hdr, dec_rows, dec_item_prefix, dec_part_base, dec_nsplit, ch_rows, ch_item_prefix, dec_cnt, dec_items,
+      ch_items, part_ml, part_acc, total;
   int64_t max_partials, max_dec_items, max_ch_items;
 };
 
@@ -1121,7 +1345,9 @@ WsLayout ws_layout(int64_t max_rows, int64_t max_tokens, int64_t max_context_tot
   w.ch_rows = off;
   off = align_up(off + max_rows * 4, 16);
   w.ch_item_prefix = off;
-  off = align_up(off + (max_rows + 1) * 4, 256);
+  off = align_up(off + (max_rows + 1) * 4, 16);
+  w.dec_cnt = off;
+  off = align_up(off + max_rows * H_kv * 4, 256);
   // every decode split covers >= kMinSplitPages pages: splits <= ctx/256 + rows/16 + rows
   const int64_t max_splits = cdiv64(max_context_total, kPage * kMinSplitPages) + 2 * max_rows;
   const int64_t G = H_q / (H_kv > 0 ? H_kv : 1);
@@ -1180,20 +1406,17 @@ int num_sms() {
 
 template <int D, int G>
 int launch_paths(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                 int n_chunk_ctas, int n_dec_ctas, cudaStream_t st) {
+                 int n_ctas, cudaStream_t st) {
+  constexpr int smem = ChCfg<D>::SMEM > DecCfg<D, G>::SMEM + 1024 ? ChCfg<D>::SMEM : DecCfg<D, G>::SMEM + 1024;
+  static_assert(smem <= 232448, "attention kernel exceeds the per-CTA shared-memory limit");
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DecCfg<D, G>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(chunk_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, ChCfg<D>::SMEM) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(attention_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
       return MS_ERR_CUDA;
     configured = true;
   }
-  if (n_chunk_ctas > 0) chunk_kernel<D, G><<<n_chunk_ctas, kChunkThreads, ChCfg<D>::SMEM, st>>>(tq, tk, tv, p);
-  if (n_dec_ctas > 0) decode_kernel<D, G><<<n_dec_ctas, kDecThreads, DecCfg<D, G>::SMEM, st>>>(p);
-  const int64_t warps = static_cast<int64_t>(p.num_rows) * p.H_q;
-  if (warps > 0) combine_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(p);
+  attention_kernel<D, G><<<n_ctas, kChunkThreads, smem, st>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? MS_OK : MS_ERR_CUDA;
 }
 
@@ -1272,6 +1495,7 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
   p.ch_rows = reinterpret_cast<int32_t*>(ws + w.ch_rows);
   p.ch_item_prefix = reinterpret_cast<int32_t*>(ws + w.ch_item_prefix);
   p.dec_items = reinterpret_cast<int2*>(ws + w.dec_items);
+  p.dec_cnt = reinterpret_cast<int32_t*>(ws + w.dec_cnt);
   p.ch_items = reinterpret_cast<int2*>(ws + w.ch_items);
   p.max_dec_items = w.max_dec_items;
   p.max_ch_items = w.max_ch_items;
@@ -1290,23 +1514,28 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
   p.dec_workers = sms * kDecWarps;
   p.scale_log2 = scale * 1.4426950408889634f;
 
+  if (num_rows > kMaxRows) return MS_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  prologue_kernel<<<1, kPrologueThreads, 0, st>>>(p);
-  // chunk work: at most one persistent CTA per SM, and no more than the tiles there can be
-  const int64_t tpt = 128 / G;
-  const int64_t max_chunk_items = (cdiv64(num_tokens, tpt) + num_rows) * H_kv;
-  const int n_chunk_ctas = static_cast<int>(max_chunk_items < sms ? max_chunk_items : sms);
-  const int n_dec_ctas = sms;
+  static bool prologue_configured = false;
+  if (!prologue_configured) {
+    if (cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             sizeof(PrologueSmem)) != cudaSuccess)
+      return MS_ERR_CUDA;
+    prologue_configured = true;
+  }
+  prologue_kernel<<<1, kPrologueThreads, sizeof(PrologueSmem), st>>>(p);
+  items_kernel<<<sms < 64 ? sms : 64, kItemThreads, 0, st>>>(p);
+  const int n_ctas = sms;  // one persistent CTA per SM
   int rc = MS_ERR_ARG;
   switch (D * 100 + G) {
-    case 6401: rc = launch_paths<64, 1>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
-    case 6402: rc = launch_paths<64, 2>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
-    case 6404: rc = launch_paths<64, 4>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
-    case 6408: rc = launch_paths<64, 8>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
-    case 12801: rc = launch_paths<128, 1>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
-    case 12802: rc = launch_paths<128, 2>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
-    case 12804: rc = launch_paths<128, 4>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
-    case 12808: rc = launch_paths<128, 8>(p, tq, tk, tv, n_chunk_ctas, n_dec_ctas, st); break;
+    case 6401: rc = launch_paths<64, 1>(p, tq, tk, tv, n_ctas, st); break;
+    case 6402: rc = launch_paths<64, 2>(p, tq, tk, tv, n_ctas, st); break;
+    case 6404: rc = launch_paths<64, 4>(p, tq, tk, tv, n_ctas, st); break;
+    case 6408: rc = launch_paths<64, 8>(p, tq, tk, tv, n_ctas, st); break;
+    case 12801: rc = launch_paths<128, 1>(p, tq, tk, tv, n_ctas, st); break;
+    case 12802: rc = launch_paths<128, 2>(p, tq, tk, tv, n_ctas, st); break;
+    case 12804: rc = launch_paths<128, 4>(p, tq, tk, tv, n_ctas, st); break;
+    case 12808: rc = launch_paths<128, 8>(p, tq, tk, tv, n_ctas, st); break;
     default: break;
   }
   return rc;
