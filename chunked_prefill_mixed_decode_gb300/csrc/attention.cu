@@ -47,7 +47,8 @@ constexpr int kPage = 16;
 constexpr int kMinSplitPages = 16;
 constexpr int kMaxSplitPages = 256;
 constexpr int kDecWarps = 8;
-constexpr int kChunkThreads = 256;  // warp 0 K/Q TMA + queue, 1 MMA, 2-5 softmax, 6 V TMA, 7 idle
+constexpr int kSoftmaxWarps = 8;
+constexpr int kChunkThreads = 32 * (2 + kSoftmaxWarps);  // warp 0 TMA + queue, 1 MMA, 2-9 softmax
 constexpr int kPrologueThreads = 1024;
 constexpr int kSortLimit = 2048;    // rows sorted longest-first up to this count
 constexpr int kMaxRows = 8192;      // rows of one step
@@ -518,6 +519,7 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
   using C = DecCfg<D, G>;
   constexpr int EPL = C::EPL, NST = C::NST;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp >= kDecWarps) return;  // the CTA's remaining warps have no decode slice
   uint8_t* wbase = dsmem + warp * C::WARP_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(wbase + C::BAR_OFF);
   float* pbuf = reinterpret_cast<float*>(wbase + C::P_OFF);  // [G][2 halves][8]
@@ -616,27 +618,33 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
       }
       const int tok0 = (cur.p0 + pi) * kPage;
       const int nv = min(kPage, cur.ctx - tok0);  // valid keys in this page (>= 1)
-      float kf[8][EPL];
+      // q . k for this lane's 8 token rows 2i + h, in two halves of 4 rows to bound registers
+      float part[G][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) lds_row<EPL>(Ks + (2 * i + h) * D + sub * EPL, kf[i]);
+      for (int hf = 0; hf < 2; ++hf) {
+        float kf[4][EPL];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lds_row<EPL>(Ks + (2 * (hf * 4 + i) + h) * D + sub * EPL, kf[i]);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float acc_d = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc_d = fmaf(q[g][e], kf[i][e], acc_d);
+            part[g][hf * 4 + i] = acc_d;
+          }
+      }
       float alpha[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float part[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float s = 0.f;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) s = fmaf(q[g][e], kf[i][e], s);
-          part[i] = s;
-        }
         // reduce-scatter over the 16 lanes of this half: lane ends with token i = sub >> 1
         const bool b3 = sub & 8, b2 = sub & 4, b1 = sub & 2;
         float w4[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float send = b3 ? part[j] : part[j + 4];
-          const float keep = b3 ? part[j + 4] : part[j];
+          const float send = b3 ? part[g][j] : part[g][j + 4];
+          const float keep = b3 ? part[g][j + 4] : part[g][j];
           w4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
         }
         float w2[2];
@@ -649,39 +657,45 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
         float y = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
         y += __shfl_xor_sync(0xffffffffu, y, 1);
         const int ti = sub >> 1;  // this lane's token: 2 * ti + h
-        const float s = (2 * ti + h < nv) ? y * p.scale_log2 : -INFINITY;
-        float mx = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 2));
+        const float sc = (2 * ti + h < nv) ? y * p.scale_log2 : -INFINITY;
+        float mx = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 2));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float m_new = fmaxf(m[g], mx);
         alpha[g] = ex2(m[g] - m_new);
-        const float pr = ex2(s - m_new);
+        const float pr = ex2(sc - m_new);
         l[g] = l[g] * alpha[g] + ((lane & 1) ? 0.f : pr);
         m[g] = m_new;
         if ((lane & 1) == 0) pbuf[(g * 2 + h) * 8 + ti] = pr;
       }
       __syncwarp();
-      float vf[8][EPL];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        lds_row<EPL>(Vs + (2 * i + h) * D + sub * EPL, vf[i]);
-        if (2 * i + h >= nv) {
+      for (int g = 0; g < G; ++g)
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) vf[i][e] = 0.f;  // keys past the context may hold stale data
+        for (int e = 0; e < EPL; ++e) acc[g][e] *= alpha[g];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float vf[4][EPL];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          lds_row<EPL>(Vs + (2 * (hf * 4 + i) + h) * D + sub * EPL, vf[i]);
+          if (2 * (hf * 4 + i) + h >= nv) {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) vf[i][e] = 0.f;  // keys past the context may hold stale data
+          }
         }
-      }
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float4 pa = *reinterpret_cast<const float4*>(pbuf + (g * 2 + h) * 8);
-        const float4 pb = *reinterpret_cast<const float4*>(pbuf + (g * 2 + h) * 8 + 4);
-        const float pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        for (int g = 0; g < G; ++g) {
+          const float4 pw = *reinterpret_cast<const float4*>(pbuf + (g * 2 + h) * 8 + hf * 4);
+          const float pv[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-          float a = acc[g][e] * alpha[g];
+          for (int e = 0; e < EPL; ++e) {
+            float a = acc[g][e];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) a = fmaf(pw[i], vf[i][e], a);
-          acc[g][e] = a;
+            for (int i = 0; i < 4; ++i) a = fmaf(pv[i], vf[i][e], a);
+            acc[g][e] = a;
+          }
         }
       }
       __syncwarp();
@@ -771,10 +785,11 @@ struct ChCfg {
   static constexpr int NSL = D / 64;                 // 64-column slabs per row
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = NSL * kSlab;         // stage b: K at KV_OFF + b*2*NSL*kSlab, V after K
-  static constexpr int P_OFF = KV_OFF + 4 * NSL * kSlab;
-  static constexpr int BAR_OFF = P_OFF + 4 * kSlab;  // two P buffers of 128 rows x 128 keys
-  static constexpr int SMEM = BAR_OFF + 512 + 1024;  // + barriers + alignment slack
-  static constexpr int TMEM_COLS = 512;              // S0, S1 (128 each), O (D)
+  static constexpr int BAR_OFF = KV_OFF + 4 * NSL * kSlab;
+  static constexpr int X_OFF = BAR_OFF + 512;        // row-max / row-sum exchange, [2][2][128] fp32
+  static constexpr int SMEM = X_OFF + 2048 + 1024;   // + alignment slack
+  static constexpr int TMEM_COLS = 512;  // S0, S1 (128 each), O (D <= 128), P0, P1 (64 each: bf16 pairs)
+  static constexpr int P_COL = 384;
 };
 
 struct ChItem {
@@ -811,10 +826,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return ok != 0;
 }
 
-// Chunk phase: warp 0 streams Q and K (and owns the work queue), warp 1 issues
-// the MMAs, warps 2-5 run the softmax (one query row per thread), warp 6 streams
-// V.  Returns when the chunk queue is empty; the caller owns TMEM and the
-// barrier invalidation.
+// Chunk phase: warp 0 (one thread) owns the work queue and streams Q, K and V
+// (K one tile ahead of V); warp 1 (one thread) issues the MMAs; warps 2-9 run
+// the softmax: the two warps that share a TMEM lane quadrant own the same 32
+// query rows and split the 128 key columns, exchanging row maxima through
+// shared memory.  Returns when the chunk queue is empty; the caller owns TMEM
+// and the barrier invalidation.
 template <int D, int G>
 __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtensorMap* tm_k_p,
                                             const CUtensorMap* tm_v_p, const AttnParams& p, uint8_t* smem,
@@ -826,12 +843,14 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
   const CUtensorMap& tm_k = *tm_k_p;
   const CUtensorMap& tm_v = *tm_v_p;
   ChBars* bars = reinterpret_cast<ChBars*>(smem + C::BAR_OFF);
+  float* xbuf = reinterpret_cast<float*>(smem + C::X_OFF);  // [parity][half][128 rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.hdr[H_NCH_ITEMS];
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + C::Q_OFF;
-  auto kv_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kSlab; };
+  auto k_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kSlab; };
+  auto v_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kSlab + NSL * kSlab; };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -842,110 +861,144 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
       mbar_init(&bars->v_full[b], 1);
       mbar_init(&bars->v_empty[b], 1);
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 128);
+      mbar_init(&bars->p_full[b], 32 * kSoftmaxWarps);
       mbar_init(&bars->o_done[b], 1);
       mbar_init(&bars->item_full[b], 1);
-      mbar_init(&bars->item_empty[b], 1 + 128 + 1);  // MMA, softmax threads, V producer
+      mbar_init(&bars->item_empty[b], 1 + 32 * kSoftmaxWarps);  // MMA thread, softmax threads
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  const uint32_t tS0 = tmem, tO = tmem + 256;
+  const uint32_t tS0 = tmem, tO = tmem + 256, tP0 = tmem + C::P_COL;  // P buffer b at tP0 + 64 b
   volatile int* abort_flag = &bars->abort;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer + work queue
+    // ---------------------------------------------------------------- work queue + TMA producer
+    // The whole warp runs this loop: lane 0 owns the queue, the waits and the
+    // barrier bookkeeping; a tile's K (or V) boxes -- one per (page, 64-column
+    // slab) -- go out as one warp-wide TMA instruction, lane L taking page
+    // L / NSL, slab L % NSL.
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      int g = 0;       // CTA-global KV tile counter
-      int n_done = 0;  // items taken by this CTA
-      bool ok = true;
-      while (ok) {
-        const int item = atomicAdd(p.hdr + H_CH_CTR, 1);
-        const int slot = n_done & 1;
-        if (n_done >= 2 && !mbar_wait(&bars->item_empty[slot], ((n_done >> 1) - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        ChItem it;
-        it.row = -1;
-        if (item < n_items) {
-          const int2 kl = __ldg(p.ch_items + item);  // (chunk row index, item within the row)
-          const int k = kl.x, local = kl.y;
-          it.row = __ldg(p.ch_rows + k);
-          it.tb = __ldg(p.cu + it.row);
-          it.d = __ldg(p.cu + it.row + 1) - it.tb;
-          it.c = __ldg(p.q_start + it.row);
-          const int n_qt = (it.d + TPT - 1) / TPT;
-          const int qt = n_qt - 1 - local / p.H_kv;  // later tiles see more keys: run them first
-          it.hk = local % p.H_kv;
-          it.tok0 = qt * TPT;
-          it.ntok = min(TPT, it.d - it.tok0);
-          it.kv_end = it.c + it.tok0 + it.ntok;
-          it.n_kt = (it.kv_end + 127) / 128;
-          it.tile0 = g;
-        }
+    }
+    const int my_pg = lane / NSL, my_s = lane % NSL;
+    int g = 0;       // CTA-global KV tile counter
+    int n_done = 0;  // items taken by this CTA
+    int g_v = 0;     // tiles whose V has been issued
+    bool ok = true;
+    auto lane0_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      int r = 1;
+      if (lane == 0) r = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+      r = __shfl_sync(0xffffffffu, r, 0);
+      return r != 0;
+    };
+    // V of tile gv (one tile behind K): its stage was last read by the PV MMA of gv - 2
+    auto load_v = [&](int gv, int row0, int npg) -> bool {
+      const int bv = gv & 1;
+      if (gv >= 2 && !lane0_wait(&bars->v_empty[bv], ((gv >> 1) - 1) & 1)) return false;
+      if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[bv], npg * kPage * D * 2);
+      __syncwarp();
+      if (my_pg < npg && lane < 8 * NSL)
+        tma_load_2d(smem + v_off(bv) + my_s * kSlab + my_pg * 2048, &tm_v, my_s * 64, row0, &bars->v_full[bv]);
+      return true;
+    };
+    while (ok) {
+      int item = 0;
+      if (lane == 0) item = atomicAdd(p.hdr + H_CH_CTR, 1);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      const int slot = n_done & 1;
+      if (n_done >= 2 && !lane0_wait(&bars->item_empty[slot], ((n_done >> 1) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      ChItem it;
+      it.row = -1;
+      if (item < n_items) {
+        const int2 kl = __ldg(p.ch_items + item);  // (chunk row index, item within the row)
+        const int k = kl.x, local = kl.y;
+        it.row = __ldg(p.ch_rows + k);
+        it.tb = __ldg(p.cu + it.row);
+        it.d = __ldg(p.cu + it.row + 1) - it.tb;
+        it.c = __ldg(p.q_start + it.row);
+        const int n_qt = (it.d + TPT - 1) / TPT;
+        const int qt = n_qt - 1 - local / p.H_kv;  // later tiles see more keys: run them first
+        it.hk = local % p.H_kv;
+        it.tok0 = qt * TPT;
+        it.ntok = min(TPT, it.d - it.tok0);
+        it.kv_end = it.c + it.tok0 + it.ntok;
+        it.n_kt = (it.kv_end + 127) / 128;
+        it.tile0 = g;
+      }
+      if (lane == 0) {
         bars->items[slot] = it;
         mbar_arrive(&bars->item_full[slot]);
-        ++n_done;
-        if (it.row < 0) break;
-        // Q tile: previous item's S MMAs must be done with it
-        if (n_done >= 2 && !mbar_wait(&bars->q_empty, (n_done - 2) & 1, abort_flag)) {
+      }
+      ++n_done;
+      if (it.row < 0) break;
+      // Q tile: the previous item's S MMAs must be done with it
+      if (n_done >= 2 && !lane0_wait(&bars->q_empty, (n_done - 2) & 1)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, 128 * D * 2);
+      __syncwarp();
+      if (lane < NSL)
+        tma_load_3d(smem + C::Q_OFF + lane * kSlab, &tm_q, lane * 64, it.hk * G, it.tb + it.tok0, &bars->q_full);
+      const int32_t* btrow = p.bt + static_cast<int64_t>(it.row) * p.bt_stride;
+      const int n_pages = (it.kv_end + kPage - 1) / kPage;
+      // lane L < 8 holds the page id of page L of the current tile; the next tile's is in flight
+      int pg_cur = lane < 8 && lane < n_pages ? __ldg(btrow + lane) : 0;
+      int row0_prev = 0, npg_prev = 0;
+      for (int kt = 0; kt < it.n_kt; ++kt, ++g) {
+        const int lp = (kt + 1) * 8 + lane;
+        const int pg_nxt = lane < 8 && lp < n_pages ? __ldg(btrow + lp) : 0;
+        const int b = g & 1;
+        const int keys = min(128, it.kv_end - kt * 128);
+        const int npg = (keys + kPage - 1) / kPage;
+        int phys = __shfl_sync(0xffffffffu, pg_cur, my_pg & 7);
+        if (my_pg < npg && lane < 8 * NSL && (phys < 0 || phys >= p.num_pages)) {
+          atomicOr(p.hdr + H_STATUS, MS_STATUS_BAD_PAGE);
+          phys = 0;
+        }
+        const int row0 = (phys * p.H_kv + it.hk) * kPage;
+        // K of tile g: its stage was last read by the S MMA of tile g - 2
+        if (g >= 2 && !lane0_wait(&bars->k_empty[b], ((g >> 1) - 1) & 1)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&bars->q_full, 128 * D * 2);
-        for (int s = 0; s < NSL; ++s)
-          tma_load_3d(smem + C::Q_OFF + s * kSlab, &tm_q, s * 64, it.hk * G, it.tb + it.tok0, &bars->q_full);
-        const int32_t* btrow = p.bt + static_cast<int64_t>(it.row) * p.bt_stride;
-        const int n_pages = (it.kv_end + kPage - 1) / kPage;
-        int pg_cur[8], pg_nxt[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) pg_cur[j] = j < n_pages ? __ldg(btrow + j) : 0;
-        for (int kt = 0; kt < it.n_kt; ++kt, ++g) {
-          // the next tile's page ids are in flight while this tile waits for its stage
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int lp = (kt + 1) * 8 + j;
-            pg_nxt[j] = lp < n_pages ? __ldg(btrow + lp) : 0;
-          }
-          const int b = g & 1;
-          const int keys = min(128, it.kv_end - kt * 128);
-          const int npg = (keys + kPage - 1) / kPage;
-          int r0[8];
-#pragma unroll
-          for (int pg = 0; pg < 8; ++pg) {
-            int phys = pg_cur[pg];
-            if (pg < npg && (phys < 0 || phys >= p.num_pages)) {
-              atomicOr(p.hdr + H_STATUS, MS_STATUS_BAD_PAGE);
-              phys = 0;
-            }
-            r0[pg] = (phys * p.H_kv + it.hk) * kPage;
-          }
-          // K of tile g: its stage was last read by the S MMA of tile g - 2
-          if (g >= 2 && !mbar_wait(&bars->k_empty[b], ((g >> 1) - 1) & 1, abort_flag)) {
+        if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[b], npg * kPage * D * 2);
+        __syncwarp();
+        if (my_pg < npg && lane < 8 * NSL)
+          tma_load_2d(smem + k_off(b) + my_s * kSlab + my_pg * 2048, &tm_k, my_s * 64, row0, &bars->k_full[b]);
+        if (kt >= 1) {
+          if (!load_v(g - 1, row0_prev, npg_prev)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars->k_full[b], npg * kPage * D * 2);
-#pragma unroll
-          for (int pg = 0; pg < 8; ++pg)
-            if (pg < npg)
-#pragma unroll
-              for (int s = 0; s < NSL; ++s)
-                tma_load_2d(smem + kv_off(b) + s * kSlab + pg * 2048, &tm_k, s * 64, r0[pg], &bars->k_full[b]);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) pg_cur[j] = pg_nxt[j];
+          g_v = g;
         }
+        row0_prev = row0;
+        npg_prev = npg;
+        pg_cur = pg_nxt;
       }
+      if (!ok) break;
+      if (!load_v(g - 1, row0_prev, npg_prev)) {
+        ok = false;
+        break;
+      }
+      g_v = g;
+    }
+    if (lane == 0) {
       if (!ok) *abort_flag = 1;
-      // copies still in flight must land before the CTA exits
+      // copies still in flight must land before the CTA moves on
       for (int t = (g > 2 ? g - 2 : 0); t < g; ++t)
         mbar_wait(&bars->k_full[t & 1], (t >> 1) & 1, nullptr, 200000000ull);
+      for (int t = (g_v > 2 ? g_v - 2 : 0); t < g_v; ++t)
+        mbar_wait(&bars->v_full[t & 1], (t >> 1) & 1, nullptr, 200000000ull);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (one thread)
@@ -977,7 +1030,7 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
             const uint32_t idesc_s = idesc_bf16_f32(128, n_cols, 0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_bf16_ss(tS0 + b * 128, kmajor_desc(sQ, kk), kmajor_desc(sbase + kv_off(b), kk), idesc_s,
+              mma_bf16_ss(tS0 + b * 128, kmajor_desc(sQ, kk), kmajor_desc(sbase + k_off(b), kk), idesc_s,
                           kk > 0 ? 1u : 0u);
             mma_commit(&bars->s_full[b]);
             mma_commit(&bars->k_empty[b]);
@@ -996,20 +1049,20 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
             if (keys != nk * 16) {
               // rows past the context in the last page may hold stale (even non-finite)
               // data: zero them in V so that P = 0 times V stays 0
-              uint8_t* v0 = smem + kv_off(bj) + NSL * kSlab;
+              uint8_t* v0 = smem + v_off(bj);
               for (int r = keys; r < nk * 16; ++r)
                 for (int s = 0; s < NSL; ++s)
                   for (int q16 = 0; q16 < 8; ++q16)
                     *reinterpret_cast<uint4*>(v0 + s * kSlab + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
               fence_proxy_async_smem();
             }
-            const uint32_t vbase = sbase + kv_off(bj) + NSL * kSlab;
+            const uint32_t vbase = sbase + v_off(bj);
             for (int kk = 0; kk < nk; ++kk) {
-              // V is the MN-major B operand: 64-column slabs one slab apart (LBO),
-              // 8-key row groups 1024 B apart (SBO), 16 keys = 2048 B per k-step
+              // P (A operand) from TMEM: 16 keys = 8 packed columns per k-step.  V is the
+              // MN-major B operand: 64-column slabs one slab apart (LBO), 8-key row groups
+              // 1024 B apart (SBO), 16 keys = 2048 B per k-step
               const uint64_t vdesc = smem_desc_sw128(vbase + kk * 2048, kSlab, 1024);
-              mma_bf16_ss(tO, kmajor_desc(sbase + C::P_OFF + bj * 2 * kSlab, kk), vdesc, idesc_pv,
-                          (j > 0 || kk > 0) ? 1u : 0u);
+              mma_bf16_ts(tO, tP0 + bj * 64 + kk * 8, vdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bars->o_done[bj]);
             mma_commit(&bars->v_empty[bj]);
@@ -1019,75 +1072,23 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
         mbar_arrive(&bars->item_empty[slot]);
       }
       if (!ok) *abort_flag = 1;
-      // every MMA this thread issued must finish before TMEM is released
+      // every MMA this thread issued must finish before TMEM is reused or released
       mma_commit(&bars->mma_done);
       mbar_wait(&bars->mma_done, 0, nullptr, 200000000ull);
     }
-  } else if (warp == 6) {
-    // ---------------------------------------------------------------- V producer
-    if (lane == 0) {
-      int g = 0;
-      bool ok = true;
-      for (int n = 0; ok; ++n) {
-        const int slot = n & 1;
-        if (!mbar_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const ChItem it = bars->items[slot];
-        if (it.row < 0) break;
-        const int32_t* btrow = p.bt + static_cast<int64_t>(it.row) * p.bt_stride;
-        const int n_pages = (it.kv_end + kPage - 1) / kPage;
-        int pg_cur[8], pg_nxt[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) pg_cur[j] = j < n_pages ? __ldg(btrow + j) : 0;
-        for (int kt = 0; kt < it.n_kt; ++kt, ++g) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int lp = (kt + 1) * 8 + j;
-            pg_nxt[j] = lp < n_pages ? __ldg(btrow + lp) : 0;
-          }
-          const int b = g & 1;
-          const int keys = min(128, it.kv_end - kt * 128);
-          const int npg = (keys + kPage - 1) / kPage;
-          // V of tile g: its stage was last read by the PV MMA of tile g - 2
-          if (g >= 2 && !mbar_wait(&bars->v_empty[b], ((g >> 1) - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->v_full[b], npg * kPage * D * 2);
-#pragma unroll
-          for (int pg = 0; pg < 8; ++pg) {
-            if (pg < npg) {
-              int phys = pg_cur[pg];
-              if (phys < 0 || phys >= p.num_pages) phys = 0;  // flagged by the K producer
-              const int r0 = (phys * p.H_kv + it.hk) * kPage;
-#pragma unroll
-              for (int s = 0; s < NSL; ++s)
-                tma_load_2d(smem + kv_off(b) + (NSL + s) * kSlab + pg * 2048, &tm_v, s * 64, r0,
-                            &bars->v_full[b]);
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) pg_cur[j] = pg_nxt[j];
-        }
-        if (!ok) break;
-        mbar_arrive(&bars->item_empty[slot]);
-      }
-      if (!ok) *abort_flag = 1;
-      for (int t = (g > 2 ? g - 2 : 0); t < g; ++t)
-        mbar_wait(&bars->v_full[t & 1], (t >> 1) & 1, nullptr, 200000000ull);
-    }
-  } else if (warp < 6) {
-    // ---------------------------------------------------------------- softmax: one query row per thread
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-    const int r = quad * 32 + lane;
+  } else if (warp < 2 + kSoftmaxWarps) {
+    // ---------------------------------------------------------------- softmax
+    const int quad = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;           // key columns [64 * half, 64 * half + 64)
+    const int r = quad * 32 + lane;             // query row of this thread
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t pair_bar = 1 + quad;         // named barrier of the two warps of this quadrant
     const float sl2 = p.scale_log2;
     // A row exponentiates against m_use, the largest scaled score seen when it
     // was last raised; it is raised (and O rescaled) only when a tile's max
     // exceeds it by more than 2^8, so P <= 256 and O, l stay exact in fp32.
     constexpr float kRescaleLog2 = 8.f;
+    constexpr int OC = D / 2;                   // O columns this warp owns
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int slot = n & 1;
@@ -1109,71 +1110,63 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
           break;
         }
         tc_fence_after();
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        const uint32_t ts = tS0 + b * 128 + lane_off;
+        uint32_t r0[32], r1[32];
+        const uint32_t ts = tS0 + b * 128 + half * 64 + lane_off;
         tmem_ld32(ts, r0);
         tmem_ld32(ts + 32, r1);
-        tmem_ld32(ts + 64, r2);
-        tmem_ld32(ts + 96, r3);
         tmem_wait_ld();
         reg_fence32(r0);
         reg_fence32(r1);
-        reg_fence32(r2);
-        reg_fence32(r3);
-        float sv[128];
+        float sv[64];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           sv[j] = __uint_as_float(r0[j]);
           sv[32 + j] = __uint_as_float(r1[j]);
-          sv[64 + j] = __uint_as_float(r2[j]);
-          sv[96 + j] = __uint_as_float(r3[j]);
         }
-        const int key0 = kt * 128;
-        if (key0 + 127 > warp_min_pos) {  // diagonal or ragged tile: causal mask (warp-uniform branch)
+        const int key0 = kt * 128 + half * 64;
+        if (kt * 128 + 127 > warp_min_pos) {  // diagonal or ragged tile: causal mask (pair-uniform)
 #pragma unroll
-          for (int j = 0; j < 128; ++j)
+          for (int j = 0; j < 64; ++j)
             if (key0 + j > pos) sv[j] = -INFINITY;
         }
-        // eight independent max / sum chains: one warp per scheduler has no other latency cover
-        float mxa[8];
+        float mxa[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-        for (int a = 0; a < 8; ++a) mxa[a] = sv[a];
-#pragma unroll
-        for (int j = 8; j < 128; ++j) mxa[j & 7] = fmaxf(mxa[j & 7], sv[j]);
-        const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                               fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+        for (int j = 4; j < 64; ++j) mxa[j & 3] = fmaxf(mxa[j & 3], sv[j]);
+        const float pm = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+        xbuf[(g & 1) * 256 + half * 128 + r] = pm;
+        named_bar_sync(pair_bar, 64);
+        const float mx = fmaxf(pm, xbuf[(g & 1) * 256 + (half ^ 1) * 128 + r]);
         const float mx_s = mx * sl2;
         const bool grow = mx_s > m_use + kRescaleLog2;
         const float m_new = grow ? mx_s : m_use;
         const float alpha = grow ? ex2(m_use - m_new) : 1.f;
         const float neg_m = -m_new;
-        float rsa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float rsa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
+        for (int j = 0; j < 64; ++j) {
           const float e = ex2(fmaf(sv[j], sl2, neg_m));
           sv[j] = e;
-          rsa[j & 7] += e;
+          rsa[j & 3] += e;
         }
-        const float rs = ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3])) + ((rsa[4] + rsa[5]) + (rsa[6] + rsa[7]));
-        l = l * alpha + rs;
+        l = l * alpha + ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3]));
         m_use = m_new;
-        // rescale the running O when a row raised its max (TMEM access is warp-wide)
-        if (kt > 0 && __any_sync(0xffffffffu, grow)) {
+        if (kt > 0 && __any_sync(0xffffffffu, grow)) {  // rescale this warp's O columns
+          // the PV MMA of the previous tile must be done with O first
           if (!warp_wait(&bars->o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < OC / 32; ++cc) {
             uint32_t rr[32];
-            tmem_ld32(tO + lane_off + cc * 32, rr);
+            tmem_ld32(tO + lane_off + half * OC + cc * 32, rr);
             tmem_wait_ld();
             reg_fence32(rr);
             float o[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(rr[j]) * alpha;
-            tmem_st32(tO + lane_off + cc * 32, o);
+            tmem_st32(tO + lane_off + half * OC + cc * 32, o);
           }
           tmem_wait_st();
         }
@@ -1182,38 +1175,35 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
           ok = false;
           break;
         }
-        uint8_t* prow = smem + C::P_OFF + b * 2 * kSlab + r * 128;
+        uint32_t pw[32];
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          __nv_bfloat162 h0 = __floats2bfloat162_rn(sv[cc * 8 + 0], sv[cc * 8 + 1]);
-          __nv_bfloat162 h1 = __floats2bfloat162_rn(sv[cc * 8 + 2], sv[cc * 8 + 3]);
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[cc * 8 + 4], sv[cc * 8 + 5]);
-          __nv_bfloat162 h3 = __floats2bfloat162_rn(sv[cc * 8 + 6], sv[cc * 8 + 7]);
-          uint4 u;
-          u.x = *reinterpret_cast<uint32_t*>(&h0);
-          u.y = *reinterpret_cast<uint32_t*>(&h1);
-          u.z = *reinterpret_cast<uint32_t*>(&h2);
-          u.w = *reinterpret_cast<uint32_t*>(&h3);
-          const int slab = cc >> 3, chunk = (cc & 7) ^ (r & 7);
-          *reinterpret_cast<uint4*>(prow + slab * kSlab + chunk * 16) = u;
+        for (int j = 0; j < 32; ++j) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * j], sv[2 * j + 1]);
+          pw[j] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        fence_proxy_async_smem();
+        tmem_st32u(tP0 + b * 64 + half * 32 + lane_off, pw);
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->p_full[b]);
       }
       if (!ok) break;
+      // row sum: the two halves of the row add their partial sums
       const int gl = it.tile0 + it.n_kt - 1;
+      xbuf[((gl + 1) & 1) * 256 + half * 128 + r] = l;
+      named_bar_sync(pair_bar, 64);
+      const float l_row = l + xbuf[((gl + 1) & 1) * 256 + (half ^ 1) * 128 + r];
+      named_bar_sync(pair_bar, 64);  // both halves have read before the slots are reused
       if (!warp_wait(&bars->o_done[gl & 1], (gl >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float inv = 1.f / l;
-      bf16* dst = p.out + (static_cast<int64_t>(it.tb + tl) * p.H_q + it.hk * G + r % G) * D;
+      const float inv = 1.f / l_row;
+      bf16* dst = p.out + (static_cast<int64_t>(it.tb + tl) * p.H_q + it.hk * G + r % G) * D + half * OC;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < OC / 32; ++cc) {
         uint32_t rr[32];
-        tmem_ld32(tO + lane_off + cc * 32, rr);
+        tmem_ld32(tO + lane_off + half * OC + cc * 32, rr);
         tmem_wait_ld();
         reg_fence32(rr);
         if (valid) {
@@ -1258,7 +1248,7 @@ __device__ __forceinline__ void invalidate_phase_barriers(uint8_t* smem, bool ch
       uint64_t* b1 = &bars->mma_done;
       for (uint64_t* b = b0; b <= b1; ++b) mbar_inval(b);
     }
-  } else if ((threadIdx.x & 31) == 0) {
+  } else if ((threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < kDecWarps) {
     using C = DecCfg<D, G>;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (threadIdx.x >> 5) * C::WARP_BYTES + C::BAR_OFF);
     for (int i = 0; i < C::NST; ++i) mbar_inval(full + i);
