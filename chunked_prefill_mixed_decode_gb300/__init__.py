@@ -21,6 +21,7 @@ from .build import LIB as _LIB_PATH
 MS_OK, MS_ERR_ARG, MS_ERR_BUDGET, MS_ERR_NO_PAGES, MS_ERR_CUDA, MS_ERR_DEVICE = 0, -1, -2, -3, -4, -5
 MS_ERR_SCRATCH = -6
 STATUS_BAD_SLOT, STATUS_BAD_POSITION, STATUS_BAD_PAGE, STATUS_TIMEOUT, STATUS_BAD_META = 1, 2, 4, 8, 16
+STATUS_INTERNAL = 32
 PAGE_SIZE = 16
 
 _ERR_NAMES = {MS_ERR_ARG: "MS_ERR_ARG", MS_ERR_BUDGET: "MS_ERR_BUDGET", MS_ERR_NO_PAGES: "MS_ERR_NO_PAGES",

@@ -514,6 +514,18 @@ __device__ __forceinline__ void merge_splits(const AttnParams& p, int k, int h0,
 
 // Decode phase: each of the CTA's 8 warps is an independent worker over its
 // own slice of shared memory, pulling decode items until the queue is empty.
+// load EPL bf16 columns of one token row from shared memory as EPL/2 fp32 pairs
+template <int EPL>
+__device__ __forceinline__ void lds_row2(const bf16* src, float2 (&f)[EPL / 2]) {
+  if constexpr (EPL == 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
+    f[0] = bf2_to_f2(u.x); f[1] = bf2_to_f2(u.y); f[2] = bf2_to_f2(u.z); f[3] = bf2_to_f2(u.w);
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    f[0] = bf2_to_f2(u.x); f[1] = bf2_to_f2(u.y);
+  }
+}
+
 template <int D, int G>
 __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem) {
   using C = DecCfg<D, G>;
@@ -595,13 +607,15 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
   pump();
 
   while (true) {
-    float q[G][EPL], acc[G][EPL], m[G], l[G];
+    constexpr int EP2 = EPL / 2;  // fp32 pairs per lane of one token row
+    float2 q[G][EP2], acc[G][EP2];
+    float m[G], l[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       m[g] = -INFINITY;
       l[g] = 0.f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
+      for (int e = 0; e < EP2; ++e) acc[g][e] = make_float2(0.f, 0.f);
     }
     for (int pi = 0; pi < cur.np; ++pi) {
       const int st = seq_con % NST;
@@ -614,7 +628,7 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
       if (pi == 0) {
         const bf16* qs = reinterpret_cast<const bf16*>(wbase + C::Q_OFF + item_par * C::Q_BYTES);
 #pragma unroll
-        for (int g = 0; g < G; ++g) lds_row<EPL>(qs + g * D + sub * EPL, q[g]);
+        for (int g = 0; g < G; ++g) lds_row2<EPL>(qs + g * D + sub * EPL, q[g]);
       }
       const int tok0 = (cur.p0 + pi) * kPage;
       const int nv = min(kPage, cur.ctx - tok0);  // valid keys in this page (>= 1)
@@ -622,17 +636,17 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
       float part[G][8];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        float kf[4][EPL];
+        float2 kf[4][EP2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) lds_row<EPL>(Ks + (2 * (hf * 4 + i) + h) * D + sub * EPL, kf[i]);
+        for (int i = 0; i < 4; ++i) lds_row2<EPL>(Ks + (2 * (hf * 4 + i) + h) * D + sub * EPL, kf[i]);
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            float acc_d = 0.f;
+            float2 acc_d = fmul2(q[g][0], kf[i][0]);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) acc_d = fmaf(q[g][e], kf[i][e], acc_d);
-            part[g][hf * 4 + i] = acc_d;
+            for (int e = 1; e < EP2; ++e) acc_d = ffma2(q[g][e], kf[i][e], acc_d);
+            part[g][hf * 4 + i] = acc_d.x + acc_d.y;
           }
       }
       float alpha[G];
@@ -671,29 +685,32 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
       }
       __syncwarp();
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+      for (int g = 0; g < G; ++g) {
+        const float2 a2 = make_float2(alpha[g], alpha[g]);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[g][e] *= alpha[g];
+        for (int e = 0; e < EP2; ++e) acc[g][e] = fmul2(acc[g][e], a2);
+      }
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        float vf[4][EPL];
+        float2 vf[4][EP2];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          lds_row<EPL>(Vs + (2 * (hf * 4 + i) + h) * D + sub * EPL, vf[i]);
+          lds_row2<EPL>(Vs + (2 * (hf * 4 + i) + h) * D + sub * EPL, vf[i]);
           if (2 * (hf * 4 + i) + h >= nv) {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) vf[i][e] = 0.f;  // keys past the context may hold stale data
+            for (int e = 0; e < EP2; ++e) vf[i][e] = make_float2(0.f, 0.f);  // keys past the context: stale data
           }
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float4 pw = *reinterpret_cast<const float4*>(pbuf + (g * 2 + h) * 8 + hf * 4);
-          const float pv[4] = {pw.x, pw.y, pw.z, pw.w};
+          const float2 pv[4] = {make_float2(pw.x, pw.x), make_float2(pw.y, pw.y), make_float2(pw.z, pw.z),
+                                make_float2(pw.w, pw.w)};
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            float a = acc[g][e];
+          for (int e = 0; e < EP2; ++e) {
+            float2 a = acc[g][e];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a = fmaf(pv[i], vf[i][e], a);
+            for (int i = 0; i < 4; ++i) a = ffma2(pv[i], vf[i][e], a);
             acc[g][e] = a;
           }
         }
@@ -713,7 +730,10 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
       for (int o = 1; o < 32; o <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
       float a[EPL];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) a[e] = acc[g][e] + __shfl_xor_sync(0xffffffffu, acc[g][e], 16);
+      for (int e = 0; e < EP2; ++e) {
+        a[2 * e] = acc[g][e].x + __shfl_xor_sync(0xffffffffu, acc[g][e].x, 16);
+        a[2 * e + 1] = acc[g][e].y + __shfl_xor_sync(0xffffffffu, acc[g][e].y, 16);
+      }
       if (cur.ns == 1) {
         if (h == 0) {
           const float inv = 1.f / lt;
@@ -784,10 +804,11 @@ template <int D>
 struct ChCfg {
   static constexpr int NSL = D / 64;                 // 64-column slabs per row
   static constexpr int Q_OFF = 0;
+  static constexpr int KVS = D == 128 ? 3 : 4;      // K/V pipeline stages
   static constexpr int KV_OFF = NSL * kSlab;         // stage b: K at KV_OFF + b*2*NSL*kSlab, V after K
-  static constexpr int BAR_OFF = KV_OFF + 4 * NSL * kSlab;
+  static constexpr int BAR_OFF = KV_OFF + 2 * KVS * NSL * kSlab;
   static constexpr int X_OFF = BAR_OFF + 512;        // row-max / row-sum exchange, [2][2][128] fp32
-  static constexpr int SMEM = X_OFF + 2048 + 1024;   // + alignment slack
+  static constexpr int SMEM = X_OFF + 2048;          // dynamic shared memory starts 1024-aligned
   static constexpr int TMEM_COLS = 512;  // S0, S1 (128 each), O (D <= 128), P0, P1 (64 each: bf16 pairs)
   static constexpr int P_COL = 384;
 };
@@ -798,8 +819,8 @@ struct ChItem {
 
 struct ChBars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[2], k_empty[2];  // K stage: free once the tile's S MMA is done
-  uint64_t v_full[2], v_empty[2];  // V stage: free once the tile's PV MMA is done
+  uint64_t k_full[4], k_empty[4];  // K stage: free once the tile's S MMA is done
+  uint64_t v_full[4], v_empty[4];  // V stage: free once the tile's PV MMA is done
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t item_full[2], item_empty[2];
   uint64_t mma_done;
@@ -849,17 +870,20 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + C::Q_OFF;
+  constexpr int KVS = C::KVS;
   auto k_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kSlab; };
   auto v_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kSlab + NSL * kSlab; };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 4; ++b) {  // all four (KVS of them in use) so that all can be invalidated
       mbar_init(&bars->k_full[b], 1);
       mbar_init(&bars->k_empty[b], 1);
       mbar_init(&bars->v_full[b], 1);
       mbar_init(&bars->v_empty[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
       mbar_init(&bars->p_full[b], 32 * kSoftmaxWarps);
       mbar_init(&bars->o_done[b], 1);
@@ -896,10 +920,10 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
       r = __shfl_sync(0xffffffffu, r, 0);
       return r != 0;
     };
-    // V of tile gv (one tile behind K): its stage was last read by the PV MMA of gv - 2
+    // V of tile gv (one tile behind K): its stage was last read by the PV MMA of gv - KVS
     auto load_v = [&](int gv, int row0, int npg) -> bool {
-      const int bv = gv & 1;
-      if (gv >= 2 && !lane0_wait(&bars->v_empty[bv], ((gv >> 1) - 1) & 1)) return false;
+      const int bv = gv % KVS;
+      if (gv >= KVS && !lane0_wait(&bars->v_empty[bv], ((gv / KVS) - 1) & 1)) return false;
       if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[bv], npg * kPage * D * 2);
       __syncwarp();
       if (my_pg < npg && lane < 8 * NSL)
@@ -956,7 +980,7 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
       for (int kt = 0; kt < it.n_kt; ++kt, ++g) {
         const int lp = (kt + 1) * 8 + lane;
         const int pg_nxt = lane < 8 && lp < n_pages ? __ldg(btrow + lp) : 0;
-        const int b = g & 1;
+        const int b = g % KVS;
         const int keys = min(128, it.kv_end - kt * 128);
         const int npg = (keys + kPage - 1) / kPage;
         int phys = __shfl_sync(0xffffffffu, pg_cur, my_pg & 7);
@@ -965,8 +989,8 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
           phys = 0;
         }
         const int row0 = (phys * p.H_kv + it.hk) * kPage;
-        // K of tile g: its stage was last read by the S MMA of tile g - 2
-        if (g >= 2 && !lane0_wait(&bars->k_empty[b], ((g >> 1) - 1) & 1)) {
+        // K of tile g: its stage was last read by the S MMA of tile g - KVS
+        if (g >= KVS && !lane0_wait(&bars->k_empty[b], ((g / KVS) - 1) & 1)) {
           ok = false;
           break;
         }
@@ -995,10 +1019,10 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
     if (lane == 0) {
       if (!ok) *abort_flag = 1;
       // copies still in flight must land before the CTA moves on
-      for (int t = (g > 2 ? g - 2 : 0); t < g; ++t)
-        mbar_wait(&bars->k_full[t & 1], (t >> 1) & 1, nullptr, 200000000ull);
-      for (int t = (g_v > 2 ? g_v - 2 : 0); t < g_v; ++t)
-        mbar_wait(&bars->v_full[t & 1], (t >> 1) & 1, nullptr, 200000000ull);
+      for (int t = (g > KVS ? g - KVS : 0); t < g; ++t)
+        mbar_wait(&bars->k_full[t % KVS], (t / KVS) & 1, nullptr, 200000000ull);
+      for (int t = (g_v > KVS ? g_v - KVS : 0); t < g_v; ++t)
+        mbar_wait(&bars->v_full[t % KVS], (t / KVS) & 1, nullptr, 200000000ull);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (one thread)
@@ -1019,8 +1043,8 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
         }
         for (int kt = 0; kt <= it.n_kt; ++kt) {
           if (kt < it.n_kt) {
-            const int g = it.tile0 + kt, b = g & 1;
-            if (!mbar_wait(&bars->k_full[b], (g >> 1) & 1, abort_flag)) {
+            const int g = it.tile0 + kt, b = g & 1, bk = g % KVS;
+            if (!mbar_wait(&bars->k_full[bk], (g / KVS) & 1, abort_flag)) {
               ok = false;
               break;
             }
@@ -1030,15 +1054,15 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
             const uint32_t idesc_s = idesc_bf16_f32(128, n_cols, 0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_bf16_ss(tS0 + b * 128, kmajor_desc(sQ, kk), kmajor_desc(sbase + k_off(b), kk), idesc_s,
+              mma_bf16_ss(tS0 + b * 128, kmajor_desc(sQ, kk), kmajor_desc(sbase + k_off(bk), kk), idesc_s,
                           kk > 0 ? 1u : 0u);
             mma_commit(&bars->s_full[b]);
-            mma_commit(&bars->k_empty[b]);
+            mma_commit(&bars->k_empty[bk]);
             if (kt == it.n_kt - 1) mma_commit(&bars->q_empty);
           }
           if (kt >= 1) {
-            const int j = kt - 1, gj = it.tile0 + j, bj = gj & 1;
-            if (!mbar_wait(&bars->v_full[bj], (gj >> 1) & 1, abort_flag) ||
+            const int j = kt - 1, gj = it.tile0 + j, bj = gj & 1, bv = gj % KVS;
+            if (!mbar_wait(&bars->v_full[bv], (gj / KVS) & 1, abort_flag) ||
                 !mbar_wait(&bars->p_full[bj], (gj >> 1) & 1, abort_flag)) {
               ok = false;
               break;
@@ -1049,14 +1073,14 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
             if (keys != nk * 16) {
               // rows past the context in the last page may hold stale (even non-finite)
               // data: zero them in V so that P = 0 times V stays 0
-              uint8_t* v0 = smem + v_off(bj);
+              uint8_t* v0 = smem + v_off(bv);
               for (int r = keys; r < nk * 16; ++r)
                 for (int s = 0; s < NSL; ++s)
                   for (int q16 = 0; q16 < 8; ++q16)
                     *reinterpret_cast<uint4*>(v0 + s * kSlab + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
               fence_proxy_async_smem();
             }
-            const uint32_t vbase = sbase + v_off(bj);
+            const uint32_t vbase = sbase + v_off(bv);
             for (int kk = 0; kk < nk; ++kk) {
               // P (A operand) from TMEM: 16 keys = 8 packed columns per k-step.  V is the
               // MN-major B operand: 64-column slabs one slab apart (LBO), 8-key row groups
@@ -1065,7 +1089,7 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
               mma_bf16_ts(tO, tP0 + bj * 64 + kk * 8, vdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bars->o_done[bj]);
-            mma_commit(&bars->v_empty[bj]);
+            mma_commit(&bars->v_empty[bv]);
           }
         }
         if (!ok) break;
@@ -1262,21 +1286,27 @@ template <int D, int G>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, AttnParams p) {
-  extern __shared__ uint8_t asmem_raw[];
-  __shared__ uint32_t s_tmem;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(asmem_raw) + 1023) & ~uintptr_t(1023));
+  // no static shared memory: the dynamic block starts 1024-aligned, as the
+  // 128-byte-swizzled TMA tiles and MMA descriptors require
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int n_ch_items = p.hdr[H_NCH_ITEMS];
   const int n_dec_items = p.hdr[H_NDEC_ITEMS];
   if (n_ch_items == 0 && n_dec_items == 0) return;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.hdr + H_STATUS, MS_STATUS_INTERNAL);
+    return;
+  }
+  uint32_t* tmem_slot = &reinterpret_cast<ChBars*>(smem + ChCfg<D>::BAR_OFF)->tmem;
   if (warp == 1) {
-    tmem_alloc(&s_tmem, ChCfg<D>::TMEM_COLS);
+    tmem_alloc(tmem_slot, ChCfg<D>::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem;
+  const uint32_t tmem = *tmem_slot;
+  __syncthreads();  // every thread holds the address before the phases reuse the memory
   const bool chunk_first = static_cast<int>(blockIdx.x) < p.hdr[H_CHUNK_CTAS];
   for (int ph = 0; ph < 2; ++ph) {
     const bool chunk = (ph == 0) == chunk_first;
@@ -1397,7 +1427,7 @@ int num_sms() {
 template <int D, int G>
 int launch_paths(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  int n_ctas, cudaStream_t st) {
-  constexpr int smem = ChCfg<D>::SMEM > DecCfg<D, G>::SMEM + 1024 ? ChCfg<D>::SMEM : DecCfg<D, G>::SMEM + 1024;
+  constexpr int smem = ChCfg<D>::SMEM > DecCfg<D, G>::SMEM ? ChCfg<D>::SMEM : DecCfg<D, G>::SMEM;
   static_assert(smem <= 232448, "attention kernel exceeds the per-CTA shared-memory limit");
   static bool configured = false;
   if (!configured) {

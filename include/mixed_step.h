@@ -68,7 +68,8 @@ enum {
   MS_STATUS_BAD_POSITION = 2,  /* position outside the cos/sin table */
   MS_STATUS_BAD_PAGE = 4,      /* block_tables entry outside the page pool */
   MS_STATUS_TIMEOUT = 8,       /* a bounded in-kernel wait gave up */
-  MS_STATUS_BAD_META = 16      /* inconsistent row metadata (lengths, offsets) */
+  MS_STATUS_BAD_META = 16,     /* inconsistent row metadata (lengths, offsets) */
+  MS_STATUS_INTERNAL = 32      /* an internal invariant failed (shared-memory alignment) */
 };
 
 /* One request as the scheduler sees it.
