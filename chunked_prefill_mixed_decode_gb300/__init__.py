@@ -39,13 +39,18 @@ class Request(ctypes.Structure):
                 ("block_table", ctypes.POINTER(ctypes.c_int32)), ("num_pages", ctypes.c_int32)]
 
 
+POLICY_DECODE_FIRST, POLICY_PREFILL_FIRST, POLICY_FAIR_SHARE = 0, 1, 2
+
+
 class SchedConfig(ctypes.Structure):
-    _fields_ = [("token_budget", ctypes.c_int32), ("max_chunk_per_request", ctypes.c_int32)]
+    _fields_ = [("token_budget", ctypes.c_int32), ("max_chunk_per_request", ctypes.c_int32),
+                ("policy", ctypes.c_int32), ("min_chunk_per_request", ctypes.c_int32),
+                ("prefill_quota", ctypes.c_int32), ("decode_share_permille", ctypes.c_int32)]
 
 
 class BatchInfo(ctypes.Structure):
     _fields_ = [("num_rows", ctypes.c_int32), ("num_decodes", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
-                ("bt_stride", ctypes.c_int32), ("unused_tokens", ctypes.c_int32)]
+                ("bt_stride", ctypes.c_int32), ("unused_tokens", ctypes.c_int32), ("num_deferred", ctypes.c_int32)]
 
 
 _lib_handle = None
@@ -115,8 +120,10 @@ def _stream(stream) -> int:
 # ---------------------------------------------------------------------------- host
 
 def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndarray], token_budget: int,
-                         max_chunk_per_request: int = 0) -> dict:
-    """Decode-first token-budget packing + varlen metadata (ms_build_batch_metadata).
+                         max_chunk_per_request: int = 0, policy: int = POLICY_DECODE_FIRST,
+                         min_chunk_per_request: int = 0, prefill_quota: int = 0,
+                         decode_share_permille: int = 500) -> dict:
+    """Token-budget packing + varlen metadata (ms_build_batch_metadata).
 
     ``states[i] = (cached_len, remaining_prompt)``; ``block_tables[i]`` is an
     int32 array of that request's physical pages.  Returns numpy int32 arrays
@@ -130,7 +137,8 @@ def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndar
         reqs[i].remaining_prompt = int(rem)
         reqs[i].block_table = _i32(bt) if len(bt) else None
         reqs[i].num_pages = len(bt)
-    cfg = SchedConfig(int(token_budget), int(max_chunk_per_request))
+    cfg = SchedConfig(int(token_budget), int(max_chunk_per_request), int(policy), int(min_chunk_per_request),
+                      int(prefill_quota), int(decode_share_permille))
     cap_rows = max(n, 1)
     cap_tokens = max(int(token_budget), 1)
     max_pages = max([len(bt) for bt in tables] + [1])
@@ -161,6 +169,7 @@ def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndar
         "num_decodes": info.num_decodes,
         "num_tokens": T,
         "unused_tokens": info.unused_tokens,
+        "num_deferred": info.num_deferred,
     }
 
 

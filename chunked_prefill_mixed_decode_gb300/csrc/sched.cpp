@@ -1,14 +1,17 @@
-// Host side of the mixed step: decode-first token-budget packing, varlen
-// metadata, and the rotary cos/sin table.
+// Host side of the mixed step: token-budget packing, varlen metadata, and the
+// rotary cos/sin table.
 //
-// Packing follows "Chunked Prefill 的 Token 预算" (zwjcode.cn), sections 03-05
-// and 08, and "Chunked Prefill: Ending the Great Stall", sections 03-04: every
-// running decode is placed first at one token each; then prompts are visited
-// in arrival order and each takes the largest chunk that fits what is left
-// (optionally capped per request, as in "Prefill head-of-line blocking",
-// "The fix").  The metadata is the zwjcode page's section 06 list: absolute
-// positions, one physical slot per new token, the block table, and the
-// context length after the round.
+// Default packing follows "Chunked Prefill 的 Token 预算" (zwjcode.cn),
+// sections 03-05 and 08, and "Chunked Prefill: Ending the Great Stall",
+// sections 03-04: every running decode is placed first at one token each; then
+// prompts are visited in arrival order and each takes the largest chunk that
+// fits what is left.  Per-prompt limits come from "Prefill head-of-line
+// blocking" (a ceiling in "The fix", a floor in "What comes next"), the prefill
+// quota from zwjcode section 08, and the prefill-first and fair-share orders
+// from "Splitting Prefill From Decode Inside a Step", "Choosing the priority
+// order".  The metadata is the zwjcode page's section 06 list: absolute
+// positions, one physical slot per new token, the block table, and the context
+// length after the round.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -41,35 +44,80 @@ extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_
     return MS_ERR_ARG;
   const int32_t budget = cfg->token_budget;
   const int32_t cap = cfg->max_chunk_per_request;
-  if (budget < 0 || cap < 0) return MS_ERR_ARG;
+  const int32_t floor_ = cfg->min_chunk_per_request;
+  const int32_t quota = cfg->prefill_quota;
+  const int32_t share = cfg->decode_share_permille;
+  const int32_t policy = cfg->policy;
+  if (budget < 0 || cap < 0 || floor_ < 0 || quota < 0 || share < 0 || share > 1000 ||
+      (policy != MS_POLICY_DECODE_FIRST && policy != MS_POLICY_PREFILL_FIRST && policy != MS_POLICY_FAIR_SHARE))
+    return MS_ERR_ARG;
   for (int32_t i = 0; i < n_req; ++i) {
     if (reqs[i].cached_len < 0 || reqs[i].remaining_prompt < 0 || reqs[i].num_pages < 0 ||
         (reqs[i].num_pages > 0 && reqs[i].block_table == nullptr))
       return MS_ERR_ARG;
   }
 
-  // 1. running decodes first, one token each, in input order
+  // 1. the two classes, each in input order
+  std::vector<int32_t> dec, pr;
+  for (int32_t i = 0; i < n_req; ++i) (reqs[i].remaining_prompt == 0 ? dec : pr).push_back(i);
+  const int64_t n_decodes = static_cast<int64_t>(dec.size());
+  auto limit = [&](int32_t i) -> int64_t {
+    const int64_t rem = reqs[i].remaining_prompt;
+    return cap > 0 && rem > cap ? cap : rem;
+  };
+  // 2. prompts' takes out of an allowance: the floor first, then the leftover, both in arrival order
+  std::vector<int64_t> take(static_cast<size_t>(n_req), 0);
+  auto prompt_takes = [&](int64_t allowance) -> int64_t {
+    int64_t left = allowance;
+    if (floor_ > 0) {
+      for (int32_t i : pr) {
+        if (left == 0) break;
+        int64_t t = limit(i) < floor_ ? limit(i) : floor_;
+        if (t > left) t = left;
+        take[i] += t;
+        left -= t;
+      }
+    }
+    for (int32_t i : pr) {
+      if (left == 0) break;
+      int64_t t = limit(i) - take[i];
+      if (t > left) t = left;
+      take[i] += t;
+      left -= t;
+    }
+    return allowance - left;
+  };
+  int64_t n_dec = 0;
+  if (policy == MS_POLICY_DECODE_FIRST) {
+    int64_t dec_cap = budget;
+    if (quota > 0) {
+      int64_t demand = 0;  // the quota reserves only what the waiting prompts can use
+      for (int32_t i : pr) demand += limit(i);
+      dec_cap = budget - (quota < demand ? quota : demand);
+    } else if (n_decodes > budget) {
+      return MS_ERR_BUDGET;
+    }
+    n_dec = n_decodes < dec_cap ? n_decodes : (dec_cap > 0 ? dec_cap : 0);
+    prompt_takes(budget - n_dec);
+  } else if (policy == MS_POLICY_PREFILL_FIRST) {
+    const int64_t used_p = prompt_takes(budget);
+    n_dec = n_decodes < budget - used_p ? n_decodes : budget - used_p;
+  } else {
+    const int64_t allow = static_cast<int64_t>(budget) * share / 1000;
+    n_dec = n_decodes < allow ? n_decodes : allow;
+    const int64_t used_p = prompt_takes(budget - n_dec);
+    n_dec = n_decodes < budget - used_p ? n_decodes : budget - used_p;
+  }
   std::vector<Row> rows;
   rows.reserve(static_cast<size_t>(n_req));
-  int32_t used = 0;
-  for (int32_t i = 0; i < n_req; ++i)
-    if (reqs[i].remaining_prompt == 0) rows.push_back({i, reqs[i].cached_len, 1});
-  const int32_t num_decodes = static_cast<int32_t>(rows.size());
-  if (num_decodes > budget) return MS_ERR_BUDGET;
-  used = num_decodes;
-
-  // 2. prompts in arrival order fill the leftover budget
-  for (int32_t i = 0; i < n_req; ++i) {
-    if (reqs[i].remaining_prompt == 0) continue;
-    const int32_t leftover = budget - used;
-    if (leftover == 0) break;
-    int32_t take = reqs[i].remaining_prompt < leftover ? reqs[i].remaining_prompt : leftover;
-    if (cap > 0 && take > cap) take = cap;
-    if (take > 0) {
-      rows.push_back({i, reqs[i].cached_len, take});
-      used += take;
+  for (int64_t k = 0; k < n_dec; ++k) rows.push_back({dec[k], reqs[dec[k]].cached_len, 1});
+  int64_t used = n_dec;
+  for (int32_t i : pr)
+    if (take[i] > 0) {
+      rows.push_back({i, reqs[i].cached_len, static_cast<int32_t>(take[i])});
+      used += take[i];
     }
-  }
+  const int32_t num_decodes = static_cast<int32_t>(n_dec);
 
   // 3. capacities and page coverage
   const int32_t S = static_cast<int32_t>(rows.size());
@@ -82,6 +130,7 @@ extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_
     if (need > stride) stride = need;
   }
   if (S > cap_rows || used > cap_tokens || static_cast<int64_t>(S) * stride > cap_bt) return MS_ERR_ARG;
+  if (n_req > 0 && num_scheduled == nullptr) return MS_ERR_ARG;
   if (used > 0 && (positions == nullptr || slot_mapping == nullptr)) return MS_ERR_ARG;
   if (static_cast<int64_t>(S) * stride > 0 && block_tables == nullptr) return MS_ERR_ARG;
 
@@ -108,9 +157,10 @@ extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_
   }
   info->num_rows = S;
   info->num_decodes = num_decodes;
-  info->num_tokens = used;
+  info->num_tokens = static_cast<int32_t>(used);
   info->bt_stride = stride;
-  info->unused_tokens = budget - used;
+  info->unused_tokens = static_cast<int32_t>(budget - used);
+  info->num_deferred = static_cast<int32_t>(n_decodes - n_dec);
   return MS_OK;
 }
 

@@ -86,22 +86,46 @@ typedef struct {
   int32_t num_pages;
 } ms_request;
 
+/* Priority orders of one round ([mer] "Choosing the priority order"). */
+enum {
+  MS_POLICY_DECODE_FIRST = 0,  /* every running decode, then prompts take the leftover (stall-free) */
+  MS_POLICY_PREFILL_FIRST = 1, /* prompts take the budget first, decodes whatever remains */
+  MS_POLICY_FAIR_SHARE = 2     /* decodes may use decode_share_permille of the budget, prompts the
+                                  rest; what one class leaves unused goes to the other */
+};
+
 /* token_budget           B_tok, the most tokens one step may hold
  *                        ([zwj] section 04: |D_t| + sum |c| <= B_tok)
- * max_chunk_per_request  per-prefill cap on one round's take; 0 = no cap
- *                        ([sfe] "The fix", [mer] build_batch's chunk_size) */
+ * max_chunk_per_request  ceiling on one prompt's take per round; 0 = none
+ *                        ([sfe] "The fix", [mer] build_batch's chunk_size)
+ * policy                 MS_POLICY_*
+ * min_chunk_per_request  floor: every waiting prompt first gets up to this many
+ *                        tokens (arrival order), then the leftover is handed out
+ *                        in arrival order; 0 = none ([sfe] "What comes next")
+ * prefill_quota          decode-first only: while prompts wait, decodes use at
+ *                        most budget - min(quota, what the prompts can take) and
+ *                        the rest wait a round ([zwj] section 08: a reserved
+ *                        prefill quota against starvation); 0 = none
+ * decode_share_permille  fair share only: the decode class's share of the
+ *                        budget, 0..1000 */
 typedef struct {
   int32_t token_budget;
   int32_t max_chunk_per_request;
+  int32_t policy;
+  int32_t min_chunk_per_request;
+  int32_t prefill_quota;
+  int32_t decode_share_permille;
 } ms_sched_config;
 
-/* Summary of one packed step.  bt_stride is the row stride of block_tables. */
+/* Summary of one packed step.  bt_stride is the row stride of block_tables;
+ * num_deferred counts running decodes the policy left for a later round. */
 typedef struct {
   int32_t num_rows;
   int32_t num_decodes;
   int32_t num_tokens;
   int32_t bt_stride;
   int32_t unused_tokens;
+  int32_t num_deferred;
 } ms_batch_info;
 
 /* ms_build_batch_metadata -- pack one round, decode first ([zwj] sections
@@ -109,10 +133,13 @@ typedef struct {
  * ([zwj] section 06).  Host only; pure (reqs are not modified: the caller
  * commits progress after the step, [zwj] section 08).
  *
- * Packing: every request with remaining_prompt == 0 is a decode row (c, 1), in
- * input order; more decodes than token_budget is MS_ERR_BUDGET.  Then, in input
- * order, each prompt takes min(remaining, leftover, cap) tokens as a chunk row
- * (c, take); packing stops when the leftover reaches 0.
+ * Packing (decode-first, no quota): every request with remaining_prompt == 0
+ * is a decode row (c, 1), in input order; more decodes than token_budget is
+ * MS_ERR_BUDGET.  Then, in input order, each prompt takes min(remaining,
+ * leftover, cap) tokens as a chunk row (c, take); packing stops when the
+ * leftover reaches 0.  The other policies and limits of ms_sched_config change
+ * how the budget is split; rows are always the scheduled decodes in input
+ * order, then the chunks in input order.
  *
  * Outputs (host, caller-allocated, capacities in elements):
  *   cu_seqlens_q  [cap_rows + 1]  row token offsets, cu[0] = 0

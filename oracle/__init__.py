@@ -23,12 +23,14 @@ Pins (tests/test_oracle.py) tie every function to values the pages print,
 closed forms, invariants and library routines.  No function here is
 "parity unpinned".
 """
-from .schedule import BudgetError, NoPagesError, schedule, batch_metadata, commit_round
+from .schedule import (BudgetError, NoPagesError, schedule, batch_metadata, commit_round, DECODE_FIRST,
+                       PREFILL_FIRST, FAIR_SHARE)
 from .rope import bf16_to_f64, f32_to_bf16_bits, rope_tables, rope_rotate, kv_append
 from .attention import attention_rows, attention_all
 
 __all__ = [
-    "BudgetError", "NoPagesError", "schedule", "batch_metadata", "commit_round",
+    "BudgetError", "NoPagesError", "schedule", "batch_metadata", "commit_round", "DECODE_FIRST",
+    "PREFILL_FIRST", "FAIR_SHARE",
     "bf16_to_f64", "f32_to_bf16_bits", "rope_tables", "rope_rotate", "kv_append",
     "attention_rows", "attention_all",
 ]

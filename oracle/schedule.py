@@ -39,30 +39,82 @@ class NoPagesError(ValueError):
     """A request's block table cannot address the tokens scheduled for it."""
 
 
-def schedule(states: Sequence[tuple], token_budget: int, max_chunk: int = 0):
+DECODE_FIRST, PREFILL_FIRST, FAIR_SHARE = 0, 1, 2
+
+
+def schedule(states: Sequence[tuple], token_budget: int, max_chunk: int = 0, policy: int = DECODE_FIRST,
+             min_chunk: int = 0, prefill_quota: int = 0, decode_share: int = 500):
     """Pack one round.
 
     ``states[i] = (cached_len, remaining)``; remaining == 0 marks a running
     decode.  Returns ``(rows, unused)`` where rows is a list of
-    ``(request_index, c, d)`` and unused the budget left over.
+    ``(request_index, c, d)`` -- decode rows first, in input order, then
+    chunk rows in input order -- and unused the budget left over.
+
+    Policies ("Splitting Prefill From Decode Inside a Step", "Choosing the
+    priority order"):
+      DECODE_FIRST   every running decode, then prompts in arrival order take
+                     what is left (zwjcode sections 05 and 08);
+      PREFILL_FIRST  prompts take the budget first, decodes whatever remains;
+      FAIR_SHARE     decodes may use decode_share / 1000 of the budget and
+                     prompts the rest; what one class leaves unused goes to
+                     the other.
+    Per-prompt limits ("Prefill head-of-line blocking", "The fix" and "What
+    comes next"): max_chunk caps one prompt's take per round (a ceiling);
+    min_chunk is a floor -- every waiting prompt first gets up to min_chunk
+    tokens in arrival order, then the leftover is handed out in arrival order.
+    prefill_quota (zwjcode section 08, "reserve a prefill quota"; section 16,
+    exercise 3): while prompts wait, decodes use at most budget - min(quota,
+    what the prompts can take) tokens and the others wait for a later round.  Without a quota, DECODE_FIRST
+    treats more decodes than the budget as an error (zwjcode section 05);
+    the other policies defer them.
     """
     decodes = [i for i, (_, rem) in enumerate(states) if rem == 0]
-    if len(decodes) > token_budget:
-        raise BudgetError(f"{len(decodes)} decodes exceed the token budget {token_budget}")
-    rows = [(i, int(states[i][0]), 1) for i in decodes]
-    leftover = token_budget - len(decodes)
-    for i, (c, rem) in enumerate(states):
-        if rem == 0:
-            continue
-        if leftover == 0:
-            break
-        take = min(int(rem), leftover)
-        if max_chunk > 0:
-            take = min(take, max_chunk)
-        if take > 0:
-            rows.append((i, int(c), take))
-            leftover -= take
-    return rows, leftover
+    prompts = [i for i, (_, rem) in enumerate(states) if rem > 0]
+    B = token_budget
+
+    def prompt_takes(allowance):
+        """Tokens per prompt (arrival order) out of `allowance`, with floor and ceiling."""
+        take = {i: 0 for i in prompts}
+        left = allowance
+        limit = {i: states[i][1] if max_chunk <= 0 else min(states[i][1], max_chunk) for i in prompts}
+        if min_chunk > 0:  # pass 1: the floor
+            for i in prompts:
+                if left == 0:
+                    break
+                t = min(limit[i], min_chunk, left)
+                take[i] += t
+                left -= t
+        for i in prompts:  # the leftover, in arrival order
+            if left == 0:
+                break
+            t = min(limit[i] - take[i], left)
+            take[i] += t
+            left -= t
+        return take, allowance - left
+
+    if policy == DECODE_FIRST:
+        # the quota reserves only what the waiting prompts can use this round
+        demand = sum(states[i][1] if max_chunk <= 0 else min(states[i][1], max_chunk) for i in prompts)
+        dec_cap = B - min(prefill_quota, demand) if prefill_quota > 0 else B
+        if prefill_quota <= 0 and len(decodes) > B:
+            raise BudgetError(f"{len(decodes)} decodes exceed the token budget {B}")
+        n_dec = min(len(decodes), max(dec_cap, 0))
+        take, used_p = prompt_takes(B - n_dec)
+    elif policy == PREFILL_FIRST:
+        take, used_p = prompt_takes(B)
+        n_dec = min(len(decodes), B - used_p)
+    elif policy == FAIR_SHARE:
+        dec_allow = (B * decode_share) // 1000
+        n_dec = min(len(decodes), dec_allow)
+        take, used_p = prompt_takes(B - n_dec)
+        n_dec = min(len(decodes), B - used_p)  # prompts left some over: decodes may take it
+    else:
+        raise ValueError(f"unknown policy {policy}")
+    rows = [(i, int(states[i][0]), 1) for i in decodes[:n_dec]]
+    rows += [(i, int(states[i][0]), take[i]) for i in prompts if take[i] > 0]
+    used = n_dec + sum(take.values())
+    return rows, B - used
 
 
 def batch_metadata(rows, block_tables: Sequence[np.ndarray], n_requests: int,

@@ -108,6 +108,44 @@ def test_scheduler_fuzz_bit_exact(ms):
             assert e.value.code == err
 
 
+@pytest.mark.parametrize("policy", [0, 1, 2])
+def test_policies_fuzz_bit_exact(ms, policy):
+    """Every scheduling policy and limit: the C++ scheduler's rows and metadata equal the oracle's."""
+    rng = np.random.default_rng(400 + policy)
+    for trial in range(300):
+        n = int(rng.integers(0, 12))
+        budget = int(rng.integers(0, 40))
+        cap = int(rng.integers(0, 2)) * int(rng.integers(1, 16))
+        floor = int(rng.integers(0, 2)) * int(rng.integers(1, 12))
+        quota = int(rng.integers(0, 2)) * int(rng.integers(0, budget + 1))
+        share = int(rng.integers(0, 1001))
+        states, tables = [], []
+        for _ in range(n):
+            c = int(rng.integers(0, 100))
+            rem = 0 if rng.random() < 0.5 else int(rng.integers(1, 60))
+            need = -(-(c + max(rem, 1)) // 16)
+            tables.append(rng.integers(0, 1000, size=need).astype(np.int32))
+            states.append((c, rem))
+        kw = dict(policy=policy, min_chunk=floor, prefill_quota=quota, decode_share=share)
+        try:
+            rows, unused = oracle.schedule(states, budget, cap, **kw)
+            n_dec = sum(1 for i, _, d in rows if states[i][1] == 0)
+            ref = oracle.batch_metadata(rows, tables, n, num_decodes=n_dec)
+            ref["unused_tokens"] = unused
+            err = None
+        except oracle.BudgetError:
+            err = ms.MS_ERR_BUDGET
+        if err is None:
+            got = ms.build_batch_metadata(states, tables, budget, cap, policy, floor, quota, share)
+            _assert_meta_equal(got, ref)
+            n_decodes = sum(1 for s_ in states if s_[1] == 0)
+            assert got["num_deferred"] == n_decodes - ref["num_decodes"]
+        else:
+            with pytest.raises(ms.MixedStepError) as e:
+                ms.build_batch_metadata(states, tables, budget, cap, policy, floor, quota, share)
+            assert e.value.code == err
+
+
 def test_rope_table_bit_exact_with_oracle(ms):
     for D in (64, 128):
         max_pos = 131073
