@@ -53,6 +53,12 @@ class BatchInfo(ctypes.Structure):
                 ("bt_stride", ctypes.c_int32), ("unused_tokens", ctypes.c_int32), ("num_deferred", ctypes.c_int32)]
 
 
+class EngineStats(ctypes.Structure):
+    _fields_ = [("num_live", ctypes.c_int32), ("num_prefilling", ctypes.c_int32),
+                ("num_free_pages", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("max_request_pages", ctypes.c_int32), ("rounds", ctypes.c_int64)]
+
+
 _lib_handle = None
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _VP = ctypes.c_void_p
@@ -93,6 +99,17 @@ def lib() -> ctypes.CDLL:
     h.ms_read_status.argtypes = [_VP, _VP, _I32P]
     h.ms_num_sms.restype = ctypes.c_int
     h.ms_num_sms.argtypes = []
+    for name, args in (
+            ("ms_engine_create", [ctypes.c_int32, ctypes.POINTER(SchedConfig), ctypes.POINTER(_VP)]),
+            ("ms_engine_destroy", [_VP]),
+            ("ms_engine_add_request", [_VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _I32P]),
+            ("ms_engine_request_pages", [_VP, ctypes.c_int32, _I32P, ctypes.c_int32, _I32P]),
+            ("ms_engine_plan", [_VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _I32P, _I32P, _I32P, _I32P,
+                                _I32P, _I32P, _I32P, ctypes.POINTER(BatchInfo)]),
+            ("ms_engine_commit", [_VP, _I32P, ctypes.c_int32, _I32P]),
+            ("ms_engine_stats", [_VP, ctypes.POINTER(EngineStats)])):
+        getattr(h, name).restype = ctypes.c_int
+        getattr(h, name).argtypes = args
     _lib_handle = h
     return h
 
@@ -171,6 +188,88 @@ def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndar
         "unused_tokens": info.unused_tokens,
         "num_deferred": info.num_deferred,
     }
+
+
+class Engine:
+    """Multi-round engine over a page pool (ms_engine_*): full-input admission, then
+    plan / device step / commit every round."""
+
+    def __init__(self, num_pages: int, token_budget: int, max_chunk_per_request: int = 0,
+                 policy: int = POLICY_DECODE_FIRST, min_chunk_per_request: int = 0, prefill_quota: int = 0,
+                 decode_share_permille: int = 500):
+        self._h = None
+        self.token_budget = int(token_budget)
+        cfg = SchedConfig(int(token_budget), int(max_chunk_per_request), int(policy), int(min_chunk_per_request),
+                          int(prefill_quota), int(decode_share_permille))
+        h = _VP()
+        _check(lib().ms_engine_create(int(num_pages), ctypes.byref(cfg), ctypes.byref(h)), "ms_engine_create")
+        self._h = h
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None and _lib_handle is not None:
+            _lib_handle.ms_engine_destroy(self._h)
+            self._h = None
+
+    def add_request(self, prompt_len: int, max_new_tokens: int, cached_len: int = 0) -> int:
+        """Admit a request; raises MixedStepError(MS_ERR_NO_PAGES) when the pool cannot hold it."""
+        rid = ctypes.c_int32()
+        _check(lib().ms_engine_add_request(self._h, int(prompt_len), int(max_new_tokens), int(cached_len),
+                                           ctypes.byref(rid)), "ms_engine_add_request")
+        return rid.value
+
+    def stats(self) -> dict:
+        st = EngineStats()
+        _check(lib().ms_engine_stats(self._h, ctypes.byref(st)), "ms_engine_stats")
+        return {k: getattr(st, k) for k, _ in EngineStats._fields_}
+
+    def request_pages(self, request_id: int) -> np.ndarray:
+        n = ctypes.c_int32()
+        cap = self.stats()["max_request_pages"]
+        out = np.zeros(max(cap, 1), dtype=np.int32)
+        _check(lib().ms_engine_request_pages(self._h, int(request_id), _i32(out), cap, ctypes.byref(n)),
+               "ms_engine_request_pages")
+        return out[: n.value].copy()
+
+    def plan(self) -> dict:
+        """Pack the next round; the metadata of build_batch_metadata plus row_request_id."""
+        st = self.stats()
+        cap_rows = max(st["num_live"], 1)
+        cap_tokens = max(self.token_budget, 1)
+        cap_bt = cap_rows * max(st["max_request_pages"], 1)
+        out = {k: np.zeros(sz, dtype=np.int32) for k, sz in (
+            ("cu_seqlens_q", cap_rows + 1), ("q_start_pos", cap_rows), ("context_lens", cap_rows),
+            ("positions", cap_tokens), ("slot_mapping", cap_tokens), ("block_tables", cap_bt),
+            ("row_request_id", cap_rows))}
+        info = BatchInfo()
+        rc = lib().ms_engine_plan(self._h, cap_rows, cap_tokens, cap_bt, _i32(out["cu_seqlens_q"]),
+                                  _i32(out["q_start_pos"]), _i32(out["context_lens"]), _i32(out["positions"]),
+                                  _i32(out["slot_mapping"]), _i32(out["block_tables"]),
+                                  _i32(out["row_request_id"]), ctypes.byref(info))
+        _check(rc, "ms_engine_plan")
+        S, T, stride = info.num_rows, info.num_tokens, info.bt_stride
+        return {
+            "cu_seqlens_q": out["cu_seqlens_q"][: S + 1].copy(),
+            "q_start_pos": out["q_start_pos"][:S].copy(),
+            "context_lens": out["context_lens"][:S].copy(),
+            "positions": out["positions"][:T].copy(),
+            "slot_mapping": out["slot_mapping"][:T].copy(),
+            "block_tables": out["block_tables"][: S * stride].reshape(S, stride).copy(),
+            "bt_stride": stride,
+            "row_request_id": out["row_request_id"][:S].copy(),
+            "num_rows": S,
+            "num_decodes": info.num_decodes,
+            "num_tokens": T,
+            "unused_tokens": info.unused_tokens,
+            "num_deferred": info.num_deferred,
+        }
+
+    def commit(self) -> list:
+        """Advance the planned rows; returns the ids of the requests that finished."""
+        cap = max(self.stats()["num_live"], 1)
+        ids = np.zeros(cap, dtype=np.int32)
+        n = ctypes.c_int32()
+        _check(lib().ms_engine_commit(self._h, _i32(ids), cap, ctypes.byref(n)), "ms_engine_commit")
+        return ids[: n.value].tolist()
 
 
 def rope_table(max_pos: int, D: int, base: float = 10000.0):

@@ -267,6 +267,75 @@ MS_API int ms_mixed_step_attention_noalloc(const void* q_rot, const void* k_cach
                                            int32_t page_size, float scale, void* out, int32_t* dev_status,
                                            ms_stream_t stream);
 
+/* ---- Multi-round engine (host) ------------------------------------------
+ * A page pool with full-input admission and a plan/commit round driver over
+ * ms_build_batch_metadata.  A request reserves ceil((prompt_len +
+ * max_new_tokens) / 16) pages when it is admitted, before its first chunk, or
+ * is refused ([mer] "The arithmetic of chunk boundaries"; [zwj] section 11,
+ * admission against the complete input length).  Each round is plan (pack the
+ * live requests in arrival order), the caller's device step, then commit
+ * ([zwj] section 08: progress is committed after the step).  The last prompt
+ * chunk yields a request's first new token, each decode one more; a request
+ * with max_new_tokens tokens is finished and its pages go back to the pool.
+ * Pages are handed out last-in-first-out from a free list that starts as
+ * num_pages-1 .. 0 (so the first request gets 0, 1, 2, ...); a finished
+ * request returns its pages in block-table order.  Not thread-safe: one
+ * engine per host thread. */
+typedef struct ms_engine ms_engine;
+
+typedef struct {
+  int32_t num_live;        /* admitted and not finished */
+  int32_t num_prefilling;  /* live requests with prompt tokens left */
+  int32_t num_free_pages;
+  int32_t num_pages;
+  int32_t max_request_pages; /* largest block table of a live request (sizes plan's cap_bt) */
+  int64_t rounds;          /* committed rounds */
+} ms_engine_counts;
+
+/* ms_engine_create -- a pool of num_pages pages and a copy of *cfg (the
+ * packing of every round).  *out owns the engine until ms_engine_destroy.
+ * Errors: MS_ERR_ARG (null pointer, num_pages < 0, out of host memory). */
+MS_API int ms_engine_create(int32_t num_pages, const ms_sched_config* cfg, ms_engine** out);
+
+/* ms_engine_destroy -- frees the engine (NULL is a no-op). */
+MS_API int ms_engine_destroy(ms_engine* e);
+
+/* ms_engine_add_request -- admit a prompt of prompt_len tokens, cached_len of
+ * them already in the cache ([sar] section 05: only the rest is prefilled),
+ * that will generate max_new_tokens tokens; *request_id gets its id (0, 1, ...
+ * in admission order).  A fully cached prompt is a running decode that has
+ * its first new token, so it must ask for at least two.
+ * Errors: MS_ERR_ARG (prompt_len < 1, max_new_tokens < 1, cached_len outside
+ * 0..prompt_len, the fully cached case with max_new_tokens < 2),
+ * MS_ERR_NO_PAGES (refused: not enough free pages; nothing changes). */
+MS_API int ms_engine_add_request(ms_engine* e, int32_t prompt_len, int32_t max_new_tokens, int32_t cached_len,
+                                 int32_t* request_id);
+
+/* ms_engine_request_pages -- the block table of a live request: *num_pages
+ * and, when cap allows, the page ids in logical order into pages (host).
+ * Errors: MS_ERR_ARG (unknown id, cap too small, null pointer). */
+MS_API int ms_engine_request_pages(const ms_engine* e, int32_t request_id, int32_t* pages, int32_t cap,
+                                   int32_t* num_pages);
+
+/* ms_engine_plan -- pack the next round over the live requests and write its
+ * metadata exactly as ms_build_batch_metadata does (same outputs, capacities
+ * and errors), with row_request_id [cap_rows] holding each row's request id
+ * instead of its index.  Planning again before commit replaces the plan. */
+MS_API int ms_engine_plan(ms_engine* e, int32_t cap_rows, int32_t cap_tokens, int64_t cap_bt,
+                          int32_t* cu_seqlens_q, int32_t* q_start_pos, int32_t* context_lens,
+                          int32_t* positions, int32_t* slot_mapping, int32_t* block_tables,
+                          int32_t* row_request_id, ms_batch_info* info);
+
+/* ms_engine_commit -- advance every row of the last plan (a decode by one
+ * token, a chunk by its length), release finished requests and write their
+ * ids, in arrival order, to finished_ids [cap_finished] (host).
+ * Errors: MS_ERR_ARG (no plan since the last commit, cap_finished smaller
+ * than the number finishing; nothing changes). */
+MS_API int ms_engine_commit(ms_engine* e, int32_t* finished_ids, int32_t cap_finished, int32_t* num_finished);
+
+/* ms_engine_stats -- counts of the pool and the live requests. */
+MS_API int ms_engine_stats(const ms_engine* e, ms_engine_counts* out);
+
 /* ms_read_status -- waits for `stream`, copies the int32 device status word at
  * dev_status (for attention: the workspace pointer) to *host_status and
  * clears it.  Returns MS_OK, MS_ERR_DEVICE when the word was non-zero, or

@@ -17,7 +17,10 @@ in the pages' order and notation:
 * ``rope``      -- rotary embedding at absolute positions (zwjcode section 07)
   and the paged K/V append through ``slot_mapping`` (zwjcode section 06);
 * ``attention`` -- causal attention of every query at absolute position p over
-  keys 0..p read through the block table (zwjcode sections 02 and 07).
+  keys 0..p read through the block table (zwjcode sections 02 and 07);
+* ``engine``    -- a multi-round driver over a page pool that reserves a
+  request's full input plus its new tokens at admission (zwjcode section 11;
+  "Splitting Prefill From Decode Inside a Step").
 
 Pins (tests/test_oracle.py) tie every function to values the pages print,
 closed forms, invariants and library routines.  No function here is
@@ -27,10 +30,11 @@ from .schedule import (BudgetError, NoPagesError, schedule, batch_metadata, comm
                        PREFILL_FIRST, FAIR_SHARE)
 from .rope import bf16_to_f64, f32_to_bf16_bits, rope_tables, rope_rotate, kv_append
 from .attention import attention_rows, attention_all
+from .engine import AdmissionError, Engine
 
 __all__ = [
     "BudgetError", "NoPagesError", "schedule", "batch_metadata", "commit_round", "DECODE_FIRST",
     "PREFILL_FIRST", "FAIR_SHARE",
     "bf16_to_f64", "f32_to_bf16_bits", "rope_tables", "rope_rotate", "kv_append",
-    "attention_rows", "attention_all",
+    "attention_rows", "attention_all", "AdmissionError", "Engine",
 ]

@@ -184,3 +184,77 @@ def test_workspace_size_grows_with_context(ms):
     b = ms.attention_workspace_size(65, 512, 2 * 64 * 4096, 32, 32, 128)
     assert 0 < a < b
     assert ms.attention_workspace_size(1, 1, 0, 4, 2, 96) == 0
+
+
+def _engine_pair(ms, num_pages, budget, **kw):
+    okw = dict(max_chunk=kw.get("max_chunk_per_request", 0), policy=kw.get("policy", 0),
+               min_chunk=kw.get("min_chunk_per_request", 0), prefill_quota=kw.get("prefill_quota", 0),
+               decode_share=kw.get("decode_share_permille", 500))
+    return ms.Engine(num_pages, budget, **kw), oracle.Engine(num_pages, budget, **okw)
+
+
+@pytest.mark.parametrize("policy", [0, 1, 2])
+def test_engine_simulation_bit_exact(ms, policy):
+    """Random arrivals over many rounds: the C++ engine's admissions, metadata, finished ids and
+    pool counts equal the oracle engine's at every round."""
+    rng = np.random.default_rng(700 + policy)
+    for trial in range(6):
+        budget = int(rng.integers(8, 96))
+        kw = dict(max_chunk_per_request=int(rng.integers(0, 2)) * int(rng.integers(1, 40)), policy=policy,
+                  min_chunk_per_request=int(rng.integers(0, 2)) * int(rng.integers(1, 16)),
+                  prefill_quota=int(rng.integers(0, 2)) * int(rng.integers(1, budget)) if policy == 0 else 0,
+                  decode_share_permille=int(rng.integers(0, 1001)))
+        num_pages = int(rng.integers(20, 300))
+        got, ref = _engine_pair(ms, num_pages, budget, **kw)
+        rounds = 0
+        for rnd in range(150):
+            for _ in range(int(rng.integers(0, 3))):
+                pl = int(rng.integers(1, 200))
+                mn = int(rng.integers(2, 30))
+                cached = int(rng.integers(0, pl + 1)) if rng.random() < 0.25 else 0
+                try:
+                    want = ref.add_request(pl, mn, cached)
+                except oracle.AdmissionError:
+                    with pytest.raises(ms.MixedStepError) as e:
+                        got.add_request(pl, mn, cached)
+                    assert e.value.code == ms.MS_ERR_NO_PAGES
+                    continue
+                assert got.add_request(pl, mn, cached) == want
+                np.testing.assert_array_equal(got.request_pages(want), ref.live[-1].pages)
+            if not ref.live:
+                continue
+            try:
+                r = ref.plan()
+            except oracle.BudgetError:
+                with pytest.raises(ms.MixedStepError) as e:
+                    got.plan()
+                assert e.value.code == ms.MS_ERR_BUDGET
+                break
+            g = got.plan()
+            for k in ("cu_seqlens_q", "q_start_pos", "context_lens", "positions", "slot_mapping",
+                      "row_request_id"):
+                np.testing.assert_array_equal(g[k], r[k], err_msg=k)
+            np.testing.assert_array_equal(g["block_tables"], r["block_tables"])
+            assert g["num_decodes"] == r["num_decodes"] and g["unused_tokens"] == r["unused_tokens"]
+            assert got.commit() == ref.commit()
+            rounds += 1
+            st = got.stats()
+            assert st["num_live"] == len(ref.live) and st["num_free_pages"] == len(ref.free)
+            assert st["rounds"] == rounds
+
+
+def test_engine_argument_errors(ms):
+    e = ms.Engine(8, 16)
+    for args in ((0, 4, 0), (10, 0, 0), (10, 4, 11), (10, 1, 10), (10, 4, -1)):
+        with pytest.raises(ms.MixedStepError) as err:
+            e.add_request(*args)
+        assert err.value.code == ms.MS_ERR_ARG
+        with pytest.raises(ValueError):
+            oracle.Engine(8, 16).add_request(*args)
+    with pytest.raises(ms.MixedStepError) as err:
+        e.commit()  # no plan yet
+    assert err.value.code == ms.MS_ERR_ARG
+    with pytest.raises(ms.MixedStepError) as err:
+        e.add_request(120, 20)  # 9 pages > 8
+    assert err.value.code == ms.MS_ERR_NO_PAGES
+    assert e.stats()["num_free_pages"] == 8
