@@ -24,6 +24,7 @@ import statistics
 import subprocess
 import sys
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -446,6 +447,105 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------- step-latency timeline
+
+TIMELINE_SCENARIOS = [
+    ("decode-first, budget 512", dict(token_budget=512)),
+    ("decode-first, budget 2048", dict(token_budget=2048)),
+    ("no chunking (budget holds the whole prompt)", dict(token_budget=None)),
+    ("prefill-first, budget 512", dict(token_budget=512, policy=1)),
+    ("fair share, decode share 10 %, budget 512", dict(token_budget=512, policy=2, decode_share_permille=100)),
+]
+
+
+def _percentile(xs, q):
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q)) if len(xs) else 0.0
+
+
+def run_timeline(args, local):
+    """Rounds of the engine around a long prompt's arrival, one scenario per scheduling setting:
+    per-step prefill tokens, decode tokens and device step latency, the decodes' inter-token
+    gaps and the prompt's time to first token (one attention layer)."""
+    import torch
+
+    import chunked_prefill_mixed_decode_gb300 as ms
+    from chunked_prefill_mixed_decode_gb300 import build as msbuild
+    from chunked_prefill_mixed_decode_gb300 import step
+    from chunked_prefill_mixed_decode_gb300.driver import RoundDriver
+
+    msbuild.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    sc = workloads.long_prompt_arrival()
+    n_dec = len(sc.decode_ctx)
+    pages = sum(-(-(c + sc.decode_new) // 16) for c in sc.decode_ctx) + -(-(sc.prompt_len + sc.prompt_new) // 16)
+    shape = types.SimpleNamespace(num_pages=pages, H_q=sc.H_q, H_kv=sc.H_kv, page_size=16, D=sc.D)
+    k_cache, v_cache = workloads.kv_pool(shape, 77, device)
+    max_pos = max(max(sc.decode_ctx) + sc.decode_new, sc.prompt_len + sc.prompt_new) + 1
+    cos, sin = step.rope_tables_device(max_pos, sc.D, device)
+    big = n_dec + sc.prompt_len
+    q, k, v = workloads.step_tensors(shape, big, 78, device)
+    results = []
+    for label, kw in TIMELINE_SCENARIOS:
+        kw = dict(kw)
+        budget = kw.pop("token_budget") or big
+        eng = ms.Engine(pages, budget, **kw)
+        dec_ids = [eng.add_request(c, sc.decode_new, c) for c in sc.decode_ctx]
+        drv = RoundDriver(eng, k_cache, v_cache, cos, sin, sc.H_q, sc.H_kv, sc.D)
+        recs, pid, prompt_done_round, prefilled = [], None, None, 0
+        rnd = 0
+        while True:
+            if rnd == sc.arrival_round:
+                pid = eng.add_request(sc.prompt_len, sc.prompt_new)
+            rec = drv.step(q, k, v)
+            d = np.diff(rec["cu_seqlens_q"])
+            if pid is not None:
+                for rid, n in zip(rec["row_request_id"].tolist(), d.tolist()):
+                    if rid == pid and prompt_done_round is None:
+                        prefilled += n
+                        if prefilled == sc.prompt_len:
+                            prompt_done_round = rnd
+            recs.append(rec)
+            rnd += 1
+            if prompt_done_round is not None and rnd > prompt_done_round + sc.tail_rounds:
+                break
+            if rnd > 4000:
+                raise RuntimeError("timeline did not finish")
+        t_end = np.cumsum([r["device_ms"] for r in recs])
+        last_tok = {}
+        gaps = []
+        dec_set = set(dec_ids)
+        for s_, r in enumerate(recs):
+            for rid in r["row_request_id"][: r["decode_tokens"]].tolist():
+                if rid in dec_set:
+                    if rid in last_tok and s_ >= sc.arrival_round:
+                        gaps.append(t_end[s_] - t_end[last_tok[rid]])
+                    last_tok[rid] = s_
+        a = sc.arrival_round
+        steady = [r["device_ms"] for r in recs[4:a]]
+        window = [r["device_ms"] for r in recs[a:prompt_done_round + 1]]
+        ttft = float(t_end[prompt_done_round] - (t_end[a - 1] if a > 0 else 0.0))
+        results.append({
+            "scenario": label, "token_budget": budget,
+            "steady_step_ms": round(statistics.median(steady), 4),
+            "prefill_steps": prompt_done_round - a + 1,
+            "max_step_ms_during_prefill": round(max(window), 4),
+            "median_step_ms_during_prefill": round(statistics.median(window), 4),
+            "decode_gap_ms": {"p50": round(_percentile(gaps, 50), 4), "p99": round(_percentile(gaps, 99), 4),
+                              "max": round(max(gaps), 4) if gaps else 0.0},
+            "prompt_ttft_ms": round(ttft, 4),
+            "host_ms_median": round(statistics.median(r["host_ms"] for r in recs), 3),
+            "steps": [[r["round"], r["decode_tokens"], r["prefill_tokens"], round(r["device_ms"], 4)]
+                      for r in recs],
+        })
+        del drv, eng
+    line = {"timeline": sc.name, "layer": f"H_q {sc.H_q}, H_kv {sc.H_kv}, D {sc.D}, page 16",
+            "decodes": n_dec, "decode_ctx": "U[512, 4096]", "prompt_len": sc.prompt_len,
+            "arrival_round": sc.arrival_round, "latency": "device time of append + attention per step",
+            "scenarios": results}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,11 +556,17 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", action="store_true",
+                    help="step-latency timeline around a long prompt's arrival (one JSON line)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.timeline:
+        if rank == 0:
+            run_timeline(args, local)
         return
     run_ours(args, world, rank, local)
 

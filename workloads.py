@@ -198,6 +198,34 @@ CONFIGS = {
 
 # --------------------------------------------------------------------------- tensors
 
+@dataclasses.dataclass
+class Arrival:
+    """A multi-round scenario: running decodes, then one long prompt arrives.
+
+    decode_ctx     cached prompt lengths of the running decodes (admitted fully cached)
+    decode_new     tokens each decode generates (long enough to outlast the run)
+    prompt_len     the long prompt that arrives at round ``arrival_round``
+    """
+    name: str
+    H_q: int
+    H_kv: int
+    D: int
+    decode_ctx: List[int]
+    decode_new: int
+    prompt_len: int
+    prompt_new: int
+    arrival_round: int
+    tail_rounds: int
+
+
+def long_prompt_arrival(seed: int = 2, prompt_len: int = 16384) -> Arrival:
+    """7B-like MHA layer (H 32, D 128): 64 decodes with c ~ U[512, 4096] are streaming
+    when a 16384-token prompt arrives at round 16 (the moment a long prompt lands)."""
+    rng = np.random.default_rng(seed)
+    ctx = [int(c) for c in rng.integers(512, 4096, size=64, endpoint=True)]
+    return Arrival("mha7b_arrival16k", 32, 32, 128, ctx, 240, prompt_len, 8, 16, 16)
+
+
 def _torch():
     import torch  # local import: the oracle-only tests do not need torch at import time
     return torch
