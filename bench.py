@@ -449,8 +449,11 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------------------- step-latency timeline
 
+GRAPH_BUCKETS_512 = [16, 32, 64, 96, 128, 192, 256, 384, 512]
+
 TIMELINE_SCENARIOS = [
     ("decode-first, budget 512", dict(token_budget=512)),
+    ("decode-first, budget 512, CUDA graph per token bucket", dict(token_budget=512, graph=GRAPH_BUCKETS_512)),
     ("decode-first, budget 2048", dict(token_budget=2048)),
     ("no chunking (budget holds the whole prompt)", dict(token_budget=None)),
     ("prefill-first, budget 512", dict(token_budget=512, policy=1)),
@@ -489,15 +492,25 @@ def run_timeline(args, local):
     for label, kw in TIMELINE_SCENARIOS:
         kw = dict(kw)
         budget = kw.pop("token_budget") or big
+        buckets = kw.pop("graph", None)
         eng = ms.Engine(pages, budget, **kw)
         dec_ids = [eng.add_request(c, sc.decode_new, c) for c in sc.decode_ctx]
-        drv = RoundDriver(eng, k_cache, v_cache, cos, sin, sc.H_q, sc.H_kv, sc.D)
+        row_pages = -(-max(max(sc.decode_ctx) + sc.decode_new, sc.prompt_len + sc.prompt_new) // 16)
+        drv = RoundDriver(eng, k_cache, v_cache, cos, sin, sc.H_q, sc.H_kv, sc.D, graph_buckets=buckets,
+                          max_row_pages=row_pages)
+        sq, sk, sv = q, k, v
+        if drv.graph is not None:  # the step's inputs live in the graph's fixed buffers
+            B = buckets[-1]
+            drv.graph.q.copy_(q[:B])
+            drv.graph.k.copy_(k[:B])
+            drv.graph.v.copy_(v[:B])
+            sq, sk, sv = drv.graph.q, drv.graph.k, drv.graph.v
         recs, pid, prompt_done_round, prefilled = [], None, None, 0
         rnd = 0
         while True:
             if rnd == sc.arrival_round:
                 pid = eng.add_request(sc.prompt_len, sc.prompt_new)
-            rec = drv.step(q, k, v)
+            rec = drv.step(sq, sk, sv)
             d = np.diff(rec["cu_seqlens_q"])
             if pid is not None:
                 for rid, n in zip(rec["row_request_id"].tolist(), d.tolist()):
@@ -525,9 +538,13 @@ def run_timeline(args, local):
         steady = [r["device_ms"] for r in recs[4:a]]
         window = [r["device_ms"] for r in recs[a:prompt_done_round + 1]]
         ttft = float(t_end[prompt_done_round] - (t_end[a - 1] if a > 0 else 0.0))
+        executed = sum(r.get("bucket", r["prefill_tokens"] + r["decode_tokens"]) for r in recs)
+        scheduled = sum(r["prefill_tokens"] + r["decode_tokens"] for r in recs)
         results.append({
-            "scenario": label, "token_budget": budget,
+            "scenario": label, "token_budget": budget, "graph_buckets": buckets,
+            "pad_tokens": executed - scheduled, "pad_fraction": round((executed - scheduled) / executed, 4),
             "steady_step_ms": round(statistics.median(steady), 4),
+            "steady_wall_ms": round(statistics.median(r["wall_ms"] for r in recs[4:a]), 4),
             "prefill_steps": prompt_done_round - a + 1,
             "max_step_ms_during_prefill": round(max(window), 4),
             "median_step_ms_during_prefill": round(statistics.median(window), 4),

@@ -59,6 +59,19 @@ class EngineStats(ctypes.Structure):
                 ("max_request_pages", ctypes.c_int32), ("rounds", ctypes.c_int64)]
 
 
+class GraphConfig(ctypes.Structure):
+    _fields_ = [("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("max_rows", ctypes.c_int32), ("max_row_pages", ctypes.c_int32),
+                ("max_pos", ctypes.c_int32), ("scale", ctypes.c_float), ("num_buckets", ctypes.c_int32),
+                ("buckets", ctypes.POINTER(ctypes.c_int32))]
+
+
+class GraphBuffers(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "cos_tab", "sin_tab", "k_cache", "v_cache", "q_rot",
+                                                "out", "workspace")] + \
+               [("ws_bytes", ctypes.c_size_t), ("dev_status", ctypes.c_void_p)]
+
+
 _lib_handle = None
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _VP = ctypes.c_void_p
@@ -107,9 +120,18 @@ def lib() -> ctypes.CDLL:
             ("ms_engine_plan", [_VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _I32P, _I32P, _I32P, _I32P,
                                 _I32P, _I32P, _I32P, ctypes.POINTER(BatchInfo)]),
             ("ms_engine_commit", [_VP, _I32P, ctypes.c_int32, _I32P]),
-            ("ms_engine_stats", [_VP, ctypes.POINTER(EngineStats)])):
+            ("ms_engine_stats", [_VP, ctypes.POINTER(EngineStats)]),
+            ("ms_graph_create", [ctypes.POINTER(GraphConfig), ctypes.POINTER(GraphBuffers), _VP,
+                                 ctypes.POINTER(_VP)]),
+            ("ms_graph_destroy", [_VP]),
+            ("ms_graph_bucket", [_VP, ctypes.c_int32]),
+            ("ms_graph_run", [_VP, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P, ctypes.c_int32, ctypes.c_int32,
+                              ctypes.c_int32, _VP, _I32P]),
+            ("ms_graph_read_status", [_VP, _VP, _I32P])):
         getattr(h, name).restype = ctypes.c_int
         getattr(h, name).argtypes = args
+    h.ms_graph_workspace_size.restype = ctypes.c_size_t
+    h.ms_graph_workspace_size.argtypes = [ctypes.POINTER(GraphConfig)]
     _lib_handle = h
     return h
 
@@ -270,6 +292,77 @@ class Engine:
         n = ctypes.c_int32()
         _check(lib().ms_engine_commit(self._h, _i32(ids), cap, ctypes.byref(n)), "ms_engine_commit")
         return ids[: n.value].tolist()
+
+
+class StepGraph:
+    """One captured CUDA graph per token bucket of the whole step (ms_graph_*).
+
+    Owns fixed device buffers: ``q``, ``k``, ``v`` (write a step's new tokens
+    into their first rows), ``q_rot`` and ``out``, [largest bucket, heads, D].
+    ``stream`` must be a side stream (the legacy default stream cannot be
+    captured)."""
+
+    def __init__(self, k_cache, v_cache, cos, sin, H_q: int, max_rows: int, max_row_pages: int, buckets,
+                 stream, scale: float = None):
+        import torch
+        self._h = None
+        dev = k_cache.device
+        num_pages, H_kv, _, D = k_cache.shape
+        self.buckets = [int(b) for b in buckets]
+        B = self.buckets[-1]
+        self.stream = stream
+        self.q = torch.zeros((B, H_q, D), dtype=torch.bfloat16, device=dev)
+        self.k = torch.zeros((B, H_kv, D), dtype=torch.bfloat16, device=dev)
+        self.v = torch.zeros((B, H_kv, D), dtype=torch.bfloat16, device=dev)
+        self.q_rot = torch.zeros_like(self.q)
+        self.out = torch.zeros_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._bk = np.asarray(self.buckets, dtype=np.int32)
+        self._cfg = GraphConfig(H_q, H_kv, D, num_pages, int(max_rows), int(max_row_pages), int(cos.shape[0]),
+                                float(scale if scale is not None else float(D) ** -0.5), len(self.buckets),
+                                _i32(self._bk))
+        n = lib().ms_graph_workspace_size(ctypes.byref(self._cfg))
+        if n == 0:
+            raise MixedStepError(MS_ERR_ARG, "ms_graph_workspace_size")
+        self.workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+        self._keep = (k_cache, v_cache, cos, sin)
+        bufs = GraphBuffers(_ptr(self.q), _ptr(self.k), _ptr(self.v), _ptr(cos), _ptr(sin), _ptr(k_cache),
+                            _ptr(v_cache), _ptr(self.q_rot), _ptr(self.out), _ptr(self.workspace), n,
+                            _ptr(self.status))
+        h = _VP()
+        _check(lib().ms_graph_create(ctypes.byref(self._cfg), ctypes.byref(bufs), _stream(stream), ctypes.byref(h)),
+               "ms_graph_create")
+        self._h = h
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None and _lib_handle is not None:
+            _lib_handle.ms_graph_destroy(self._h)
+            self._h = None
+
+    def bucket(self, num_tokens: int) -> int:
+        b = lib().ms_graph_bucket(self._h, int(num_tokens))
+        _check(min(b, 0), "ms_graph_bucket")
+        return b
+
+    def run(self, meta: dict) -> int:
+        """Replay the step for host metadata ``meta`` (build_batch_metadata or Engine.plan);
+        returns the bucket it ran in."""
+        arrs = [np.ascontiguousarray(meta[k], dtype=np.int32).reshape(-1)
+                for k in ("cu_seqlens_q", "q_start_pos", "context_lens", "positions", "slot_mapping",
+                          "block_tables")]
+        arrs = [a if a.size else np.zeros(1, dtype=np.int32) for a in arrs]
+        used = ctypes.c_int32()
+        rc = lib().ms_graph_run(self._h, *[_i32(a) for a in arrs], int(meta["bt_stride"]), int(meta["num_rows"]),
+                                int(meta["num_tokens"]), _stream(self.stream), ctypes.byref(used))
+        _check(rc, "ms_graph_run")
+        return used.value
+
+    def read_status(self) -> int:
+        v = ctypes.c_int32()
+        rc = lib().ms_graph_read_status(self._h, _stream(self.stream), ctypes.byref(v))
+        if rc not in (MS_OK, MS_ERR_DEVICE):
+            _check(rc, "ms_graph_read_status")
+        return int(v.value)
 
 
 def rope_table(max_pos: int, D: int, base: float = 10000.0):

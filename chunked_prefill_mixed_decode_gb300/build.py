@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmixed_step.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["sched.cpp", "engine.cpp", "append_rope.cu", "attention.cu"]
+SOURCES = ["sched.cpp", "engine.cpp", "graph.cpp", "append_rope.cu", "attention.cu"]
 
 
 def _nvcc() -> str:

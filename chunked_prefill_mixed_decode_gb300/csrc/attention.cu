@@ -188,7 +188,8 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
     if (s < S && S <= kMaxRows) {
       const int32_t a = p.cu[s], b = p.cu[s + 1];
       const int32_t d = b - a, c = p.q_start[s], ctx = p.ctx_lens[s];
-      const bool ok = a >= 0 && b <= p.num_tokens && d >= 1 && c >= 0 && ctx == c + d &&
+      // d == 0 is a pad row: valid, and neither a decode nor a chunk
+      const bool ok = a >= 0 && b <= p.num_tokens && d >= 0 && c >= 0 && ctx == c + d &&
                       cdiv64(ctx, kPage) <= p.bt_stride;
       if (ok) {
         rd[i] = d;
@@ -1469,9 +1470,9 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
     return MS_ERR_ARG;
   const int G = H_q / H_kv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return MS_ERR_ARG;
-  if (num_rows == 0) return MS_OK;
+  if (num_rows == 0 || num_tokens == 0) return MS_OK;  // no tokens: every row is a pad row
   if (!q_rot || !k_cache || !v_cache || !cu_seqlens_q || !q_start_pos || !context_lens || !block_tables || !out ||
-      !workspace || num_pages < 1 || num_tokens < num_rows || bt_stride < 1)
+      !workspace || num_pages < 1 || bt_stride < 1)
     return MS_ERR_ARG;
   if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)

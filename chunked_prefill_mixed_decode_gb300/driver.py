@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import time
 
-from . import Engine, attention_workspace_size, kv_append_rope, mixed_step_attention, read_status
+from . import Engine, StepGraph, attention_workspace_size, kv_append_rope, mixed_step_attention, read_status
 from .step import to_device
 
 
@@ -22,12 +22,18 @@ class RoundDriver:
     row order, writes the attention output into ``out`` and returns the
     round's record.  Every step is synchronised, as a serving loop that reads
     its sampled tokens would be.
+
+    With ``graph_buckets`` (ascending token counts) every step replays a
+    captured CUDA graph of its bucket (StepGraph) instead of launching the
+    kernels one by one; ``max_row_pages`` then bounds every request's pages.
+    The record adds the bucket and the pad tokens.
     """
 
     def __init__(self, engine: Engine, k_cache, v_cache, cos, sin, H_q: int, H_kv: int, D: int,
-                 scale: float | None = None, stream=None):
+                 scale: float | None = None, stream=None, graph_buckets=None, max_row_pages: int = 0):
         import torch
         self.engine = engine
+        self.graph = None
         self.k_cache, self.v_cache = k_cache, v_cache
         self.cos, self.sin = cos, sin
         self.H_q, self.H_kv, self.D = H_q, H_kv, D
@@ -39,16 +45,24 @@ class RoundDriver:
         # upper bounds: a row holds at least one token (and a step at most 8192 rows);
         # the rows' contexts fit in the pool
         max_rows = min(max(budget, 1), 8192)
+        self.round = 0
+        self.ev0 = torch.cuda.Event(enable_timing=True)
+        self.ev1 = torch.cuda.Event(enable_timing=True)
+        if graph_buckets:
+            if stream is None:  # the legacy default stream cannot be captured
+                self.stream = torch.cuda.Stream(self.device)
+            self.graph = StepGraph(k_cache, v_cache, cos, sin, H_q, max_rows, max_row_pages, graph_buckets,
+                                   self.stream, scale)
+            self.q_rot, self.out = self.graph.q_rot, self.graph.out
+            return
         ws = attention_workspace_size(max_rows, max(budget, 1), num_pages * 16, H_q, H_kv, D)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=self.device)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.q_rot = torch.empty((max(budget, 1), H_q, D), dtype=torch.bfloat16, device=self.device)
         self.out = torch.empty_like(self.q_rot)
-        self.round = 0
-        self.ev0 = torch.cuda.Event(enable_timing=True)
-        self.ev1 = torch.cuda.Event(enable_timing=True)
 
     def step(self, q, k, v) -> dict:
+        import torch
         t0 = time.perf_counter()
         meta = self.engine.plan()
         T = meta["num_tokens"]
@@ -56,7 +70,23 @@ class RoundDriver:
                "prefill_tokens": T - meta["num_decodes"], "unused_tokens": meta["unused_tokens"],
                "deferred_decodes": meta["num_deferred"], "row_request_id": meta["row_request_id"],
                "cu_seqlens_q": meta["cu_seqlens_q"], "meta": meta}
-        if T > 0:
+        if T > 0 and self.graph is not None:
+            g = self.graph
+            t_plan = time.perf_counter()
+            self.stream.wait_stream(torch.cuda.current_stream(self.device))
+            with torch.cuda.stream(self.stream):
+                for src, dst in ((q, g.q), (k, g.k), (v, g.v)):
+                    if src.data_ptr() != dst.data_ptr():
+                        dst[:T].copy_(src[:T])
+            self.ev0.record(self.stream)
+            rec["bucket"] = g.run(meta)
+            rec["pad_tokens"] = rec["bucket"] - T
+            self.ev1.record(self.stream)
+            st = g.read_status()
+            if st:
+                raise RuntimeError(f"device status {st} in round {self.round}")
+            rec["device_ms"] = self.ev0.elapsed_time(self.ev1)
+        elif T > 0:
             batch = to_device(meta, self.device, non_blocking=True)
             t_plan = time.perf_counter()
             self.ev0.record(self.stream)

@@ -208,7 +208,10 @@ MS_API size_t ms_attention_workspace_size(int32_t max_rows, int32_t max_tokens, 
  * j % 16.  A chunk [c, c+d) sees the cached prefix [0, c) plus its own tokens
  * causally ([zwj] sections 02 and 07; [sar] section 05).  Rows with d == 1 run
  * the split-KV decode path; rows with d > 1 run the tensor-core chunk path; a
- * persistent queue orders the work longest-first.  bf16 in, fp32 accumulate,
+ * persistent queue orders the work longest-first.  A row with d == 0
+ * (cu_seqlens_q[s + 1] == cu_seqlens_q[s], context_lens[s] == q_start_pos[s])
+ * is a pad row and computes nothing; tokens no row covers are left unwritten
+ * (the padding of a fixed-shape step, [sar] section 05).  bf16 in, fp32 accumulate,
  * bf16 out.
  *   q_rot        device bf16 [num_tokens, H_q, D]
  *   k_cache, v_cache  device bf16 [num_pages, H_kv, 16, D], num_pages pages
@@ -335,6 +338,100 @@ MS_API int ms_engine_commit(ms_engine* e, int32_t* finished_ids, int32_t cap_fin
 
 /* ms_engine_stats -- counts of the pool and the live requests. */
 MS_API int ms_engine_stats(const ms_engine* e, ms_engine_counts* out);
+
+/* ---- CUDA-graph replay with padded token buckets (device) -----------------
+ * A CUDA graph records fixed shapes while chunked prefill changes the token
+ * count every step; the engine captures one graph per token bucket and pads
+ * each step up to the next bucket ([sar] section 05).  One graph records
+ * ms_kv_append_rope + ms_mixed_step_attention at the bucket's token count,
+ * max_rows rows, block-table stride max_row_pages and context bound
+ * num_pages * 16.  A replay pads the step: tokens past num_tokens get slot -1
+ * (no cache write) and position 0, rows past num_rows get d = 0 (pad rows).
+ * The pad tokens still pass through the append (their q_rot rows are junk);
+ * the attention output of real tokens equals the unpadded call's. */
+typedef struct ms_step_graph ms_step_graph;
+
+/* H_q, H_kv, D, num_pages  as for ms_mixed_step_attention
+ * max_rows       rows any replayed step may hold (<= 8192)
+ * max_row_pages  block-table stride of every replay (the longest row's pages)
+ * max_pos        rows of the cos/sin tables
+ * scale          softmax scale
+ * buckets        host, num_buckets ascending token counts, one graph each */
+typedef struct {
+  int32_t H_q, H_kv, D;
+  int32_t num_pages;
+  int32_t max_rows;
+  int32_t max_row_pages;
+  int32_t max_pos;
+  float scale;
+  int32_t num_buckets;
+  const int32_t* buckets;
+} ms_graph_config;
+
+/* Device buffers the graphs are recorded on (caller-owned, fixed for the
+ * graph's life).  q [B, H_q, D], k and v [B, H_kv, D], q_rot and out
+ * [B, H_q, D] (bf16, B = the largest bucket): the caller writes each step's
+ * new tokens into rows 0..num_tokens-1 of q, k, v before ms_graph_run.
+ * cos_tab/sin_tab fp32 [max_pos][D/2]; k_cache/v_cache the page pools;
+ * workspace 256-byte aligned, ws_bytes >= ms_graph_workspace_size (it holds
+ * the fixed metadata buffers and the attention workspace); dev_status device
+ * int32 or NULL (the append's status bits). */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* cos_tab;
+  const float* sin_tab;
+  void* k_cache;
+  void* v_cache;
+  void* q_rot;
+  void* out;
+  void* workspace;
+  size_t ws_bytes;
+  int32_t* dev_status;
+} ms_graph_buffers;
+
+/* ms_graph_workspace_size -- bytes of workspace for this config, 0 if the
+ * config is invalid. */
+MS_API size_t ms_graph_workspace_size(const ms_graph_config* cfg);
+
+/* ms_graph_create -- clear the workspace to an all-pad step, run each bucket's
+ * step once on `stream` (one-time kernel setup) and capture it into a graph.
+ * Call it outside any stream capture, on a stream other than the legacy
+ * default stream (NULL), which cannot be captured.  Unlike the other device
+ * calls it allocates: two pinned host staging buffers (cudaHostAlloc) and the
+ * instantiated graphs, all released by ms_graph_destroy.
+ * Errors: MS_ERR_ARG (bad config, NULL stream, workspace too small or
+ * misaligned), MS_ERR_CUDA. */
+MS_API int ms_graph_create(const ms_graph_config* cfg, const ms_graph_buffers* bufs, ms_stream_t stream,
+                           ms_step_graph** out);
+
+/* ms_graph_destroy -- waits for pending metadata copies, frees the graphs and
+ * the staging buffers (NULL is a no-op). */
+MS_API int ms_graph_destroy(ms_step_graph* g);
+
+/* ms_graph_bucket -- the bucket a step of num_tokens tokens runs in, or
+ * MS_ERR_ARG when it exceeds the largest bucket. */
+MS_API int ms_graph_bucket(const ms_step_graph* g, int32_t num_tokens);
+
+/* ms_graph_run -- one step: pad the host metadata (as ms_build_batch_metadata
+ * writes it) into the pinned staging buffer, copy it into the fixed device
+ * buffers on `stream` and launch the bucket's graph.  The host waits only for
+ * the copies of the replay before last (the staging buffers alternate).
+ * *bucket_used (may be NULL) gets the bucket.  Device errors land in the
+ * status words (ms_graph_read_status).
+ * Errors: MS_ERR_ARG (num_tokens above the largest bucket, num_rows >
+ * max_rows, bt_stride > max_row_pages, cu_seqlens_q inconsistent with
+ * num_tokens, null pointers), MS_ERR_CUDA. */
+MS_API int ms_graph_run(ms_step_graph* g, const int32_t* cu_seqlens_q, const int32_t* q_start_pos,
+                        const int32_t* context_lens, const int32_t* positions, const int32_t* slot_mapping,
+                        const int32_t* block_tables, int32_t bt_stride, int32_t num_rows, int32_t num_tokens,
+                        ms_stream_t stream, int32_t* bucket_used);
+
+/* ms_graph_read_status -- waits for `stream`, ORs and clears the append and
+ * attention status words of the graph's buffers into *host_status.  Returns
+ * MS_OK, MS_ERR_DEVICE when a bit was set, or MS_ERR_ARG / MS_ERR_CUDA. */
+MS_API int ms_graph_read_status(ms_step_graph* g, ms_stream_t stream, int32_t* host_status);
 
 /* ms_read_status -- waits for `stream`, copies the int32 device status word at
  * dev_status (for attention: the workspace pointer) to *host_status and

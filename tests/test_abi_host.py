@@ -258,3 +258,23 @@ def test_engine_argument_errors(ms):
         e.add_request(120, 20)  # 9 pages > 8
     assert err.value.code == ms.MS_ERR_NO_PAGES
     assert e.stats()["num_free_pages"] == 8
+
+
+def test_graph_config_errors(ms):
+    """Invalid graph configs are refused before any CUDA call."""
+    import ctypes
+    bk = np.array([16, 32], dtype=np.int32)
+    ok = ms.GraphConfig(4, 2, 64, 8, 4, 8, 128, 0.125, 2, bk.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+    assert ms.lib().ms_graph_workspace_size(ctypes.byref(ok)) > 0
+    for field, bad in (("D", 96), ("max_rows", 0), ("max_rows", 8193), ("num_buckets", 0), ("H_kv", 3)):
+        cfg = ms.GraphConfig.from_buffer_copy(ok)
+        setattr(cfg, field, bad)
+        assert ms.lib().ms_graph_workspace_size(ctypes.byref(cfg)) == 0, field
+    desc = np.array([32, 16], dtype=np.int32)
+    cfg = ms.GraphConfig.from_buffer_copy(ok)
+    cfg.buckets = desc.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    assert ms.lib().ms_graph_workspace_size(ctypes.byref(cfg)) == 0  # buckets must ascend
+    h = ctypes.c_void_p()
+    bufs = ms.GraphBuffers()
+    assert ms.lib().ms_graph_create(ctypes.byref(ok), ctypes.byref(bufs), None, ctypes.byref(h)) == ms.MS_ERR_ARG
+    assert ms.lib().ms_graph_destroy(None) == ms.MS_OK
