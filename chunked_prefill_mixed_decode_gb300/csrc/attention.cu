@@ -14,18 +14,24 @@
 //     ring in shared memory with bulk async copies; the G query heads of the
 //     KV head share every page read.  Lanes hold 8 (D = 128) or 4 (D = 64)
 //     columns of two token rows per 16-byte load; dot products finish with
-//     warp shuffles.  Each item leaves a partial (max, sum, accumulator);
-//     a combine kernel merges the splits.
-//   chunk rows (d > 1): tcgen05 tensor cores.  One CTA owns a 128-row query
+//     warp shuffles.  Each item leaves a partial (max, sum, accumulator); the
+//     last split of a (row, KV head) to finish merges them into the output.
+//   chunk rows (d > 1): tcgen05 tensor cores.  A CTA owns a 128-row query
 //     tile (128/G tokens x G heads of one KV head) and walks 128-key tiles of
 //     the prefix and its own chunk.  TMA loads Q and K/V pages (one 16-row box
-//     per page and 64-column slab, 128-byte swizzle), S = Q K^T lands in TMEM,
-//     four softmax warps own one row each, write P (bf16) to shared memory, and
-//     O += P V accumulates in TMEM, rescaled only when a row's max grows.
+//     per page and 64-column slab, 128-byte swizzle); S = Q K^T lands in TMEM;
+//     eight softmax warps (two per TMEM lane quadrant, each taking half of the
+//     128 key columns) write P (bf16) back into TMEM, and O += P V runs with P
+//     as the TMEM operand, accumulating in TMEM and rescaled only when a row's
+//     maximum grows by more than a factor 2^8.
 //
 // A one-CTA prologue validates the metadata, chooses the split size, orders
-// rows longest-first and lays out the work lists in the workspace; both paths
-// pull work from atomic counters with no inter-CTA waiting.
+// rows longest-first and decides how many CTAs start on chunk tiles; a second
+// small kernel expands the per-row item counts into flat item tables.  One
+// persistent kernel (a CTA per SM) then runs both queues: CTAs below the split
+// start on chunk tiles, the rest on decode items, and each moves to the other
+// queue when its own runs dry.  Work comes from atomic counters; no CTA waits
+// on another.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
