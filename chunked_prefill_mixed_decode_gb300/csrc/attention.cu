@@ -54,7 +54,7 @@ constexpr int kMinSplitPages = 16;
 constexpr int kMaxSplitPages = 256;
 constexpr int kDecWarps = 8;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kChunkThreads = 32 * (2 + kSoftmaxWarps);  // warp 0 TMA + queue, 1 MMA, 2-9 softmax
+constexpr int kChunkThreads = 32 * (4 + kSoftmaxWarps);  // warp 0 TMA + queue, 2-9 softmax, 1/10/11 MMA
 constexpr int kPrologueThreads = 1024;
 constexpr int kSortLimit = 2048;    // rows sorted longest-first up to this count
 constexpr int kMaxRows = 8192;      // rows of one step
@@ -270,11 +270,12 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
         sm.c[pos] = static_cast<int32_t>(c);
       } else {
         rows[pos] = s;
-        const int64_t items = kind == 0 ? cdiv64(cdiv64(c + 1, kPage), split) : cdiv64(d, tpt);
+        const int64_t n_qt = cdiv64(d, tpt);
+        const int64_t items = kind == 0 ? cdiv64(cdiv64(c + 1, kPage), split) : cdiv64(n_qt, 2);
         sm.pref[pos] = static_cast<int32_t>(items);
         if (kind == 1) {
           unsigned long long tiles = 0;
-          for (int64_t qt = 0; qt < items; ++qt) tiles += cdiv64(c + (d < (qt + 1) * tpt ? d : (qt + 1) * tpt), 128);
+          for (int64_t qt = 0; qt < n_qt; ++qt) tiles += cdiv64(c + (d < (qt + 1) * tpt ? d : (qt + 1) * tpt), 128);
           atomicAdd(&s_tiles, tiles * p.H_kv);
         }
       }
@@ -287,11 +288,12 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
         for (int m = 0; m < n; ++m) rank += sm.key[m] > k;
         rows[rank] = sm.id[j];
         const int64_t c = sm.c[j], d = sm.d[j];
-        const int64_t items = kind == 0 ? cdiv64(cdiv64(c + 1, kPage), split) : cdiv64(d, tpt);
+        const int64_t n_qt = cdiv64(d, tpt);
+        const int64_t items = kind == 0 ? cdiv64(cdiv64(c + 1, kPage), split) : cdiv64(n_qt, 2);
         sm.pref[rank] = static_cast<int32_t>(items);
         if (kind == 1) {
           unsigned long long tiles = 0;
-          for (int64_t qt = 0; qt < items; ++qt) tiles += cdiv64(c + (d < (qt + 1) * tpt ? d : (qt + 1) * tpt), 128);
+          for (int64_t qt = 0; qt < n_qt; ++qt) tiles += cdiv64(c + (d < (qt + 1) * tpt ? d : (qt + 1) * tpt), 128);
           atomicAdd(&s_tiles, tiles * p.H_kv);
         }
       }
@@ -805,44 +807,57 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
 // chunk rows: tcgen05 tensor cores, TMEM accumulators, TMA-staged pages
 // ----------------------------------------------------------------------------
 
-constexpr int kSlab = 128 * 128;  // bytes of one 128-row x 64-column bf16 slab (128-byte rows)
+constexpr int kQSlab = 128 * 128;  // one 128-row x 64-column bf16 slab of a Q tile (128-byte rows)
+constexpr int kKVSlab = 64 * 128;  // one 64-key x 64-column bf16 slab of a K or V tile
+constexpr int kKeys = 64;          // keys per KV tile
+constexpr int kTilePages = kKeys / kPage;
 
 template <int D>
 struct ChCfg {
-  static constexpr int NSL = D / 64;                 // 64-column slabs per row
-  static constexpr int Q_OFF = 0;
-  static constexpr int KVS = D == 128 ? 3 : 4;      // K/V pipeline stages
-  static constexpr int KV_OFF = NSL * kSlab;         // stage b: K at KV_OFF + b*2*NSL*kSlab, V after K
-  static constexpr int BAR_OFF = KV_OFF + 2 * KVS * NSL * kSlab;
-  static constexpr int X_OFF = BAR_OFF + 512;        // row-max / row-sum exchange, [2][2][128] fp32
-  static constexpr int SMEM = X_OFF + 2048;          // dynamic shared memory starts 1024-aligned
-  static constexpr int TMEM_COLS = 512;  // S0, S1 (128 each), O (D <= 128), P0, P1 (64 each: bf16 pairs)
-  static constexpr int P_COL = 384;
+  static constexpr int NSL = D / 64;                  // 64-column slabs per row
+  static constexpr int Q_BYTES = NSL * kQSlab;        // one 128-row Q tile
+  static constexpr int Q_OFF = 0;                     // Q tile t at Q_OFF + t * Q_BYTES
+  static constexpr int KVS = D == 128 ? 4 : 6;        // K/V pipeline stages
+  static constexpr int KV_OFF = 2 * Q_BYTES;          // stage b: K at KV_OFF + b*2*NSL*kKVSlab, V after K
+  static constexpr int BAR_OFF = KV_OFF + 2 * KVS * NSL * kKVSlab;
+  static constexpr int SMEM = BAR_OFF + 1024;         // dynamic shared memory starts 1024-aligned
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int O_COL = 128;                   // O of Q tile t at column t * O_COL
+  static constexpr int S_COL = 256;                   // S/P buffer b of Q tile t at S_COL + (2t + b) * 64
 };
 
+// A work item is a pair of consecutive 128-row Q tiles of one chunk row and KV
+// head; both read every K/V tile the pair needs from the same shared stages.
 struct ChItem {
-  int row, tb, d, c, tok0, ntok, hk, kv_end, n_kt, tile0;  // tile0: CTA-global index of its first KV tile
+  int row, tb, c, hk;
+  int n_kt;     // KV tiles the pair needs (those of its later tile)
+  int kv0;      // CTA-global index of the item's first KV tile (stage and parity)
+  int tok0[2], ntok[2], kv_end[2], nkt[2];  // per Q tile; ntok[1] == 0: no second tile
+  int t0[2];    // per Q tile: index of its first KV tile among all tiles its softmax group ran
 };
 
 struct ChBars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4];  // K stage: free once the tile's S MMA is done
-  uint64_t v_full[4], v_empty[4];  // V stage: free once the tile's PV MMA is done
-  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t k_full[8], k_empty[8];  // K stage: free once both S issuers' MMAs are done
+  uint64_t v_full[8], v_empty[8];  // V stage: free once the PV issuer's MMAs are done
+  uint64_t s_full[2][2], p_full[2][2], o_done[2][2];  // [Q tile][S/P buffer]
   uint64_t item_full[2], item_empty[2];
-  uint64_t mma_done;
+  uint64_t mma_done[3];
   uint32_t tmem;
   int abort;
   ChItem items[2];
 };
 
-static_assert(sizeof(ChBars) <= 512, "chunk-kernel barrier block exceeds its reserved space");
-static_assert(ChCfg<128>::SMEM <= 232448, "chunk kernel exceeds the per-CTA shared-memory limit");
+static_assert(sizeof(ChBars) <= 1024, "chunk-phase barrier block exceeds its reserved space");
+static_assert(ChCfg<128>::SMEM <= 232448 && ChCfg<64>::SMEM <= 232448,
+              "chunk phase exceeds the per-CTA shared-memory limit");
+static_assert(ChCfg<128>::KVS <= 8 && ChCfg<64>::KVS <= 8, "more K/V stages than barriers");
 
-// K-major, 128-byte-swizzled operand: slab-major 64-column blocks of 128-byte rows;
-// k-step kk (16 columns) lives in slab kk / 4 at byte offset (kk % 4) * 32.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
-  return smem_desc_sw128(base + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+// K-major, 128-byte-swizzled operand: slab-major 64-column blocks of 128-byte
+// rows, slab_bytes apart; k-step kk (16 columns) lives in slab kk / 4 at byte
+// offset (kk % 4) * 32.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, int slab_bytes) {
+  return smem_desc_sw128(base + (kk >> 2) * slab_bytes + (kk & 3) * 32, 16, 1024);
 }
 
 // wait by lane 0, result and ordering shared with the whole warp
@@ -854,55 +869,62 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return ok != 0;
 }
 
-// Chunk phase: warp 0 (one thread) owns the work queue and streams Q, K and V
-// (K one tile ahead of V); warp 1 (one thread) issues the MMAs; warps 2-9 run
-// the softmax: the two warps that share a TMEM lane quadrant own the same 32
-// query rows and split the 128 key columns, exchanging row maxima through
-// shared memory.  Returns when the chunk queue is empty; the caller owns TMEM
-// and the barrier invalidation.
+// Chunk phase.  Warp 0 owns the work queue and streams Q and K/V with TMA (K
+// one tile ahead of V); warps 2-5 and 6-9 are two softmax groups, group t
+// owning Q tile t of the current pair, one query row per thread over 64-key
+// tiles.  One thread issues a tcgen05.mma only about every 110-140 cycles,
+// whatever its N, well below the tensor rate at these shapes, so three
+// warps issue: warp 1 the S MMAs of group 0, warp 10 those of group 1, and
+// warp 11 the PV MMAs of both.  Each group has two S buffers in
+// TMEM, so its next S is computed while it exponentiates the current one, and
+// P (bf16) overwrites the S values it came from, where the PV MMA reads it.
+// The two groups run a tile apart at most, so one group's exponentials
+// overlap the other group's MMAs.  Returns when the chunk queue is empty; the
+// caller owns TMEM and the barrier invalidation.
 template <int D, int G>
 __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtensorMap* tm_k_p,
                                             const CUtensorMap* tm_v_p, const AttnParams& p, uint8_t* smem,
                                             uint32_t tmem) {
   using C = ChCfg<D>;
   constexpr int NSL = C::NSL;
-  constexpr int TPT = 128 / G;  // query tokens per 128-row tile
+  constexpr int TPT = 128 / G;  // query tokens per 128-row Q tile
+  constexpr int KVS = C::KVS;
   const CUtensorMap& tm_q = *tm_q_p;
   const CUtensorMap& tm_k = *tm_k_p;
   const CUtensorMap& tm_v = *tm_v_p;
   ChBars* bars = reinterpret_cast<ChBars*>(smem + C::BAR_OFF);
-  float* xbuf = reinterpret_cast<float*>(smem + C::X_OFF);  // [parity][half][128 rows]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.hdr[H_NCH_ITEMS];
 
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + C::Q_OFF;
-  constexpr int KVS = C::KVS;
-  auto k_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kSlab; };
-  auto v_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kSlab + NSL * kSlab; };
+  auto k_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kKVSlab; };
+  auto v_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kKVSlab + NSL * kKVSlab; };
+  auto s_col = [&](int t, int b) { return tmem + C::S_COL + (2 * t + b) * 64; };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
-    for (int b = 0; b < 4; ++b) {  // all four (KVS of them in use) so that all can be invalidated
+    mbar_init(&bars->q_empty, 2);  // one commit per S issuer
+    for (int b = 0; b < 8; ++b) {  // all of them, so that all can be invalidated
       mbar_init(&bars->k_full[b], 1);
-      mbar_init(&bars->k_empty[b], 1);
+      mbar_init(&bars->k_empty[b], 2);
       mbar_init(&bars->v_full[b], 1);
       mbar_init(&bars->v_empty[b], 1);
     }
+    for (int t = 0; t < 2; ++t)
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bars->s_full[t][b], 1);
+        mbar_init(&bars->p_full[t][b], 128);  // the four warps of group t
+        mbar_init(&bars->o_done[t][b], 1);
+      }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 32 * kSoftmaxWarps);
-      mbar_init(&bars->o_done[b], 1);
       mbar_init(&bars->item_full[b], 1);
-      mbar_init(&bars->item_empty[b], 1 + 32 * kSoftmaxWarps);  // MMA thread, softmax threads
+      mbar_init(&bars->item_empty[b], 3 + 32 * kSoftmaxWarps);  // MMA issuers, softmax threads
     }
-    mbar_init(&bars->mma_done, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars->mma_done[i], 1);
     bars->abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  const uint32_t tS0 = tmem, tO = tmem + 256, tP0 = tmem + C::P_COL;  // P buffer b at tP0 + 64 b
   volatile int* abort_flag = &bars->abort;
 
   if (warp == 0) {
@@ -917,9 +939,11 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
       prefetch_tmap(&tm_v);
     }
     const int my_pg = lane / NSL, my_s = lane % NSL;
-    int g = 0;       // CTA-global KV tile counter
-    int n_done = 0;  // items taken by this CTA
-    int g_v = 0;     // tiles whose V has been issued
+    const bool loader = lane < kTilePages * NSL;
+    int g = 0;               // CTA-global KV tile counter
+    int g_v = 0;             // tiles whose V has been issued
+    int n_done = 0;          // items taken by this CTA
+    int t_run[2] = {0, 0};   // KV tiles run by each softmax group so far
     bool ok = true;
     auto lane0_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
       int r = 1;
@@ -927,14 +951,14 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
       r = __shfl_sync(0xffffffffu, r, 0);
       return r != 0;
     };
-    // V of tile gv (one tile behind K): its stage was last read by the PV MMA of gv - KVS
+    // V of tile gv (one tile behind K): its stage was last read by the PV MMAs of gv - KVS
     auto load_v = [&](int gv, int row0, int npg) -> bool {
       const int bv = gv % KVS;
       if (gv >= KVS && !lane0_wait(&bars->v_empty[bv], ((gv / KVS) - 1) & 1)) return false;
       if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[bv], npg * kPage * D * 2);
       __syncwarp();
-      if (my_pg < npg && lane < 8 * NSL)
-        tma_load_2d(smem + v_off(bv) + my_s * kSlab + my_pg * 2048, &tm_v, my_s * 64, row0, &bars->v_full[bv]);
+      if (loader && my_pg < npg)
+        tma_load_2d(smem + v_off(bv) + my_s * kKVSlab + my_pg * 2048, &tm_v, my_s * 64, row0, &bars->v_full[bv]);
       return true;
     };
     while (ok) {
@@ -953,16 +977,25 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
         const int k = kl.x, local = kl.y;
         it.row = __ldg(p.ch_rows + k);
         it.tb = __ldg(p.cu + it.row);
-        it.d = __ldg(p.cu + it.row + 1) - it.tb;
+        const int d = __ldg(p.cu + it.row + 1) - it.tb;
         it.c = __ldg(p.q_start + it.row);
-        const int n_qt = (it.d + TPT - 1) / TPT;
-        const int qt = n_qt - 1 - local / p.H_kv;  // later tiles see more keys: run them first
+        const int n_qt = (d + TPT - 1) / TPT;
+        const int n_pair = (n_qt + 1) >> 1;
+        const int pair = n_pair - 1 - local / p.H_kv;  // later tiles see more keys: run them first
         it.hk = local % p.H_kv;
-        it.tok0 = qt * TPT;
-        it.ntok = min(TPT, it.d - it.tok0);
-        it.kv_end = it.c + it.tok0 + it.ntok;
-        it.n_kt = (it.kv_end + 127) / 128;
-        it.tile0 = g;
+        it.n_kt = 0;
+        for (int t = 0; t < 2; ++t) {
+          const int qt = 2 * pair + t;
+          const bool has = qt < n_qt;
+          it.tok0[t] = has ? qt * TPT : 0;
+          it.ntok[t] = has ? min(TPT, d - qt * TPT) : 0;
+          it.kv_end[t] = has ? it.c + it.tok0[t] + it.ntok[t] : 0;
+          it.nkt[t] = (it.kv_end[t] + kKeys - 1) / kKeys;
+          it.t0[t] = t_run[t];
+          t_run[t] += it.nkt[t];
+          it.n_kt = max(it.n_kt, it.nkt[t]);
+        }
+        it.kv0 = g;
       }
       if (lane == 0) {
         bars->items[slot] = it;
@@ -970,41 +1003,46 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
       }
       ++n_done;
       if (it.row < 0) break;
-      // Q tile: the previous item's S MMAs must be done with it
+      // Q tiles: the previous item's S MMAs must be done with them
       if (n_done >= 2 && !lane0_wait(&bars->q_empty, (n_done - 2) & 1)) {
         ok = false;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, 128 * D * 2);
+      const int nq = it.ntok[1] > 0 ? 2 : 1;
+      if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, nq * 128 * D * 2);
       __syncwarp();
-      if (lane < NSL)
-        tma_load_3d(smem + C::Q_OFF + lane * kSlab, &tm_q, lane * 64, it.hk * G, it.tb + it.tok0, &bars->q_full);
+      if (lane < nq * NSL) {
+        const int t = lane / NSL, s = lane % NSL;
+        tma_load_3d(smem + C::Q_OFF + t * C::Q_BYTES + s * kQSlab, &tm_q, s * 64, it.hk * G, it.tb + it.tok0[t],
+                    &bars->q_full);
+      }
+      const int kv_max = max(it.kv_end[0], it.kv_end[1]);
       const int32_t* btrow = p.bt + static_cast<int64_t>(it.row) * p.bt_stride;
-      const int n_pages = (it.kv_end + kPage - 1) / kPage;
-      // lane L < 8 holds the page id of page L of the current tile; the next tile's is in flight
-      int pg_cur = lane < 8 && lane < n_pages ? __ldg(btrow + lane) : 0;
+      const int n_pages = (kv_max + kPage - 1) / kPage;
+      // lane L < 4 holds the page id of page L of the current tile; the next tile's is in flight
+      int pg_cur = lane < kTilePages && lane < n_pages ? __ldg(btrow + lane) : 0;
       int row0_prev = 0, npg_prev = 0;
       for (int kt = 0; kt < it.n_kt; ++kt, ++g) {
-        const int lp = (kt + 1) * 8 + lane;
-        const int pg_nxt = lane < 8 && lp < n_pages ? __ldg(btrow + lp) : 0;
+        const int lp = (kt + 1) * kTilePages + lane;
+        const int pg_nxt = lane < kTilePages && lp < n_pages ? __ldg(btrow + lp) : 0;
         const int b = g % KVS;
-        const int keys = min(128, it.kv_end - kt * 128);
+        const int keys = min(kKeys, kv_max - kt * kKeys);
         const int npg = (keys + kPage - 1) / kPage;
-        int phys = __shfl_sync(0xffffffffu, pg_cur, my_pg & 7);
-        if (my_pg < npg && lane < 8 * NSL && (phys < 0 || phys >= p.num_pages)) {
+        int phys = __shfl_sync(0xffffffffu, pg_cur, my_pg & (kTilePages - 1));
+        if (loader && my_pg < npg && (phys < 0 || phys >= p.num_pages)) {
           atomicOr(p.hdr + H_STATUS, MS_STATUS_BAD_PAGE);
           phys = 0;
         }
         const int row0 = (phys * p.H_kv + it.hk) * kPage;
-        // K of tile g: its stage was last read by the S MMA of tile g - KVS
+        // K of tile g: its stage was last read by the S MMAs of tile g - KVS
         if (g >= KVS && !lane0_wait(&bars->k_empty[b], ((g / KVS) - 1) & 1)) {
           ok = false;
           break;
         }
         if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[b], npg * kPage * D * 2);
         __syncwarp();
-        if (my_pg < npg && lane < 8 * NSL)
-          tma_load_2d(smem + k_off(b) + my_s * kSlab + my_pg * 2048, &tm_k, my_s * 64, row0, &bars->k_full[b]);
+        if (loader && my_pg < npg)
+          tma_load_2d(smem + k_off(b) + my_s * kKVSlab + my_pg * 2048, &tm_k, my_s * 64, row0, &bars->k_full[b]);
         if (kt >= 1) {
           if (!load_v(g - 1, row0_prev, npg_prev)) {
             ok = false;
@@ -1031,8 +1069,65 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
       for (int t = (g_v > KVS ? g_v - KVS : 0); t < g_v; ++t)
         mbar_wait(&bars->v_full[t % KVS], (t / KVS) & 1, nullptr, 200000000ull);
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer (one thread)
+  } else if (warp == 1 || warp == 2 + kSoftmaxWarps) {
+    // ---------------------------------------------------------------- S issuer of one group
+    // Every S issuer walks every KV tile of the item and commits to the K
+    // stage's "empty" barrier (two commits per phase), issuing MMAs only for
+    // the tiles its Q tile needs.  It waits for each stage to be full even
+    // when it has no MMA for it: that keeps its commits in step with the
+    // producer, so a phase can never complete on commits meant for a later one.
+    const int t = warp == 1 ? 0 : 1;
+    if (lane == 0) {
+      const uint32_t sq = sbase + C::Q_OFF + t * C::Q_BYTES;
+      bool ok = true;
+      for (int n = 0; ok; ++n) {
+        const int slot = n & 1;
+        if (!mbar_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const ChItem it = bars->items[slot];
+        if (it.row < 0) break;
+        if (it.nkt[t] > 0 && !mbar_wait(&bars->q_full, n & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int kv_max = max(it.kv_end[0], it.kv_end[1]);
+        for (int kt = 0; kt < it.n_kt; ++kt) {
+          const int g = it.kv0 + kt, bk = g % KVS;
+          if (!mbar_wait(&bars->k_full[bk], (g / KVS) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (kt < it.nkt[t]) {
+            const int gt = it.t0[t] + kt, b = gt & 1;
+            // S buffer b last held P of the group's tile gt - 2: its PV MMA must be done
+            if (gt >= 2 && !mbar_wait(&bars->o_done[t][b], ((gt - 2) >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int keys = min(kKeys, kv_max - kt * kKeys);
+            const uint32_t idesc_s = idesc_bf16_f32(128, (keys + 15) & ~15, 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_bf16_ss(s_col(t, b), kmajor_desc(sq, kk, kQSlab), kmajor_desc(sbase + k_off(bk), kk, kKVSlab),
+                          idesc_s, kk > 0 ? 1u : 0u);
+            mma_commit(&bars->s_full[t][b]);
+          }
+          mma_commit(&bars->k_empty[bk]);
+          if (kt == it.n_kt - 1) mma_commit(&bars->q_empty);
+        }
+        if (!ok) break;
+        mbar_arrive(&bars->item_empty[slot]);
+      }
+      if (!ok) *abort_flag = 1;
+      // every MMA this thread issued must finish before TMEM is reused or released
+      mma_commit(&bars->mma_done[t]);
+      mbar_wait(&bars->mma_done[t], 0, nullptr, 200000000ull);
+    }
+  } else if (warp == 3 + kSoftmaxWarps) {
+    // ---------------------------------------------------------------- PV issuer of both groups
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
       bool ok = true;
@@ -1044,82 +1139,66 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
         }
         const ChItem it = bars->items[slot];
         if (it.row < 0) break;
-        if (!mbar_wait(&bars->q_full, n & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        for (int kt = 0; kt <= it.n_kt; ++kt) {
-          if (kt < it.n_kt) {
-            const int g = it.tile0 + kt, b = g & 1, bk = g % KVS;
-            if (!mbar_wait(&bars->k_full[bk], (g / KVS) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const int keys = min(128, it.kv_end - kt * 128);
-            const int n_cols = (keys + 15) & ~15;
-            const uint32_t idesc_s = idesc_bf16_f32(128, n_cols, 0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_bf16_ss(tS0 + b * 128, kmajor_desc(sQ, kk), kmajor_desc(sbase + k_off(bk), kk), idesc_s,
-                          kk > 0 ? 1u : 0u);
-            mma_commit(&bars->s_full[b]);
-            mma_commit(&bars->k_empty[bk]);
-            if (kt == it.n_kt - 1) mma_commit(&bars->q_empty);
+        const int kv_max = max(it.kv_end[0], it.kv_end[1]);
+        for (int j = 0; j < it.n_kt && ok; ++j) {
+          const int gj = it.kv0 + j, bv = gj % KVS;
+          if (!mbar_wait(&bars->v_full[bv], (gj / KVS) & 1, abort_flag)) {
+            ok = false;
+            break;
           }
-          if (kt >= 1) {
-            const int j = kt - 1, gj = it.tile0 + j, bj = gj & 1, bv = gj % KVS;
-            if (!mbar_wait(&bars->v_full[bv], (gj / KVS) & 1, abort_flag) ||
-                !mbar_wait(&bars->p_full[bj], (gj >> 1) & 1, abort_flag)) {
+          const int keys = min(kKeys, kv_max - j * kKeys);  // keys loaded in this tile
+          const int nk = (keys + 15) >> 4;
+          if (keys != nk * 16) {
+            // rows past the context in the last page may hold stale (even non-finite)
+            // data: zero them in V so that P = 0 times V stays 0
+            uint8_t* v0 = smem + v_off(bv);
+            for (int r = keys; r < nk * 16; ++r)
+              for (int s = 0; s < NSL; ++s)
+                for (int q16 = 0; q16 < 8; ++q16)
+                  *reinterpret_cast<uint4*>(v0 + s * kKVSlab + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+          }
+          const uint32_t vbase = sbase + v_off(bv);
+          for (int t = 0; t < 2; ++t) {
+            if (j >= it.nkt[t]) continue;
+            const int gt = it.t0[t] + j, b = gt & 1;
+            if (!mbar_wait(&bars->p_full[t][b], (gt >> 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const int keys = min(128, it.kv_end - j * 128);
-            const int nk = (keys + 15) >> 4;
-            if (keys != nk * 16) {
-              // rows past the context in the last page may hold stale (even non-finite)
-              // data: zero them in V so that P = 0 times V stays 0
-              uint8_t* v0 = smem + v_off(bv);
-              for (int r = keys; r < nk * 16; ++r)
-                for (int s = 0; s < NSL; ++s)
-                  for (int q16 = 0; q16 < 8; ++q16)
-                    *reinterpret_cast<uint4*>(v0 + s * kSlab + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
-              fence_proxy_async_smem();
-            }
-            const uint32_t vbase = sbase + v_off(bv);
-            for (int kk = 0; kk < nk; ++kk) {
+            const int nk_t = (min(kKeys, it.kv_end[t] - j * kKeys) + 15) >> 4;  // key steps this Q tile sees
+            for (int kk = 0; kk < nk_t; ++kk) {
               // P (A operand) from TMEM: 16 keys = 8 packed columns per k-step.  V is the
               // MN-major B operand: 64-column slabs one slab apart (LBO), 8-key row groups
               // 1024 B apart (SBO), 16 keys = 2048 B per k-step
-              const uint64_t vdesc = smem_desc_sw128(vbase + kk * 2048, kSlab, 1024);
-              mma_bf16_ts(tO, tP0 + bj * 64 + kk * 8, vdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+              const uint64_t vdesc = smem_desc_sw128(vbase + kk * 2048, kKVSlab, 1024);
+              mma_bf16_ts(tmem + t * C::O_COL, s_col(t, b) + kk * 8, vdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(&bars->o_done[bj]);
-            mma_commit(&bars->v_empty[bv]);
+            mma_commit(&bars->o_done[t][b]);
           }
+          if (!ok) break;
+          mma_commit(&bars->v_empty[bv]);
         }
         if (!ok) break;
         mbar_arrive(&bars->item_empty[slot]);
       }
       if (!ok) *abort_flag = 1;
-      // every MMA this thread issued must finish before TMEM is reused or released
-      mma_commit(&bars->mma_done);
-      mbar_wait(&bars->mma_done, 0, nullptr, 200000000ull);
+      mma_commit(&bars->mma_done[2]);
+      mbar_wait(&bars->mma_done[2], 0, nullptr, 200000000ull);
     }
-  } else if (warp < 2 + kSoftmaxWarps) {
+  } else if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
     // ---------------------------------------------------------------- softmax
+    const int t = (warp - 2) >> 2;              // Q tile of this group
     const int quad = warp & 3;                  // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;           // key columns [64 * half, 64 * half + 64)
     const int r = quad * 32 + lane;             // query row of this thread
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t pair_bar = 1 + quad;         // named barrier of the two warps of this quadrant
+    const uint32_t tO = tmem + t * C::O_COL + lane_off;
     const float sl2 = p.scale_log2;
     // A row exponentiates against m_use, the largest scaled score seen when it
     // was last raised; it is raised (and O rescaled) only when a tile's max
     // exceeds it by more than 2^8, so P <= 256 and O, l stay exact in fp32.
     constexpr float kRescaleLog2 = 8.f;
-    constexpr int OC = D / 2;                   // O columns this warp owns
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int slot = n & 1;
@@ -1129,131 +1208,122 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
       }
       const ChItem it = bars->items[slot];
       if (it.row < 0) break;
-      const int tl = it.tok0 + r / G;  // token of this row within the chunk
-      const bool valid = (r / G) < it.ntok;
-      const int pos = it.c + (valid ? tl : it.tok0 + it.ntok - 1);
-      const int warp_min_pos = it.c + it.tok0 + (quad * 32) / G;  // smallest position of this warp's rows
-      float m_use = -INFINITY, l = 0.f;
-      for (int kt = 0; kt < it.n_kt; ++kt) {
-        const int g = it.tile0 + kt, b = g & 1;
-        if (!warp_wait(&bars->s_full[b], (g >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t r0[32], r1[32];
-        const uint32_t ts = tS0 + b * 128 + half * 64 + lane_off;
-        tmem_ld32(ts, r0);
-        tmem_ld32(ts + 32, r1);
-        tmem_wait_ld();
-        reg_fence32(r0);
-        reg_fence32(r1);
-        float sv[64];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          sv[j] = __uint_as_float(r0[j]);
-          sv[32 + j] = __uint_as_float(r1[j]);
-        }
-        const int key0 = kt * 128 + half * 64;
-        if (kt * 128 + 127 > warp_min_pos) {  // diagonal or ragged tile: causal mask (pair-uniform)
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (key0 + j > pos) sv[j] = -INFINITY;
-        }
-        float mxa[4] = {sv[0], sv[1], sv[2], sv[3]};
-#pragma unroll
-        for (int j = 4; j < 64; ++j) mxa[j & 3] = fmaxf(mxa[j & 3], sv[j]);
-        const float pm = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
-        xbuf[(g & 1) * 256 + half * 128 + r] = pm;
-        named_bar_sync(pair_bar, 64);
-        const float mx = fmaxf(pm, xbuf[(g & 1) * 256 + (half ^ 1) * 128 + r]);
-        const float mx_s = mx * sl2;
-        const bool grow = mx_s > m_use + kRescaleLog2;
-        const float m_new = grow ? mx_s : m_use;
-        const float alpha = grow ? ex2(m_use - m_new) : 1.f;
-        const float neg_m = -m_new;
-        float rsa[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float e = ex2(fmaf(sv[j], sl2, neg_m));
-          sv[j] = e;
-          rsa[j & 3] += e;
-        }
-        l = l * alpha + ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3]));
-        m_use = m_new;
-        if (kt > 0 && __any_sync(0xffffffffu, grow)) {  // rescale this warp's O columns
-          // the PV MMA of the previous tile must be done with O first
-          if (!warp_wait(&bars->o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag)) {
+      const int nkt = it.nkt[t];
+      if (nkt > 0) {
+        const int tl = it.tok0[t] + r / G;  // token of this row within the chunk
+        const bool valid = (r / G) < it.ntok[t];
+        const int pos = it.c + (valid ? tl : it.tok0[t] + it.ntok[t] - 1);
+        const int warp_min_pos = it.c + it.tok0[t] + (quad * 32) / G;  // smallest position of this warp's rows
+        float m_use = -INFINITY, l = 0.f;
+        for (int kt = 0; kt < nkt; ++kt) {
+          const int gt = it.t0[t] + kt, b = gt & 1;
+          if (!warp_wait(&bars->s_full[t][b], (gt >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          uint32_t r0[32], r1[32];
+          const uint32_t ts = s_col(t, b) + lane_off;
+          tmem_ld32(ts, r0);
+          tmem_ld32(ts + 32, r1);
+          tmem_wait_ld();
+          reg_fence32(r0);
+          reg_fence32(r1);
+          float sv[64];
 #pragma unroll
-          for (int cc = 0; cc < OC / 32; ++cc) {
-            uint32_t rr[32];
-            tmem_ld32(tO + lane_off + half * OC + cc * 32, rr);
-            tmem_wait_ld();
-            reg_fence32(rr);
-            float o[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(rr[j]) * alpha;
-            tmem_st32(tO + lane_off + half * OC + cc * 32, o);
+          for (int j = 0; j < 32; ++j) {
+            sv[j] = __uint_as_float(r0[j]);
+            sv[32 + j] = __uint_as_float(r1[j]);
           }
+          const int key0 = kt * kKeys;
+          if (key0 + kKeys - 1 > warp_min_pos) {  // diagonal or ragged tile: causal mask (warp-uniform test)
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if (key0 + j > pos) sv[j] = -INFINITY;
+          }
+          float mxa[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+          for (int j = 4; j < 64; ++j) mxa[j & 3] = fmaxf(mxa[j & 3], sv[j]);
+          const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+          const float mx_s = mx * sl2;
+          const bool grow = mx_s > m_use + kRescaleLog2;
+          const float m_new = grow ? mx_s : m_use;
+          const float alpha = grow ? ex2(m_use - m_new) : 1.f;
+          const float neg_m = -m_new;
+          float rsa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const float e = ex2(fmaf(sv[j], sl2, neg_m));
+            sv[j] = e;
+            rsa[j & 3] += e;
+          }
+          l = l * alpha + ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3]));
+          m_use = m_new;
+          if (kt > 0 && __any_sync(0xffffffffu, grow)) {  // rescale this row's O
+            // the PV MMA of the previous tile must be done with O first
+            if (!warp_wait(&bars->o_done[t][(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t rr[32];
+              tmem_ld32(tO + cc * 32, rr);
+              tmem_wait_ld();
+              reg_fence32(rr);
+              float o[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(rr[j]) * alpha;
+              tmem_st32(tO + cc * 32, o);
+            }
+            tmem_wait_st();
+          }
+          // P (bf16 pairs) over the first 32 columns of the S values it came from
+          uint32_t pw[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * j], sv[2 * j + 1]);
+            pw[j] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          tmem_st32u(ts, pw);
           tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full[t][b]);
         }
-        // P buffer b was last read by the PV MMA of tile g - 2
-        if (g >= 2 && !warp_wait(&bars->o_done[b], ((g - 2) >> 1) & 1, abort_flag)) {
+        if (!ok) break;
+        const int gl = it.t0[t] + nkt - 1;
+        if (!warp_wait(&bars->o_done[t][gl & 1], (gl >> 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
-        uint32_t pw[32];
+        tc_fence_after();
+        const float inv = 1.f / l;
+        bf16* dst = p.out + (static_cast<int64_t>(it.tb + tl) * p.H_q + it.hk * G + r % G) * D;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * j], sv[2 * j + 1]);
-          pw[j] = *reinterpret_cast<uint32_t*>(&h2);
-        }
-        tmem_st32u(tP0 + b * 64 + half * 32 + lane_off, pw);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[b]);
-      }
-      if (!ok) break;
-      // row sum: the two halves of the row add their partial sums
-      const int gl = it.tile0 + it.n_kt - 1;
-      xbuf[((gl + 1) & 1) * 256 + half * 128 + r] = l;
-      named_bar_sync(pair_bar, 64);
-      const float l_row = l + xbuf[((gl + 1) & 1) * 256 + (half ^ 1) * 128 + r];
-      named_bar_sync(pair_bar, 64);  // both halves have read before the slots are reused
-      if (!warp_wait(&bars->o_done[gl & 1], (gl >> 1) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const float inv = 1.f / l_row;
-      bf16* dst = p.out + (static_cast<int64_t>(it.tb + tl) * p.H_q + it.hk * G + r % G) * D + half * OC;
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(tO + cc * 32, rr);
+          tmem_wait_ld();
+          reg_fence32(rr);
+          if (valid) {
 #pragma unroll
-      for (int cc = 0; cc < OC / 32; ++cc) {
-        uint32_t rr[32];
-        tmem_ld32(tO + lane_off + half * OC + cc * 32, rr);
-        tmem_wait_ld();
-        reg_fence32(rr);
-        if (valid) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 u;
-            __nv_bfloat162 h0 =
-                __floats2bfloat162_rn(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv);
-            __nv_bfloat162 h1 =
-                __floats2bfloat162_rn(__uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
-            __nv_bfloat162 h2 =
-                __floats2bfloat162_rn(__uint_as_float(rr[j + 4]) * inv, __uint_as_float(rr[j + 5]) * inv);
-            __nv_bfloat162 h3 =
-                __floats2bfloat162_rn(__uint_as_float(rr[j + 6]) * inv, __uint_as_float(rr[j + 7]) * inv);
-            u.x = *reinterpret_cast<uint32_t*>(&h0);
-            u.y = *reinterpret_cast<uint32_t*>(&h1);
-            u.z = *reinterpret_cast<uint32_t*>(&h2);
-            u.w = *reinterpret_cast<uint32_t*>(&h3);
-            *reinterpret_cast<uint4*>(dst + cc * 32 + j) = u;
+            for (int j = 0; j < 32; j += 8) {
+              uint4 u;
+              __nv_bfloat162 h0 =
+                  __floats2bfloat162_rn(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv);
+              __nv_bfloat162 h1 =
+                  __floats2bfloat162_rn(__uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
+              __nv_bfloat162 h2 =
+                  __floats2bfloat162_rn(__uint_as_float(rr[j + 4]) * inv, __uint_as_float(rr[j + 5]) * inv);
+              __nv_bfloat162 h3 =
+                  __floats2bfloat162_rn(__uint_as_float(rr[j + 6]) * inv, __uint_as_float(rr[j + 7]) * inv);
+              u.x = *reinterpret_cast<uint32_t*>(&h0);
+              u.y = *reinterpret_cast<uint32_t*>(&h1);
+              u.z = *reinterpret_cast<uint32_t*>(&h2);
+              u.w = *reinterpret_cast<uint32_t*>(&h3);
+              *reinterpret_cast<uint4*>(dst + cc * 32 + j) = u;
+            }
           }
         }
       }
@@ -1276,7 +1346,7 @@ __device__ __forceinline__ void invalidate_phase_barriers(uint8_t* smem, bool ch
     if (threadIdx.x == 0) {
       ChBars* bars = reinterpret_cast<ChBars*>(smem + ChCfg<D>::BAR_OFF);
       uint64_t* b0 = &bars->q_full;
-      uint64_t* b1 = &bars->mma_done;
+      uint64_t* b1 = &bars->mma_done[2];
       for (uint64_t* b = b0; b <= b1; ++b) mbar_inval(b);
     }
   } else if ((threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < kDecWarps) {
