@@ -52,7 +52,6 @@ using namespace ms;
 constexpr int kPage = 16;
 constexpr int kMinSplitPages = 16;
 constexpr int kMaxSplitPages = 256;
-constexpr int kDecWarps = 8;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kChunkThreads = 32 * (4 + kSoftmaxWarps);  // warp 0 TMA + queue, 2-9 softmax, 1/10/11 MMA
 constexpr int kPrologueThreads = 1024;
@@ -106,7 +105,8 @@ struct AttnParams {
   int64_t context_total;
   int32_t bt_stride, num_rows, num_tokens, num_pages;
   int32_t H_q, H_kv, D, G;
-  int32_t dec_workers;
+  int32_t dec_workers;  // decode worker warps in the grid
+  int32_t num_sms;
   float scale_log2;
 };
 
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
   // 7. starting split of the SMs between chunk tiles and decode pages: warp 0
   // evaluates every split in fp32 (fp64 is slow on this part) and keeps the best
   if (tid < 32) {
-    const int sms = p.dec_workers / kDecWarps;
+    const int sms = p.num_sms;
     const float t_tiles = static_cast<float>(s_tiles) * kChunkTileNs;  // SM-ns of chunk work
     const float dec_bytes = static_cast<float>(s_dec_pages) * p.H_kv * kPage * p.D * 4.f;
     const float sm_gbs = kDecodeSmGBs / (1.f + 0.18f * (p.G - 1));
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kItemThreads) items_kernel(AttnParams p) {
 template <int D, int G>
 struct DecCfg {
   static constexpr int EPL = D / 16;               // columns per lane of one token row
-  static constexpr int NST = D == 128 ? (G >= 8 ? 2 : 3) : (G >= 8 ? 5 : 6);
+  static constexpr int NST = D == 128 ? 2 : 4;            // ring stages per warp
   static constexpr int PAGE_BYTES = kPage * D * 2;  // one page of one KV head
   static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
   static constexpr int Q_BYTES = G * D * 2;
@@ -418,7 +418,9 @@ struct DecCfg {
   static constexpr int P_OFF = Q_OFF + 2 * Q_BYTES;
   static constexpr int BAR_OFF = P_OFF + G * 16 * 4;
   static constexpr int WARP_BYTES = (BAR_OFF + NST * 8 + 127) / 128 * 128;
-  static constexpr int SMEM = kDecWarps * WARP_BYTES;
+  // as many worker warps as the CTA has, while their rings fit in shared memory
+  static constexpr int WARPS = 12 * WARP_BYTES <= 230000 ? 12 : 10;
+  static constexpr int SMEM = WARPS * WARP_BYTES;
 };
 
 
@@ -540,7 +542,7 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
   using C = DecCfg<D, G>;
   constexpr int EPL = C::EPL, NST = C::NST;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp >= kDecWarps) return;  // the CTA's remaining warps have no decode slice
+  if (warp >= DecCfg<D, G>::WARPS) return;  // the CTA's remaining warps have no decode slice
   uint8_t* wbase = dsmem + warp * C::WARP_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(wbase + C::BAR_OFF);
   float* pbuf = reinterpret_cast<float*>(wbase + C::P_OFF);  // [G][2 halves][8]
@@ -849,6 +851,8 @@ struct ChBars {
 };
 
 static_assert(sizeof(ChBars) <= 1024, "chunk-phase barrier block exceeds its reserved space");
+static_assert(DecCfg<128, 8>::SMEM <= 232448 && DecCfg<64, 8>::SMEM <= 232448 && DecCfg<128, 4>::WARPS == 12,
+              "decode rings exceed the per-CTA shared-memory limit");
 static_assert(ChCfg<128>::SMEM <= 232448 && ChCfg<64>::SMEM <= 232448,
               "chunk phase exceeds the per-CTA shared-memory limit");
 static_assert(ChCfg<128>::KVS <= 8 && ChCfg<64>::KVS <= 8, "more K/V stages than barriers");
@@ -1349,7 +1353,7 @@ __device__ __forceinline__ void invalidate_phase_barriers(uint8_t* smem, bool ch
       uint64_t* b1 = &bars->mma_done[2];
       for (uint64_t* b = b0; b <= b1; ++b) mbar_inval(b);
     }
-  } else if ((threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < kDecWarps) {
+  } else if ((threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < DecCfg<D, G>::WARPS) {
     using C = DecCfg<D, G>;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (threadIdx.x >> 5) * C::WARP_BYTES + C::BAR_OFF);
     for (int i = 0; i < C::NST; ++i) mbar_inval(full + i);
@@ -1501,6 +1505,20 @@ int num_sms() {
   return n;
 }
 
+// decode worker warps per CTA for head dim D and group size G
+int dec_warps(int D, int G) {
+  switch (D * 100 + G) {
+    case 6401: return DecCfg<64, 1>::WARPS;
+    case 6402: return DecCfg<64, 2>::WARPS;
+    case 6404: return DecCfg<64, 4>::WARPS;
+    case 6408: return DecCfg<64, 8>::WARPS;
+    case 12801: return DecCfg<128, 1>::WARPS;
+    case 12802: return DecCfg<128, 2>::WARPS;
+    case 12804: return DecCfg<128, 4>::WARPS;
+    default: return DecCfg<128, 8>::WARPS;
+  }
+}
+
 template <int D, int G>
 int launch_paths(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  int n_ctas, cudaStream_t st) {
@@ -1608,7 +1626,8 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
   p.H_kv = H_kv;
   p.D = D;
   p.G = G;
-  p.dec_workers = sms * kDecWarps;
+  p.dec_workers = sms * dec_warps(D, G);
+  p.num_sms = sms;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   if (num_rows > kMaxRows) return MS_ERR_ARG;
