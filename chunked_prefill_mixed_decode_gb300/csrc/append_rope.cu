@@ -67,6 +67,9 @@ __device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const fl
 }
 
 __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendArgs a) {
+  // the attention call that follows may start its launch now; it waits for
+  // this kernel before it reads q_rot or the pages
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int half = a.D >> 1;
   const int per_row = half / kVec;                 // threads per (token, head) row
   const int heads = a.H_q + 2 * a.H_kv;

@@ -166,11 +166,31 @@ __device__ __forceinline__ int find_in_prefix(const int32_t* pref, int n, int it
   return lo;
 }
 
+// Work items of one row: decode splits of `split` pages, or pairs of 128-row Q tiles.
+__device__ __forceinline__ int row_items(int kind, int c, int d, int tpt, unsigned split) {
+  if (kind == 0) return static_cast<int>((static_cast<unsigned>(c + kPage) / kPage + split - 1) / split);
+  const int n_qt = (d + tpt - 1) / tpt;
+  return (n_qt + 1) >> 1;
+}
+
+// 128x128 tiles of a chunk row's Q tiles against their causal key ranges (the
+// cost model's unit of chunk work)
+__device__ __forceinline__ unsigned chunk_tiles(int c, int d, int tpt) {
+  unsigned tiles = 0;
+  for (int end = tpt; end - tpt < d; end += tpt) tiles += static_cast<unsigned>(c + min(d, end) + 127) >> 7;
+  return tiles;
+}
+
 // One CTA: validate the rows, split them into decode rows (d = 1) and chunk
 // rows (d > 1), order each list longest-first, size the decode splits, lay
 // out the per-item tables, zero the split counters and pick how many CTAs of
 // the main kernel start on chunk work.  Every row's values are read from
 // global memory once; the rest happens in registers and shared memory.
+//
+// Launched as a programmatic dependent of the kernel before it on the stream
+// (normally the append), it reads only the row metadata, which is complete
+// before that kernel starts, and runs alongside it; before it exits it waits
+// for that kernel, so the kernels after it see the append's writes.
 __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParams p) {
   extern __shared__ __align__(16) uint8_t psm_raw[];
   PrologueSmem& sm = *reinterpret_cast<PrologueSmem*>(psm_raw);
@@ -181,6 +201,7 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
   const int tid = threadIdx.x;
   const int S = p.num_rows;
   int32_t* hdr = p.hdr;
+  griddep_launch_dependents();
   if (tid == 0) s_tiles = 0;
   // 1. this thread's rows s = tid + i * 1024: load, validate, count (block sums, no atomics)
   int rd[R], rc[R];
@@ -227,12 +248,14 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
       p.dec_item_prefix[0] = 0;
       p.ch_item_prefix[0] = 0;
     }
+    griddep_wait();
     return;
   }
   // 2. decode split size: about 16 items per decode worker warp, clamped
   int64_t split = cdiv64(static_cast<int64_t>(s_dec_pages) * p.H_kv, static_cast<int64_t>(p.dec_workers) * 16);
   split = split < kMinSplitPages ? kMinSplitPages : (split > kMaxSplitPages ? kMaxSplitPages : split);
   const int tpt = 128 / p.G;
+  const unsigned split32 = static_cast<unsigned>(split);
   // 3. the two row lists, each in input order first
   int dpos[R], cpos[R];
   int64_t n_dec = 0, n_ch = 0;
@@ -261,23 +284,17 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
       const int s = tid + i * kPrologueThreads;
       const int pos = kind == 0 ? dpos[i] : cpos[i];
       if (s >= S || pos < 0) continue;
-      const int64_t c = rc[i], d = rd[i];
+      const int c = rc[i], d = rd[i];
       if (sorted) {
-        const int64_t cost = kind == 0 ? c + 1 : d * (2 * c + d + 1) / 2;
+        const int64_t cost = kind == 0 ? c + 1 : static_cast<int64_t>(d) * (2ll * c + d + 1) / 2;
         sm.key[pos] = (cost << 16) | (0xffff - (pos & 0xffff));  // ties keep input order
         sm.id[pos] = s;
         sm.d[pos] = static_cast<int32_t>(d);
         sm.c[pos] = static_cast<int32_t>(c);
       } else {
         rows[pos] = s;
-        const int64_t n_qt = cdiv64(d, tpt);
-        const int64_t items = kind == 0 ? cdiv64(cdiv64(c + 1, kPage), split) : cdiv64(n_qt, 2);
-        sm.pref[pos] = static_cast<int32_t>(items);
-        if (kind == 1) {
-          unsigned long long tiles = 0;
-          for (int64_t qt = 0; qt < n_qt; ++qt) tiles += cdiv64(c + (d < (qt + 1) * tpt ? d : (qt + 1) * tpt), 128);
-          atomicAdd(&s_tiles, tiles * p.H_kv);
-        }
+        sm.pref[pos] = row_items(kind, c, d, tpt, split32);
+        if (kind == 1) atomicAdd(&s_tiles, static_cast<unsigned long long>(chunk_tiles(c, d, tpt)) * p.H_kv);
       }
     }
     __syncthreads();
@@ -287,15 +304,9 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
         int rank = 0;
         for (int m = 0; m < n; ++m) rank += sm.key[m] > k;
         rows[rank] = sm.id[j];
-        const int64_t c = sm.c[j], d = sm.d[j];
-        const int64_t n_qt = cdiv64(d, tpt);
-        const int64_t items = kind == 0 ? cdiv64(cdiv64(c + 1, kPage), split) : cdiv64(n_qt, 2);
-        sm.pref[rank] = static_cast<int32_t>(items);
-        if (kind == 1) {
-          unsigned long long tiles = 0;
-          for (int64_t qt = 0; qt < n_qt; ++qt) tiles += cdiv64(c + (d < (qt + 1) * tpt ? d : (qt + 1) * tpt), 128);
-          atomicAdd(&s_tiles, tiles * p.H_kv);
-        }
+        const int c = sm.c[j], d = sm.d[j];
+        sm.pref[rank] = row_items(kind, c, d, tpt, split32);
+        if (kind == 1) atomicAdd(&s_tiles, static_cast<unsigned long long>(chunk_tiles(c, d, tpt)) * p.H_kv);
       }
       __syncthreads();
     }
@@ -344,36 +355,28 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
     hdr[H_CH_CTR] = 0;
     hdr[H_SPLIT] = static_cast<int32_t>(split);
   }
-  // 7. starting split of the SMs between chunk tiles and decode pages: warp 0
-  // evaluates every split in fp32 (fp64 is slow on this part) and keeps the best
-  if (tid < 32) {
-    const int sms = p.num_sms;
-    const float t_tiles = static_cast<float>(s_tiles) * kChunkTileNs;  // SM-ns of chunk work
-    const float dec_bytes = static_cast<float>(s_dec_pages) * p.H_kv * kPage * p.D * 4.f;
-    const float sm_gbs = kDecodeSmGBs / (1.f + 0.18f * (p.G - 1));
-    float best_t = 3.0e38f;
-    int best_n = sms;
-    for (int n = tid; n <= sms; n += 32) {
-      const float tc = s_tiles == 0 ? 0.f : (n == 0 ? 3.0e38f : t_tiles / n);
-      const float bw = fminf((sms - n) * sm_gbs, kHbmGBs);
-      const float td = dec_bytes == 0.f ? 0.f : (n == sms ? 3.0e38f : dec_bytes / bw);
-      const float t = fmaxf(tc, td);
-      if (t <= best_t * 1.0001f) {  // ties: more chunk CTAs while decode stays HBM-bound
-        best_t = fminf(t, best_t);
-        best_n = n;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
-      const int on = __shfl_xor_sync(0xffffffffu, best_n, o);
-      if (ot < best_t * 0.9999f || (ot <= best_t * 1.0001f && on > best_n)) {
-        best_t = ot;
-        best_n = on;
-      }
-    }
-    if (tid == 0) hdr[H_CHUNK_CTAS] = best_n;
+  // 7. starting split of the SMs between chunk tiles and decode pages.  Chunk
+  // time falls as 1/n with n chunk CTAs; decode time is bytes over the
+  // bandwidth of the other SMs, capped by HBM.  Take the balance point, or,
+  // while decode stays HBM-bound, as many chunk CTAs as keep it so.
+  if (tid == 0) {
+    const float S = static_cast<float>(p.num_sms);
+    const float T = static_cast<float>(s_tiles) * kChunkTileNs;                     // SM-ns of chunk work
+    const float B = static_cast<float>(s_dec_pages) * p.H_kv * kPage * p.D * 4.f;  // decode bytes
+    const float g = kDecodeSmGBs / (1.f + 0.18f * (p.G - 1));                      // GB/s per decode SM
+    const float n_hbm = fmaxf(0.f, floorf(S - kHbmGBs / g));  // most chunk CTAs with decode at HBM rate
+    float n;
+    if (T == 0.f)
+      n = B == 0.f ? S : n_hbm;
+    else if (B == 0.f)
+      n = S;
+    else if (T * kHbmGBs <= B * n_hbm)  // chunk done within the HBM-bound decode time
+      n = n_hbm;
+    else
+      n = fminf(S - 1.f, fmaxf(1.f, rintf(__fdividef(T * g * S, B + T * g))));
+    hdr[H_CHUNK_CTAS] = static_cast<int>(n);
   }
+  griddep_wait();
 }
 
 // Item tables: item i of a list -> (row index in queue order, item within the
@@ -383,6 +386,8 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
 constexpr int kItemThreads = 512;
 __global__ void __launch_bounds__(kItemThreads) items_kernel(AttnParams p) {
   __shared__ int32_t pref[kMaxRows + 1];
+  griddep_launch_dependents();
+  griddep_wait();  // the prologue's lists and prefixes
   for (int kind = 0; kind < 2; ++kind) {
     const int n = kind == 0 ? p.hdr[H_NDEC] : p.hdr[H_NCH];
     const int n_items = kind == 0 ? p.hdr[H_NDEC_ITEMS] : p.hdr[H_NCH_ITEMS];
@@ -1371,13 +1376,13 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   // 128-byte-swizzled TMA tiles and MMA descriptors require
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
-  const int n_ch_items = p.hdr[H_NCH_ITEMS];
-  const int n_dec_items = p.hdr[H_NDEC_ITEMS];
-  if (n_ch_items == 0 && n_dec_items == 0) return;
   if ((smem_u32(smem) & 1023u) != 0) {
+    griddep_wait();
     if (threadIdx.x == 0) atomicOr(p.hdr + H_STATUS, MS_STATUS_INTERNAL);
     return;
   }
+  // set-up that needs nothing from the kernels before: it overlaps their tail
+  // when this kernel is launched as a programmatic dependent
   uint32_t* tmem_slot = &reinterpret_cast<ChBars*>(smem + ChCfg<D>::BAR_OFF)->tmem;
   if (warp == 1) {
     tmem_alloc(tmem_slot, ChCfg<D>::TMEM_COLS);
@@ -1387,7 +1392,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // the item tables (and, through the prologue, the append's q_rot and pages)
+  const int n_ch_items = p.hdr[H_NCH_ITEMS];
+  const int n_dec_items = p.hdr[H_NDEC_ITEMS];
   __syncthreads();  // every thread holds the address before the phases reuse the memory
+  if (n_ch_items == 0 && n_dec_items == 0) {
+    if (warp == 1) tmem_dealloc(tmem, ChCfg<D>::TMEM_COLS);
+    return;
+  }
   const bool chunk_first = static_cast<int>(blockIdx.x) < p.hdr[H_CHUNK_CTAS];
   for (int ph = 0; ph < 2; ++ph) {
     const bool chunk = (ph == 0) == chunk_first;
@@ -1505,6 +1517,25 @@ int num_sms() {
   return n;
 }
 
+// Launch as a programmatic dependent of the previous kernel on the stream: the
+// kernel may start while that one finishes and orders itself with
+// griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // decode worker warps per CTA for head dim D and group size G
 int dec_warps(int D, int G) {
   switch (D * 100 + G) {
@@ -1531,7 +1562,9 @@ int launch_paths(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& 
       return MS_ERR_CUDA;
     configured = true;
   }
-  attention_kernel<D, G><<<n_ctas, kChunkThreads, smem, st>>>(tq, tk, tv, p);
+  if (launch_dependent(attention_kernel<D, G>, dim3(n_ctas), dim3(kChunkThreads), smem, st, tq, tk, tv, p) !=
+      cudaSuccess)
+    return MS_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MS_OK : MS_ERR_CUDA;
 }
 
@@ -1639,8 +1672,10 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
       return MS_ERR_CUDA;
     prologue_configured = true;
   }
-  prologue_kernel<<<1, kPrologueThreads, sizeof(PrologueSmem), st>>>(p);
-  items_kernel<<<sms < 64 ? sms : 64, kItemThreads, 0, st>>>(p);
+  if (launch_dependent(prologue_kernel, dim3(1), dim3(kPrologueThreads), sizeof(PrologueSmem), st, p) !=
+          cudaSuccess ||
+      launch_dependent(items_kernel, dim3(sms < 64 ? sms : 64), dim3(kItemThreads), 0, st, p) != cudaSuccess)
+    return MS_ERR_CUDA;
   const int n_ctas = sms;  // one persistent CTA per SM
   int rc = MS_ERR_ARG;
   switch (D * 100 + G) {
