@@ -321,7 +321,9 @@ def run_ours(args, world, rank, local):
 
 def run_e2e(args, ms, step, subs, cos, sin, k_cache, v_cache, ws, status, device, stream, dist):
     """Same metric through the public API from host buffers: per batch, the C++ scheduler
-    builds the metadata, which goes H2D with q/k/v from pinned memory; the output comes back."""
+    builds the metadata, which goes H2D (one packed copy) with q/k/v from pinned memory; the
+    output comes back D2H.  Uploads and downloads run on their own streams, ordered with events,
+    so they overlap the compute of neighbouring batches; every step ends with a full sync."""
     import torch
     host = []
     for s in subs:
@@ -329,23 +331,40 @@ def run_e2e(args, ms, step, subs, cos, sin, k_cache, v_cache, ws, status, device
                          out=torch.empty_like(s["out"], device="cpu").pin_memory()))
     n = max(1, min(args.steps, args.e2e_steps))
     h2d = d2h = 0
+    # uploads, compute and downloads on three streams: batch i + 1 uploads while batch i computes
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    stagers = [step.MetaStager(s["meta"]["num_rows"], s["meta"]["num_tokens"],
+                               s["meta"]["num_rows"] * s["meta"]["bt_stride"], device) for s in subs]
+    done = [None] * len(subs)  # compute of the batch's previous step (its device buffers are free after it)
 
     def e2e_step():
         nonlocal h2d, d2h
         h2d = d2h = 0
-        for s, hb in zip(subs, host):
+        for i, (s, hb) in enumerate(zip(subs, host)):
             wl = s["wl"]
             meta = ms.build_batch_metadata(s["states"], s["tables"], wl.token_budget, wl.max_chunk)
-            b = step.to_device(meta, device, non_blocking=True)
-            q = hb["q"].to(device, non_blocking=True)
-            k = hb["k"].to(device, non_blocking=True)
-            v = hb["v"].to(device, non_blocking=True)
+            if done[i] is not None:
+                up.wait_event(done[i])
+            b = stagers[i].stage(meta, up)
+            q, k, v = s["q"], s["k"], s["v"]
+            with torch.cuda.stream(up):
+                q.copy_(hb["q"], non_blocking=True)
+                k.copy_(hb["k"], non_blocking=True)
+                v.copy_(hb["v"], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(up)
+            stream.wait_event(ready)
             q_rot = s["q_rot"]
             ms.kv_append_rope(q, k, v, b.positions, b.slot_mapping, cos, sin, k_cache, v_cache, q_rot=q_rot,
                               dev_status=status, stream=stream)
             ms.mixed_step_attention(q_rot, k_cache, v_cache, b.cu_seqlens_q, b.q_start_pos, b.context_lens,
                                     b.block_tables, b.context_total, s["out"], ws, stream=stream)
-            hb["out"].copy_(s["out"], non_blocking=True)
+            fin = torch.cuda.Event()
+            fin.record(stream)
+            done[i] = fin
+            down.wait_event(fin)
+            with torch.cuda.stream(down):
+                hb["out"].copy_(s["out"], non_blocking=True)
             h2d += b.h2d_bytes + (q.numel() + k.numel() + v.numel()) * 2
             d2h += s["out"].numel() * 2
         torch.cuda.synchronize()

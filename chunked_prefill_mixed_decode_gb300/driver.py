@@ -11,7 +11,7 @@ from __future__ import annotations
 import time
 
 from . import Engine, StepGraph, attention_workspace_size, kv_append_rope, mixed_step_attention, read_status
-from .step import to_device
+from .step import MetaStager
 
 
 class RoundDriver:
@@ -55,6 +55,7 @@ class RoundDriver:
                                    self.stream, scale)
             self.q_rot, self.out = self.graph.q_rot, self.graph.out
             return
+        self.stager = MetaStager(max_rows, max(budget, 1), 64 * max_rows, self.device)  # grows on demand
         ws = attention_workspace_size(max_rows, max(budget, 1), num_pages * 16, H_q, H_kv, D)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=self.device)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
@@ -87,7 +88,7 @@ class RoundDriver:
                 raise RuntimeError(f"device status {st} in round {self.round}")
             rec["device_ms"] = self.ev0.elapsed_time(self.ev1)
         elif T > 0:
-            batch = to_device(meta, self.device, non_blocking=True)
+            batch = self.stager.stage(meta, self.stream)
             t_plan = time.perf_counter()
             self.ev0.record(self.stream)
             kv_append_rope(q[:T], k[:T], v[:T], batch.positions, batch.slot_mapping, self.cos, self.sin,

@@ -56,6 +56,67 @@ def to_device(meta: dict, device, non_blocking: bool = False) -> DeviceBatch:
                        int(np.asarray(meta["context_lens"], dtype=np.int64).sum()), meta)
 
 
+class MetaStager:
+    """Reusable pinned staging for one step's metadata: the six arrays are packed
+    into one pinned host buffer and reach the device in a single copy.
+
+    Two host/device buffer pairs alternate; a host buffer is refilled only after
+    the copy that last read it has finished (an event per buffer).  Device
+    buffers are reused in stream order, so the kernels of a step finish reading
+    one before a later copy on the same stream overwrites it.
+    """
+
+    def __init__(self, max_rows: int, max_tokens: int, max_bt: int, device):
+        self.device = device
+        self.cap = 0
+        self.events = [None, None]
+        self.flip = 0
+        self._grow(3 * max_rows + 1 + 2 * max_tokens + max_bt + 6 * 4)  # plus alignment slack
+
+    def _grow(self, cap: int):
+        import torch
+        for ev in self.events:
+            if ev is not None:
+                ev.synchronize()
+        torch.cuda.synchronize(self.device)  # earlier steps may still read the old device buffers
+        self.cap = cap
+        self.host = [torch.empty(cap, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.dev = [torch.empty(cap, dtype=torch.int32, device=self.device) for _ in range(2)]
+        self.events = [None, None]
+
+    def stage(self, meta: dict, stream=None) -> DeviceBatch:
+        import torch
+        S, T, stride = int(meta["num_rows"]), int(meta["num_tokens"]), int(meta["bt_stride"])
+        need = 3 * S + 1 + 2 * T + S * stride + 6 * 4
+        if need > self.cap:
+            self._grow(max(need, 2 * self.cap))
+        i = self.flip
+        self.flip ^= 1
+        if self.events[i] is not None:
+            self.events[i].synchronize()
+        hv = self.host[i].numpy()
+        views, off = {}, 0
+        for k, n in (("cu_seqlens_q", S + 1), ("q_start_pos", S), ("context_lens", S), ("positions", T),
+                     ("slot_mapping", T), ("block_tables", S * stride)):
+            n_alloc = max(n, 1)
+            if off + n_alloc > self.cap:
+                raise ValueError("metadata larger than the stager's capacity")
+            hv[off:off + n] = np.asarray(meta[k], dtype=np.int32).reshape(-1)[:n]
+            views[k] = (off, n_alloc)
+            off += (n_alloc + 3) & ~3  # keep each array 16-byte aligned
+        st = stream if stream is not None else torch.cuda.current_stream(self.dev[i].device)
+        with torch.cuda.stream(st):
+            self.dev[i][:off].copy_(self.host[i][:off], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(st)
+        self.events[i] = ev
+        d = {k: self.dev[i][o:o + n] for k, (o, n) in views.items()}
+        bt = d["block_tables"].view(S, stride) if S > 0 and stride > 0 else d["block_tables"][:1].view(1, 1)
+        return DeviceBatch(d["cu_seqlens_q"], d["q_start_pos"], d["context_lens"], d["positions"],
+                           d["slot_mapping"], bt, S, T, int(meta["num_decodes"]),
+                           int(np.asarray(meta["context_lens"], dtype=np.int64).sum()), meta)
+
+
 def schedule(states, block_tables, token_budget, max_chunk=0) -> dict:
     return build_batch_metadata(states, block_tables, token_budget, max_chunk)
 
