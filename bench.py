@@ -216,12 +216,14 @@ def run_ours(args, world, rank, local):
     k_cache, v_cache = pool
 
     def one_step(events=None):
+        # a batch's events bracket its append and attention call, with nothing between
+        # the two: the attention call's kernels launch as programmatic dependents of the append
         for j, s in enumerate(subs):
             b = s["batch"]
-            ms.kv_append_rope(s["q"], s["k"], s["v"], b.positions, b.slot_mapping, cos, sin, k_cache, v_cache,
-                              q_rot=s["q_rot"], dev_status=status, stream=stream)
             if events is not None:
                 events[j][0].record(stream)
+            ms.kv_append_rope(s["q"], s["k"], s["v"], b.positions, b.slot_mapping, cos, sin, k_cache, v_cache,
+                              q_rot=s["q_rot"], dev_status=status, stream=stream)
             ms.mixed_step_attention(s["q_rot"], k_cache, v_cache, b.cu_seqlens_q, b.q_start_pos, b.context_lens,
                                     b.block_tables, b.context_total, s["out"], ws, stream=stream)
             if events is not None:
@@ -262,33 +264,35 @@ def run_ours(args, world, rank, local):
     value = total_tokens / (max_ms / 1e3)
     ms_per_step = max_ms / args.steps
 
-    # ---- roofline of the attention call (the dominant launch group) and of the whole step
-    attn_bytes = sum(s["counts"]["attn_bytes"] for s in subs)
+    # ---- roofline of one batch of the path (append + attention call: the dominant, and only,
+    # launch group; 4 launches) and of the whole step
+    grp_bytes = sum(s["counts"]["step_bytes"] for s in subs)
     attn_flops = sum(s["counts"]["flops"] for s in subs)
-    attn_avg_ms = sum(statistics.mean(a) for a in attn_ms) / n_sub  # mean over batches of the mean duration
-    attn_bytes_avg = attn_bytes / n_sub
-    attn_flops_avg = attn_flops / n_sub
-    t_mem = attn_bytes_avg / (peaks["hbm_gbs"] * 1e9)
-    t_flop = attn_flops_avg / (peaks["bf16_tflops_sustained"] * 1e12)
+    grp_avg_ms = sum(statistics.mean(a) for a in attn_ms) / n_sub  # mean over batches of the mean duration
+    grp_bytes_avg = grp_bytes / n_sub
+    flops_avg = attn_flops / n_sub
+    t_mem = grp_bytes_avg / (peaks["hbm_gbs"] * 1e9)
+    t_flop = flops_avg / (peaks["bf16_tflops_sustained"] * 1e12)
     if t_mem >= t_flop:
-        achieved = attn_bytes_avg / (attn_avg_ms / 1e3) / 1e9
+        achieved = grp_bytes_avg / (grp_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None}
     else:
-        achieved = attn_flops_avg / (attn_avg_ms / 1e3) / 1e12
+        achieved = flops_avg / (grp_avg_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4), "traffic": None}
     cap = captured_traffic(args.config)
-    if cap is not None and roof["bound"] == "hbm":
-        # scale the captured launch's DRAM bytes to the average launch by algorithmic bytes
+    if cap is not None and roof["bound"] == "hbm" and "append_dram_bytes" in cap:
+        # scale the captured batch's DRAM bytes (append + attention) to the average batch
         b = int(cap.get("batch", 0))
-        scale = attn_bytes_avg / subs[b]["counts"]["attn_bytes"]
-        roof["traffic"] = int((cap["dram_bytes_read"] + cap["dram_bytes_write"]) * scale)
-        roof["traffic_source"] = f"ncu capture of batch {b}, scaled by algorithmic bytes"
-    roof["kernel"] = "ms_mixed_step_attention (prologue + items + persistent attention_kernel launches)"
+        scale = grp_bytes_avg / subs[b]["counts"]["step_bytes"]
+        roof["traffic"] = int((cap["dram_bytes_read"] + cap["dram_bytes_write"] + cap["append_dram_bytes"]) * scale)
+        roof["traffic_source"] = f"ncu capture of batch {b} (append + attention kernels), scaled by algorithmic bytes"
+    roof["kernel"] = ("one batch of the path: ms_kv_append_rope + ms_mixed_step_attention "
+                      "(append, prologue, items and persistent attention_kernel launches)")
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
-    roof["per_launch"] = {"alg_bytes": int(attn_bytes_avg), "alg_flops": int(attn_flops_avg),
-                          "avg_ms": round(attn_avg_ms, 4)}
+    roof["per_launch"] = {"alg_bytes": int(grp_bytes_avg), "alg_flops": int(flops_avg),
+                          "avg_ms": round(grp_avg_ms, 4)}
     step_bytes = sum(s["counts"]["step_bytes"] for s in subs)
     step_flops = attn_flops
     t_roof = max(step_bytes / (peaks["hbm_gbs"] * 1e9), step_flops / (peaks["bf16_tflops_sustained"] * 1e12))
