@@ -130,12 +130,22 @@ def test_worked_example_four_rounds(env):
 
 
 @pytest.mark.parametrize("H_q,H_kv,D", [(8, 2, 128), (8, 8, 64), (4, 4, 128), (16, 2, 128), (8, 2, 64),
-                                        (4, 1, 64)])
+                                        (4, 1, 64), (8, 4, 128), (16, 2, 64)])
 def test_small_mixed_all_rows(env, H_q, H_kv, D):
     """Decodes at c = 0, page boundaries and beyond a tile; chunks of 130 (several tiles), 200 at offset 300
     and a 5-token tail at offset 16."""
     wl = workloads.small_mixed(seed=H_q * 100 + H_kv * 10 + D, H_q=H_q, H_kv=H_kv, D=D)
     _full_parity(env, wl, _states(wl), seed=7)
+
+
+@pytest.mark.parametrize("H_q,H_kv,D", [(4, 4, 128), (8, 2, 128), (8, 8, 64)])
+def test_odd_query_tile_counts(env, H_q, H_kv, D):
+    """Chunks whose 128-row query tiles come in odd numbers, so that the last work item holds a
+    single tile (G = 1: 300 tokens = 3 tiles; G = 4: 70 tokens = 3 tiles, 390 = 13), next to
+    decodes."""
+    wl = workloads.small_mixed(seed=50 + H_q + D, H_q=H_q, H_kv=H_kv, D=D, dec_ctx=(3, 129, 640),
+                               prompts=((0, 300), (50, 70), (1000, 390)))
+    _full_parity(env, wl, _states(wl), seed=9)
 
 
 def test_decode_only_and_chunk_only(env):
