@@ -39,6 +39,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "mixed_step.h"
@@ -1483,18 +1484,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// the driver's tensor-map encoder, looked up once (thread-safe static initialisation)
 EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -1506,15 +1506,42 @@ bool encode_bf16(EncodeTiledFn fn, CUtensorMap* map, const void* base, int rank,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_num_sms = 0;
+// Per-device host state (devices 0 .. kMaxDevices - 1): the SM count and which
+// kernels have had their shared-memory limit raised.  Safe to use from
+// several host threads: every entry is computed the same way by whoever gets
+// there first.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_num_sms[kMaxDevices];
+std::atomic<uint32_t> g_smem_attr_set[kMaxDevices];
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
 
 int num_sms() {
-  if (g_num_sms > 0) return g_num_sms;
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  g_num_sms = n;
+  const int dev = current_device();
+  if (dev < 0) return -1;
+  const int cached = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (cached > 0) return cached;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return -1;
+  g_num_sms[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+// Raise `kernel`'s dynamic shared-memory limit on the current device once
+// (bit `slot` of the device's mask).
+template <typename Kernel>
+int ensure_smem_limit(Kernel kernel, int slot, int bytes) {
+  const int dev = current_device();
+  if (dev < 0) return MS_ERR_CUDA;
+  if (g_smem_attr_set[dev].load(std::memory_order_acquire) & (1u << slot)) return MS_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return MS_ERR_CUDA;
+  g_smem_attr_set[dev].fetch_or(1u << slot, std::memory_order_release);
+  return MS_OK;
 }
 
 // Launch as a programmatic dependent of the previous kernel on the stream: the
@@ -1555,13 +1582,8 @@ int launch_paths(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& 
                  int n_ctas, cudaStream_t st) {
   constexpr int smem = ChCfg<D>::SMEM > DecCfg<D, G>::SMEM ? ChCfg<D>::SMEM : DecCfg<D, G>::SMEM;
   static_assert(smem <= 232448, "attention kernel exceeds the per-CTA shared-memory limit");
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(attention_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return MS_ERR_CUDA;
-    configured = true;
-  }
+  const int slot = (D == 128 ? 4 : 0) + (G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3);  // one bit per instance
+  if (ensure_smem_limit(attention_kernel<D, G>, slot, smem) != MS_OK) return MS_ERR_CUDA;
   if (launch_dependent(attention_kernel<D, G>, dim3(n_ctas), dim3(kChunkThreads), smem, st, tq, tk, tv, p) !=
       cudaSuccess)
     return MS_ERR_CUDA;
@@ -1665,13 +1687,7 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
 
   if (num_rows > kMaxRows) return MS_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  static bool prologue_configured = false;
-  if (!prologue_configured) {
-    if (cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             sizeof(PrologueSmem)) != cudaSuccess)
-      return MS_ERR_CUDA;
-    prologue_configured = true;
-  }
+  if (ensure_smem_limit(prologue_kernel, 8, static_cast<int>(sizeof(PrologueSmem))) != MS_OK) return MS_ERR_CUDA;
   if (launch_dependent(prologue_kernel, dim3(1), dim3(kPrologueThreads), sizeof(PrologueSmem), st, p) !=
           cudaSuccess ||
       launch_dependent(items_kernel, dim3(sms < 64 ? sms : 64), dim3(kItemThreads), 0, st, p) != cudaSuccess)
@@ -1719,7 +1735,6 @@ extern "C" MS_API int ms_read_status(int32_t* dev_status, ms_stream_t stream, in
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB per device
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_step_scratch[kNoAllocScratchBytes];
 
@@ -1730,8 +1745,8 @@ void* g_scratch_addr[kMaxDevices] = {};
 // device (host code must not pass the symbol itself to a kernel: on the host
 // it names a stand-in, not device memory).
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MS_ERR_CUDA;
+  const int dev = current_device();
+  if (dev < 0) return MS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
