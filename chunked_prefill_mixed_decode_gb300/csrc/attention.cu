@@ -415,18 +415,21 @@ __global__ void __launch_bounds__(kItemThreads) items_kernel(AttnParams p) {
 
 template <int D, int G>
 struct DecCfg {
-  static constexpr int EPL = D / 16;               // columns per lane of one token row
-  static constexpr int NST = D == 128 ? 2 : 4;            // ring stages per warp
+  static constexpr int EPL = D / 16;               // columns per lane of one token row (G = 1 path)
+  static constexpr int NST = D == 128 ? 2 : 4;     // ring stages per warp
   static constexpr int PAGE_BYTES = kPage * D * 2;  // one page of one KV head
-  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
+  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;  // K page, then V page
   static constexpr int Q_BYTES = G * D * 2;
-  static constexpr int Q_OFF = NST * STAGE_BYTES;
-  static constexpr int P_OFF = Q_OFF + 2 * Q_BYTES;
-  static constexpr int BAR_OFF = P_OFF + G * 16 * 4;
-  static constexpr int WARP_BYTES = (BAR_OFF + NST * 8 + 127) / 128 * 128;
+  // per-warp tail: two Q buffers, the P exchange (G = 1 path), the ring barriers
+  static constexpr int T_P = 2 * Q_BYTES;
+  static constexpr int T_BAR = T_P + G * 16 * 4;
+  static constexpr int TAIL_BYTES = (T_BAR + NST * 8 + 127) / 128 * 128;
   // as many worker warps as the CTA has, while their rings fit in shared memory
-  static constexpr int WARPS = 12 * WARP_BYTES <= 230000 ? 12 : 10;
-  static constexpr int SMEM = WARPS * WARP_BYTES;
+  static constexpr int WARPS = 12 * (NST * STAGE_BYTES + TAIL_BYTES) <= 230000 ? 12 : 10;
+  // all warps' stages first (each stage 1024-aligned, as 128-byte-swizzled TMA
+  // tiles need), then the warps' tails
+  static constexpr int TAIL_OFF = WARPS * NST * STAGE_BYTES;
+  static constexpr int SMEM = TAIL_OFF + WARPS * TAIL_BYTES;
 };
 
 
@@ -544,14 +547,16 @@ __device__ __forceinline__ void lds_row2(const bf16* src, float2 (&f)[EPL / 2]) 
 }
 
 template <int D, int G>
-__device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem) {
+__device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem, const CUtensorMap* tm_k,
+                                             const CUtensorMap* tm_v) {
   using C = DecCfg<D, G>;
   constexpr int EPL = C::EPL, NST = C::NST;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp >= DecCfg<D, G>::WARPS) return;  // the CTA's remaining warps have no decode slice
-  uint8_t* wbase = dsmem + warp * C::WARP_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(wbase + C::BAR_OFF);
-  float* pbuf = reinterpret_cast<float*>(wbase + C::P_OFF);  // [G][2 halves][8]
+  uint8_t* stg = dsmem + warp * NST * C::STAGE_BYTES;             // this warp's ring stages
+  uint8_t* tail = dsmem + C::TAIL_OFF + warp * C::TAIL_BYTES;     // its Q buffers, P exchange, barriers
+  uint64_t* full = reinterpret_cast<uint64_t*>(tail + C::T_BAR);
+  float* pbuf = reinterpret_cast<float*>(tail + C::T_P);  // [G][2 halves][8]
   const int n_items = p.hdr[H_NDEC_ITEMS];
   const int split = p.hdr[H_SPLIT];
   if (lane == 0) {
@@ -591,19 +596,28 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
     int phys = __shfl_sync(0xffffffffu, iss_bt, pi & 31);
     if (lane == 0) {
       const int st = seq_iss % NST;
-      uint8_t* stage = wbase + st * C::STAGE_BYTES;
+      uint8_t* stage = stg + st * C::STAGE_BYTES;
       if (phys < 0 || phys >= p.num_pages) {
         atomicOr(p.hdr + H_STATUS, MS_STATUS_BAD_PAGE);
         phys = 0;
       }
-      const int64_t off = (static_cast<int64_t>(phys) * p.H_kv + it.hk) * head_stride;
       const uint32_t bytes = 2 * C::PAGE_BYTES + (pi == 0 ? C::Q_BYTES : 0);
       mbar_arrive_expect_tx(full + st, bytes);
-      bulk_g2s(stage, p.k_cache + off, C::PAGE_BYTES, full + st);
-      bulk_g2s(stage + C::PAGE_BYTES, p.v_cache + off, C::PAGE_BYTES, full + st);
+      if constexpr (G == 1) {  // the page as it lies in memory
+        const int64_t off = (static_cast<int64_t>(phys) * p.H_kv + it.hk) * head_stride;
+        bulk_g2s(stage, p.k_cache + off, C::PAGE_BYTES, full + st);
+        bulk_g2s(stage + C::PAGE_BYTES, p.v_cache + off, C::PAGE_BYTES, full + st);
+      } else {  // 16-row x 64-column boxes, 128-byte swizzled, for conflict-free ldmatrix
+        const int row0 = (phys * p.H_kv + it.hk) * kPage;
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s) {
+          tma_load_2d(stage + s * 2048, tm_k, s * 64, row0, full + st);
+          tma_load_2d(stage + C::PAGE_BYTES + s * 2048, tm_v, s * 64, row0, full + st);
+        }
+      }
       if (pi == 0)
-        bulk_g2s(wbase + C::Q_OFF + qpar * C::Q_BYTES,
-                 p.q_rot + (static_cast<int64_t>(it.tok) * p.H_q + it.hk * G) * D, C::Q_BYTES, full + st);
+        bulk_g2s(tail + qpar * C::Q_BYTES, p.q_rot + (static_cast<int64_t>(it.tok) * p.H_q + it.hk * G) * D,
+                 C::Q_BYTES, full + st);
     }
     ++seq_iss;
   };
@@ -624,6 +638,7 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
   pump();
 
   while (true) {
+    if constexpr (G == 1) {
     constexpr int EP2 = EPL / 2;  // fp32 pairs per lane of one token row
     float2 q[G][EP2], acc[G][EP2];
     float m[G], l[G];
@@ -640,10 +655,10 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
         failed = true;
         break;
       }
-      const bf16* Ks = reinterpret_cast<const bf16*>(wbase + st * C::STAGE_BYTES);
+      const bf16* Ks = reinterpret_cast<const bf16*>(stg + st * C::STAGE_BYTES);
       const bf16* Vs = Ks + kPage * D;
       if (pi == 0) {
-        const bf16* qs = reinterpret_cast<const bf16*>(wbase + C::Q_OFF + item_par * C::Q_BYTES);
+        const bf16* qs = reinterpret_cast<const bf16*>(tail + item_par * C::Q_BYTES);
 #pragma unroll
         for (int g = 0; g < G; ++g) lds_row2<EPL>(qs + g * D + sub * EPL, q[g]);
       }
@@ -779,6 +794,130 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
         }
       }
       if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + rec * 2) = make_float2(m[g], lt);
+    }
+    } else {
+    // G >= 2: tensor-core MMAs (mma.sync m16n8k16) on each page.  S^T = K Q^T
+    // holds 16 tokens x 8 query heads (heads past G are zero); P^T goes back
+    // through a register transpose; O^T = V^T P^T accumulates D x 8.
+    constexpr int NK = D / 16;  // 16-column steps of a K row, and 16-row blocks of O^T
+    const int gq = lane >> 2, tq = lane & 3;
+    uint32_t qb[NK][2];
+    float acc[NK][4];
+#pragma unroll
+    for (int j = 0; j < NK; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    float mu0 = -INFINITY, mu1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2 tq and 2 tq + 1
+    constexpr float kRescaleLog2 = 8.f;  // raise the reference max only when it grows by 2^8
+    for (int pi = 0; pi < cur.np; ++pi) {
+      const int st = seq_con % NST;
+      if (!mbar_wait(full + st, (seq_con / NST) & 1u, nullptr)) {
+        failed = true;
+        break;
+      }
+      const uint32_t kb = smem_u32(stg + st * C::STAGE_BYTES), vb = kb + C::PAGE_BYTES;
+      if (pi == 0) {
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(tail + item_par * C::Q_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+          qb[kk][0] = gq < G ? q32[(gq * D + 16 * kk + 2 * tq) >> 1] : 0u;
+          qb[kk][1] = gq < G ? q32[(gq * D + 16 * kk + 8 + 2 * tq) >> 1] : 0u;
+        }
+      }
+      const int tok0 = (cur.p0 + pi) * kPage;
+      const int nv = min(kPage, cur.ctx - tok0);  // valid keys in this page (>= 1)
+      // S^T: lane holds (token gq, heads 2 tq, 2 tq + 1) and (token gq + 8, same heads)
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < NK; ++kk) {
+        const int r = lane & 15, chunk = (kk & 3) * 2 + (lane >> 4);
+        uint32_t a[4];
+        ldsm_x4(kb + (kk >> 2) * 2048 + r * 128 + ((chunk ^ (r & 7)) << 4), a);
+        mma_16816_bf16(c, a, qb[kk][0], qb[kk][1]);
+      }
+      const float sl2 = p.scale_log2;
+      const float s0 = gq < nv ? c[0] * sl2 : -INFINITY, s1 = gq < nv ? c[1] * sl2 : -INFINITY;
+      const float s2 = gq + 8 < nv ? c[2] * sl2 : -INFINITY, s3 = gq + 8 < nv ? c[3] * sl2 : -INFINITY;
+      float mh0 = fmaxf(s0, s2), mh1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mh0 = fmaxf(mh0, __shfl_xor_sync(0xffffffffu, mh0, o));
+        mh1 = fmaxf(mh1, __shfl_xor_sync(0xffffffffu, mh1, o));
+      }
+      const bool g0 = mh0 > mu0 + kRescaleLog2, g1 = mh1 > mu1 + kRescaleLog2;
+      if (__any_sync(0xffffffffu, g0 || g1)) {
+        const float n0 = g0 ? mh0 : mu0, n1 = g1 ? mh1 : mu1;
+        const float a0 = g0 ? ex2(mu0 - n0) : 1.f, a1 = g1 ? ex2(mu1 - n1) : 1.f;
+#pragma unroll
+        for (int j = 0; j < NK; ++j) {
+          acc[j][0] *= a0;
+          acc[j][1] *= a1;
+          acc[j][2] *= a0;
+          acc[j][3] *= a1;
+        }
+        l0 *= a0;
+        l1 *= a1;
+        mu0 = n0;
+        mu1 = n1;
+      }
+      const float p0 = ex2(s0 - mu0), p1 = ex2(s1 - mu1), p2 = ex2(s2 - mu0), p3 = ex2(s3 - mu1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1), h23 = __floats2bfloat162_rn(p2, p3);
+      // P^T as the B operand: lane holds (tokens 2 tq, 2 tq + 1 | + 8, head gq)
+      const uint32_t b0 = movmatrix_trans(*reinterpret_cast<uint32_t*>(&h01));
+      const uint32_t b1 = movmatrix_trans(*reinterpret_cast<uint32_t*>(&h23));
+      if (nv < kPage) {
+        // rows past the context in the last page may hold stale (even non-finite) data:
+        // zero them in V so that P = 0 times V stays 0
+        uint8_t* v0 = stg + st * C::STAGE_BYTES + C::PAGE_BYTES;
+        for (int i = lane; i < (kPage - nv) * (D / 8); i += 32) {
+          const int r = nv + i / (D / 8), cc = i % (D / 8);  // row, 16-byte chunk of the row
+          *reinterpret_cast<uint4*>(v0 + (cc >> 3) * 2048 + r * 128 + (cc & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();  // ordered before the next copy into this stage
+        __syncwarp();
+      }
+#pragma unroll
+      for (int j = 0; j < NK; ++j) {
+        const int r = ((lane >> 4) << 3) + (lane & 7), chunk = (j & 3) * 2 + ((lane >> 3) & 1);
+        uint32_t a[4];
+        ldsm_x4_trans(vb + (j >> 2) * 2048 + r * 128 + ((chunk ^ (r & 7)) << 4), a);
+        mma_16816_bf16(acc[j], a, b0, b1);
+      }
+      __syncwarp();
+      ++seq_con;
+      pump();
+    }
+    if (failed) break;
+    // O^T: lane holds (d 16 j + gq, heads 2 tq, 2 tq + 1) and (d 16 j + gq + 8, same heads)
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int hh = 2 * tq + e;
+      if (hh >= G) continue;
+      const float L = e == 0 ? l0 : l1, M = e == 0 ? mu0 : mu1;
+      if (cur.ns == 1) {
+        const float inv = 1.f / L;
+        bf16* dst = p.out + (static_cast<int64_t>(cur.tok) * p.H_q + cur.hk * G + hh) * D;
+#pragma unroll
+        for (int j = 0; j < NK; ++j) {
+          dst[16 * j + gq] = __float2bfloat16_rn(acc[j][e] * inv);
+          dst[16 * j + gq + 8] = __float2bfloat16_rn(acc[j][2 + e] * inv);
+        }
+      } else {
+        const int64_t rec = cur.part + hh;
+        float* dst = p.part_acc + rec * D;
+#pragma unroll
+        for (int j = 0; j < NK; ++j) {
+          dst[16 * j + gq] = acc[j][e];
+          dst[16 * j + gq + 8] = acc[j][2 + e];
+        }
+        if (gq == 0) *reinterpret_cast<float2*>(p.part_ml + rec * 2) = make_float2(M, L);
+      }
+    }
     }
     if (cur.ns > 1) {
       __threadfence();  // this split's records are visible before it is counted
@@ -1361,7 +1500,7 @@ __device__ __forceinline__ void invalidate_phase_barriers(uint8_t* smem, bool ch
     }
   } else if ((threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < DecCfg<D, G>::WARPS) {
     using C = DecCfg<D, G>;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (threadIdx.x >> 5) * C::WARP_BYTES + C::BAR_OFF);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::TAIL_OFF + (threadIdx.x >> 5) * C::TAIL_BYTES + C::T_BAR);
     for (int i = 0; i < C::NST; ++i) mbar_inval(full + i);
   }
 }
@@ -1413,7 +1552,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       __syncthreads();
       if (aborted) break;
     } else if (!chunk && n_dec_items > 0) {
-      decode_phase<D, G>(p, smem);
+      decode_phase<D, G>(p, smem, &tm_k, &tm_v);
       __syncwarp();
       invalidate_phase_barriers<D, G>(smem, false);
       __syncthreads();
