@@ -9,13 +9,14 @@
 // Stall", section 03; "Splitting Prefill From Decode Inside a Step", "Two
 // kernels with different limiting resources"), so they take two paths:
 //
-//   decode rows (d = 1): split-KV on CUDA cores.  One warp owns a work item
-//     (row, KV head, span of pages) and streams its pages through a private
-//     ring in shared memory with bulk async copies; the G query heads of the
-//     KV head share every page read.  Lanes hold 8 (D = 128) or 4 (D = 64)
-//     columns of two token rows per 16-byte load; dot products finish with
-//     warp shuffles.  Each item leaves a partial (max, sum, accumulator); the
-//     last split of a (row, KV head) to finish merges them into the output.
+//   decode rows (d = 1): split-KV with warp-level tensor-core MMAs.  One warp
+//     owns a work item (row, KV head, span of pages) and streams its pages
+//     through a private ring in shared memory with TMA (128-byte swizzled
+//     16-row boxes); the G query heads of the KV head share every page read.
+//     Per page, S^T = K Q^T (16 tokens x G heads, padded to 8) and
+//     O^T += V^T P^T run as mma.sync m16n8k16 on ldmatrix fragments, with P
+//     transposed in registers.  Each item leaves a partial (max, sum,
+//     accumulator); the last split of a (row, KV head) to finish merges them.
 //   chunk rows (d > 1): tcgen05 tensor cores.  A CTA owns a 128-row query
 //     tile (128/G tokens x G heads of one KV head) and walks 128-key tiles of
 //     the prefix and its own chunk.  TMA loads Q and K/V pages (one 16-row box
@@ -410,19 +411,17 @@ __global__ void __launch_bounds__(kItemThreads) items_kernel(AttnParams p) {
 }
 
 // ----------------------------------------------------------------------------
-// decode rows: split-KV on CUDA cores
+// decode rows: split-KV, warp-level tensor-core MMAs
 // ----------------------------------------------------------------------------
 
 template <int D, int G>
 struct DecCfg {
-  static constexpr int EPL = D / 16;               // columns per lane of one token row (G = 1 path)
   static constexpr int NST = D == 128 ? 2 : 4;     // ring stages per warp
   static constexpr int PAGE_BYTES = kPage * D * 2;  // one page of one KV head
   static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;  // K page, then V page
   static constexpr int Q_BYTES = G * D * 2;
-  // per-warp tail: two Q buffers, the P exchange (G = 1 path), the ring barriers
-  static constexpr int T_P = 2 * Q_BYTES;
-  static constexpr int T_BAR = T_P + G * 16 * 4;
+  // per-warp tail: two Q buffers, then the ring barriers
+  static constexpr int T_BAR = 2 * Q_BYTES;
   static constexpr int TAIL_BYTES = (T_BAR + NST * 8 + 127) / 128 * 128;
   // as many worker warps as the CTA has, while their rings fit in shared memory
   static constexpr int WARPS = 12 * (NST * STAGE_BYTES + TAIL_BYTES) <= 230000 ? 12 : 10;
@@ -462,19 +461,6 @@ __device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, i
   return it;
 }
 
-// load EPL bf16 columns of one token row from shared memory as fp32
-template <int EPL>
-__device__ __forceinline__ void lds_row(const bf16* src, float (&f)[EPL]) {
-  if constexpr (EPL == 8) {
-    const uint4 u = *reinterpret_cast<const uint4*>(src);
-    const float2 a = bf2_to_f2(u.x), b = bf2_to_f2(u.y), c = bf2_to_f2(u.z), d = bf2_to_f2(u.w);
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
-  } else {
-    const uint2 u = *reinterpret_cast<const uint2*>(src);
-    const float2 a = bf2_to_f2(u.x), b = bf2_to_f2(u.y);
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  }
-}
 
 // Merge the ns split records of decode row k for query heads h0 .. h0+nh-1
 // into bf16 output (one warp; lane owns D/32 columns).  Records written by
@@ -532,31 +518,23 @@ __device__ __forceinline__ void merge_splits(const AttnParams& p, int k, int h0,
   }
 }
 
-// Decode phase: each of the CTA's 8 warps is an independent worker over its
-// own slice of shared memory, pulling decode items until the queue is empty.
-// load EPL bf16 columns of one token row from shared memory as EPL/2 fp32 pairs
-template <int EPL>
-__device__ __forceinline__ void lds_row2(const bf16* src, float2 (&f)[EPL / 2]) {
-  if constexpr (EPL == 8) {
-    const uint4 u = *reinterpret_cast<const uint4*>(src);
-    f[0] = bf2_to_f2(u.x); f[1] = bf2_to_f2(u.y); f[2] = bf2_to_f2(u.z); f[3] = bf2_to_f2(u.w);
-  } else {
-    const uint2 u = *reinterpret_cast<const uint2*>(src);
-    f[0] = bf2_to_f2(u.x); f[1] = bf2_to_f2(u.y);
-  }
-}
+// Decode phase: each worker warp of the CTA (12, or 10 at D = 128, G = 8) is
+// independent, with its own ring of page stages, pulling decode items until
+// the queue is empty.  Per page it runs mma.sync m16n8k16 on ldmatrix
+// fragments: 16 tokens against the G query heads (padded to 8).  tcgen05 does
+// not fit here: its M is at least 64 rows and one thread issues an MMA only
+// every 110-140 cycles, while a decode page is 16 rows per warp.
 
 template <int D, int G>
 __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem, const CUtensorMap* tm_k,
                                              const CUtensorMap* tm_v) {
   using C = DecCfg<D, G>;
-  constexpr int EPL = C::EPL, NST = C::NST;
+  constexpr int NST = C::NST;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp >= DecCfg<D, G>::WARPS) return;  // the CTA's remaining warps have no decode slice
   uint8_t* stg = dsmem + warp * NST * C::STAGE_BYTES;             // this warp's ring stages
-  uint8_t* tail = dsmem + C::TAIL_OFF + warp * C::TAIL_BYTES;     // its Q buffers, P exchange, barriers
+  uint8_t* tail = dsmem + C::TAIL_OFF + warp * C::TAIL_BYTES;     // its Q buffers and barriers
   uint64_t* full = reinterpret_cast<uint64_t*>(tail + C::T_BAR);
-  float* pbuf = reinterpret_cast<float*>(tail + C::T_P);  // [G][2 halves][8]
   const int n_items = p.hdr[H_NDEC_ITEMS];
   const int split = p.hdr[H_SPLIT];
   if (lane == 0) {
@@ -565,8 +543,6 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
   }
   __syncwarp();
 
-  const int h = lane >> 4, sub = lane & 15;  // token parity of this lane, column chunk
-  const int64_t head_stride = static_cast<int64_t>(kPage) * D;
 
   auto dequeue = [&]() -> int {
     int v = 0;
@@ -603,17 +579,12 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
       }
       const uint32_t bytes = 2 * C::PAGE_BYTES + (pi == 0 ? C::Q_BYTES : 0);
       mbar_arrive_expect_tx(full + st, bytes);
-      if constexpr (G == 1) {  // the page as it lies in memory
-        const int64_t off = (static_cast<int64_t>(phys) * p.H_kv + it.hk) * head_stride;
-        bulk_g2s(stage, p.k_cache + off, C::PAGE_BYTES, full + st);
-        bulk_g2s(stage + C::PAGE_BYTES, p.v_cache + off, C::PAGE_BYTES, full + st);
-      } else {  // 16-row x 64-column boxes, 128-byte swizzled, for conflict-free ldmatrix
-        const int row0 = (phys * p.H_kv + it.hk) * kPage;
+      // 16-row x 64-column boxes, 128-byte swizzled, for conflict-free ldmatrix
+      const int row0 = (phys * p.H_kv + it.hk) * kPage;
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s) {
-          tma_load_2d(stage + s * 2048, tm_k, s * 64, row0, full + st);
-          tma_load_2d(stage + C::PAGE_BYTES + s * 2048, tm_v, s * 64, row0, full + st);
-        }
+      for (int s = 0; s < D / 64; ++s) {
+        tma_load_2d(stage + s * 2048, tm_k, s * 64, row0, full + st);
+        tma_load_2d(stage + C::PAGE_BYTES + s * 2048, tm_v, s * 64, row0, full + st);
       }
       if (pi == 0)
         bulk_g2s(tail + qpar * C::Q_BYTES, p.q_rot + (static_cast<int64_t>(it.tok) * p.H_q + it.hk * G) * D,
@@ -638,167 +609,9 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
   pump();
 
   while (true) {
-    if constexpr (G == 1) {
-    constexpr int EP2 = EPL / 2;  // fp32 pairs per lane of one token row
-    float2 q[G][EP2], acc[G][EP2];
-    float m[G], l[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
-      l[g] = 0.f;
-#pragma unroll
-      for (int e = 0; e < EP2; ++e) acc[g][e] = make_float2(0.f, 0.f);
-    }
-    for (int pi = 0; pi < cur.np; ++pi) {
-      const int st = seq_con % NST;
-      if (!mbar_wait(full + st, (seq_con / NST) & 1u, nullptr)) {
-        failed = true;
-        break;
-      }
-      const bf16* Ks = reinterpret_cast<const bf16*>(stg + st * C::STAGE_BYTES);
-      const bf16* Vs = Ks + kPage * D;
-      if (pi == 0) {
-        const bf16* qs = reinterpret_cast<const bf16*>(tail + item_par * C::Q_BYTES);
-#pragma unroll
-        for (int g = 0; g < G; ++g) lds_row2<EPL>(qs + g * D + sub * EPL, q[g]);
-      }
-      const int tok0 = (cur.p0 + pi) * kPage;
-      const int nv = min(kPage, cur.ctx - tok0);  // valid keys in this page (>= 1)
-      // q . k for this lane's 8 token rows 2i + h, in two halves of 4 rows to bound registers
-      float part[G][8];
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float2 kf[4][EP2];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) lds_row2<EPL>(Ks + (2 * (hf * 4 + i) + h) * D + sub * EPL, kf[i]);
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float2 acc_d = fmul2(q[g][0], kf[i][0]);
-#pragma unroll
-            for (int e = 1; e < EP2; ++e) acc_d = ffma2(q[g][e], kf[i][e], acc_d);
-            part[g][hf * 4 + i] = acc_d.x + acc_d.y;
-          }
-      }
-      float alpha[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        // reduce-scatter over the 16 lanes of this half: lane ends with token i = sub >> 1
-        const bool b3 = sub & 8, b2 = sub & 4, b1 = sub & 2;
-        float w4[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float send = b3 ? part[g][j] : part[g][j + 4];
-          const float keep = b3 ? part[g][j + 4] : part[g][j];
-          w4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-        float w2[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float send = b2 ? w4[j] : w4[j + 2];
-          const float keep = b2 ? w4[j + 2] : w4[j];
-          w2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-        float y = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
-        y += __shfl_xor_sync(0xffffffffu, y, 1);
-        const int ti = sub >> 1;  // this lane's token: 2 * ti + h
-        const float sc = (2 * ti + h < nv) ? y * p.scale_log2 : -INFINITY;
-        float mx = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m[g], mx);
-        alpha[g] = ex2(m[g] - m_new);
-        const float pr = ex2(sc - m_new);
-        l[g] = l[g] * alpha[g] + ((lane & 1) ? 0.f : pr);
-        m[g] = m_new;
-        if ((lane & 1) == 0) pbuf[(g * 2 + h) * 8 + ti] = pr;
-      }
-      __syncwarp();
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float2 a2 = make_float2(alpha[g], alpha[g]);
-#pragma unroll
-        for (int e = 0; e < EP2; ++e) acc[g][e] = fmul2(acc[g][e], a2);
-      }
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float2 vf[4][EP2];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          lds_row2<EPL>(Vs + (2 * (hf * 4 + i) + h) * D + sub * EPL, vf[i]);
-          if (2 * (hf * 4 + i) + h >= nv) {
-#pragma unroll
-            for (int e = 0; e < EP2; ++e) vf[i][e] = make_float2(0.f, 0.f);  // keys past the context: stale data
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 pw = *reinterpret_cast<const float4*>(pbuf + (g * 2 + h) * 8 + hf * 4);
-          const float2 pv[4] = {make_float2(pw.x, pw.x), make_float2(pw.y, pw.y), make_float2(pw.z, pw.z),
-                                make_float2(pw.w, pw.w)};
-#pragma unroll
-          for (int e = 0; e < EP2; ++e) {
-            float2 a = acc[g][e];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a = ffma2(pv[i], vf[i][e], a);
-            acc[g][e] = a;
-          }
-        }
-      }
-      __syncwarp();
-      ++seq_con;
-      pump();
-    }
-    if (failed) break;
-    // Per query head: one split writes the normalised bf16 output itself;
-    // otherwise it leaves a partial record (max, sum, unnormalised accumulator)
-    // and the last split of the (row, KV head) to finish merges them all.
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float lt = l[g];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
-      float a[EPL];
-#pragma unroll
-      for (int e = 0; e < EP2; ++e) {
-        a[2 * e] = acc[g][e].x + __shfl_xor_sync(0xffffffffu, acc[g][e].x, 16);
-        a[2 * e + 1] = acc[g][e].y + __shfl_xor_sync(0xffffffffu, acc[g][e].y, 16);
-      }
-      if (cur.ns == 1) {
-        if (h == 0) {
-          const float inv = 1.f / lt;
-          bf16* dst = p.out + (static_cast<int64_t>(cur.tok) * p.H_q + cur.hk * G + g) * D + sub * EPL;
-          uint32_t w[EPL / 2];
-#pragma unroll
-          for (int e = 0; e < EPL / 2; ++e) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(a[2 * e] * inv, a[2 * e + 1] * inv);
-            w[e] = *reinterpret_cast<uint32_t*>(&b2);
-          }
-          if constexpr (EPL == 8)
-            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-          else
-            *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-        }
-        continue;
-      }
-      const int64_t rec = cur.part + g;
-      if (h == 0) {
-        float* dst = p.part_acc + rec * D + sub * EPL;
-        if constexpr (EPL == 8) {
-          *reinterpret_cast<float4*>(dst) = make_float4(a[0], a[1], a[2], a[3]);
-          *reinterpret_cast<float4*>(dst + 4) = make_float4(a[4], a[5], a[6], a[7]);
-        } else {
-          *reinterpret_cast<float4*>(dst) = make_float4(a[0], a[1], a[2], a[3]);
-        }
-      }
-      if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + rec * 2) = make_float2(m[g], lt);
-    }
-    } else {
-    // G >= 2: tensor-core MMAs (mma.sync m16n8k16) on each page.  S^T = K Q^T
-    // holds 16 tokens x 8 query heads (heads past G are zero); P^T goes back
-    // through a register transpose; O^T = V^T P^T accumulates D x 8.
+    // Tensor-core MMAs (mma.sync m16n8k16) on each page.  S^T = K Q^T holds
+    // 16 tokens x 8 query heads (heads past G are zero); P^T goes back through
+    // a register transpose; O^T = V^T P^T accumulates D x 8.
     constexpr int NK = D / 16;  // 16-column steps of a K row, and 16-row blocks of O^T
     const int gq = lane >> 2, tq = lane & 3;
     uint32_t qb[NK][2];
@@ -917,7 +730,6 @@ __device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem
         }
         if (gq == 0) *reinterpret_cast<float2*>(p.part_ml + rec * 2) = make_float2(M, L);
       }
-    }
     }
     if (cur.ns > 1) {
       __threadfence();  // this split's records are visible before it is counted
