@@ -156,6 +156,34 @@ def test_decode_only_and_chunk_only(env):
     _full_parity(env, wl, _states(wl), seed=9)
 
 
+@pytest.mark.parametrize("n_dec", [3000, 8191])
+def test_many_rows(env, n_dec):
+    """Steps past the prologue's sort limit (2048 rows per list are ordered longest-first; more
+    keep input order) up to the 8192-row maximum: decodes with short contexts and one chunk."""
+    rng = np.random.default_rng(n_dec)
+    ctx = tuple(int(c) for c in rng.integers(0, 80, size=n_dec))
+    wl = workloads.small_mixed(seed=60, H_q=4, H_kv=2, D=64, dec_ctx=ctx, prompts=((40, 37),))
+    _full_parity(env, wl, _states(wl), seed=10)
+
+
+def test_more_rows_than_a_step_holds_is_refused(env):
+    """8193 rows: the call returns MS_ERR_ARG before any launch."""
+    torch, ms, step = env
+    S = 8193
+    meta = {"cu_seqlens_q": np.arange(S + 1, dtype=np.int32), "q_start_pos": np.zeros(S, np.int32),
+            "context_lens": np.ones(S, np.int32), "positions": np.zeros(S, np.int32),
+            "slot_mapping": np.arange(S, dtype=np.int32), "block_tables": np.zeros((S, 1), np.int32),
+            "num_rows": S, "num_tokens": S, "num_decodes": S, "bt_stride": 1}
+    b = step.to_device(meta, "cuda")
+    q = torch.zeros((S, 4, 64), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((S, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ms.MixedStepError) as e:
+        ms.mixed_step_attention(q, kc, kc, b.cu_seqlens_q, b.q_start_pos, b.context_lens, b.block_tables, S,
+                                torch.empty_like(q), ws)
+    assert e.value.code == ms.MS_ERR_ARG
+
+
 def test_chunked_prefill_matches_full_prefill_on_gpu(env):
     """zwjcode section 07: chunks [2, 3, 1] of a 6-token prompt -- and a 300-token prompt as
     [100, 37, 163] -- give the same outputs as one full prefill (same pool, same inputs)."""
