@@ -52,7 +52,7 @@ using bf16 = __nv_bfloat16;
 using namespace ms;
 
 constexpr int kPage = 16;
-constexpr int kMinSplitPages = 16;
+constexpr int kMinSplitPages = 32;
 constexpr int kMaxSplitPages = 256;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kChunkThreads = 32 * (4 + kSoftmaxWarps);  // warp 0 TMA + queue, 2-9 softmax, 1/10/11 MMA
@@ -253,9 +253,11 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
     griddep_wait();
     return;
   }
-  // 2. decode split size: about 16 items per decode worker warp, clamped
-  int64_t split = cdiv64(static_cast<int64_t>(s_dec_pages) * p.H_kv, static_cast<int64_t>(p.dec_workers) * 16);
-  split = split < kMinSplitPages ? kMinSplitPages : (split > kMaxSplitPages ? kMaxSplitPages : split);
+  // 2. decode split size: about 8 items per decode worker warp, clamped; at least
+  // 32 pages (64 when G >= 4, whose items carry G heads of partials to merge)
+  int64_t split = cdiv64(static_cast<int64_t>(s_dec_pages) * p.H_kv, static_cast<int64_t>(p.dec_workers) * 8);
+  const int64_t min_split = p.G >= 4 ? 2 * kMinSplitPages : kMinSplitPages;
+  split = split < min_split ? min_split : (split > kMaxSplitPages ? kMaxSplitPages : split);
   const int tpt = 128 / p.G;
   const unsigned split32 = static_cast<unsigned>(split);
   // 3. the two row lists, each in input order first
@@ -1413,7 +1415,7 @@ WsLayout ws_layout(int64_t max_rows, int64_t max_tokens, int64_t max_context_tot
   off = align_up(off + (max_rows + 1) * 4, 16);
   w.dec_cnt = off;
   off = align_up(off + max_rows * H_kv * 4, 256);
-  // every decode split covers >= kMinSplitPages pages: splits <= ctx/256 + rows/16 + rows
+  // every decode split covers >= kMinSplitPages pages: splits <= ctx / (16 * kMinSplitPages) + rows
   const int64_t max_splits = cdiv64(max_context_total, kPage * kMinSplitPages) + 2 * max_rows;
   const int64_t G = H_q / (H_kv > 0 ? H_kv : 1);
   w.max_dec_items = H_kv * max_splits;
