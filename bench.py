@@ -10,6 +10,7 @@ the prompt's nine prefix offsets 0, 448, ..., 3584 (nine batches per step,
 is larger than L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+  python bench.py --timeline | --split   (supplementary: step-latency timeline; decode/chunk split)
 
 Under torchrun each rank runs its own replica (weak scaling); timing is the
 max over ranks.  --impl reference times the fp64 CPU oracle on a bounded sample
@@ -595,6 +596,123 @@ def run_timeline(args, local):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------- decode / chunk split
+
+SPLIT_CONFIGS = ["mha7b_b512", "mha13b_b2048", "gqa8b_b8192", "long_bimodal_b4608"]
+
+
+def _timed(fn, reps: int, stream) -> float:
+    """Mean device milliseconds of fn() over reps launches (events on the launching stream)."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_split(args, local):
+    """Attribute each workload's step to its two bounds: the attention call on the mixed batch, on
+    its decode rows alone (HBM GB/s of their KV reads) and on its prefill chunks alone (TFLOP/s
+    of their causal pairs), plus the append on the mixed batch.  Every variant reads the same KV
+    pool; each call is timed alone (back to back, CUDA events), summed over the workload's batches."""
+    import torch
+
+    import chunked_prefill_mixed_decode_gb300 as ms
+    from chunked_prefill_mixed_decode_gb300 import build as msbuild
+    from chunked_prefill_mixed_decode_gb300 import roofline, step
+
+    msbuild.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_src = read_peaks()
+    reps = max(5, args.split_reps)
+    out = []
+    for name in args.split_configs:
+        wls = load_workload(name)
+        wl0 = wls[0]
+        k_cache, v_cache = workloads.kv_pool(wl0, 1000, device)
+        cos, sin = step.rope_tables_device(max(wl.max_pos for wl in wls) + 1, wl0.D, device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        acc = {"mixed_ms": 0.0, "append_ms": 0.0, "decode_only_ms": 0.0, "chunk_only_ms": 0.0,
+               "decode_bytes": 0, "decode_kv_bytes": 0, "chunk_flops": 0, "append_bytes": 0, "mixed_bytes": 0,
+               "mixed_flops": 0}
+        for i, wl in enumerate(wls):
+            parts = {"mixed": wl.requests,
+                     "decode_only": [r for r in wl.requests if r.remaining == 0],
+                     "chunk_only": [r for r in wl.requests if r.remaining > 0]}
+            for label, reqs in parts.items():
+                states = [(r.cached_len, r.remaining) for r in reqs]
+                tables = [r.block_table for r in reqs]
+                meta = ms.build_batch_metadata(states, tables, wl.token_budget, wl.max_chunk)
+                T = meta["num_tokens"]
+                if T == 0:
+                    continue
+                b = step.to_device(meta, device)
+                q, k, v = workloads.step_tensors(wl, T, 50 + i, device)
+                q_rot, o = torch.empty_like(q), torch.empty_like(q)
+                ws = step.workspace_for(b, wl.H_q, wl.H_kv, wl.D, device)
+                rows = [(int(meta["q_start_pos"][s_]), int(meta["cu_seqlens_q"][s_ + 1] - meta["cu_seqlens_q"][s_]))
+                        for s_ in range(meta["num_rows"])]
+                cnt = roofline.step_counts(rows, wl.H_q, wl.H_kv, wl.D, meta["bt_stride"])
+
+                def append():
+                    ms.kv_append_rope(q, k, v, b.positions, b.slot_mapping, cos, sin, k_cache, v_cache,
+                                      q_rot=q_rot, dev_status=status, stream=stream)
+
+                def attend():
+                    ms.mixed_step_attention(q_rot, k_cache, v_cache, b.cu_seqlens_q, b.q_start_pos,
+                                            b.context_lens, b.block_tables, b.context_total, o, ws, stream=stream)
+
+                append()
+                t_attn = _timed(attend, reps, stream)
+                if ms.read_status(status) or ms.read_status(ws):
+                    raise RuntimeError(f"device status set in {name} {label}")
+                acc[label + "_ms"] += t_attn
+                if label == "mixed":
+                    acc["append_ms"] += _timed(append, reps, stream)
+                    acc["append_bytes"] += cnt["append_bytes"]
+                    acc["mixed_bytes"] += cnt["attn_bytes"]
+                    acc["mixed_flops"] += cnt["flops"]
+                elif label == "decode_only":
+                    acc["decode_bytes"] += cnt["attn_bytes"]
+                    acc["decode_kv_bytes"] += cnt["decode_kv_bytes"]
+                else:
+                    acc["chunk_flops"] += cnt["flops"]
+                del b, q, k, v, q_rot, o, ws
+        del k_cache, v_cache
+        torch.cuda.empty_cache()
+        hbm, tf = peaks["hbm_gbs"], peaks["bf16_tflops"]
+        dec_gbs = acc["decode_bytes"] / (acc["decode_only_ms"] / 1e3) / 1e9 if acc["decode_only_ms"] else None
+        chk_tf = acc["chunk_flops"] / (acc["chunk_only_ms"] / 1e3) / 1e12 if acc["chunk_only_ms"] else None
+        t_roof_mixed = max(acc["mixed_bytes"] / (hbm * 1e9), acc["mixed_flops"] / (tf * 1e12)) * 1e3
+        out.append({
+            "config": name, "batches": len(wls),
+            "attention_mixed_ms": round(acc["mixed_ms"], 4),
+            "attention_mixed_frac_of_roofline": round(t_roof_mixed / acc["mixed_ms"], 4),
+            "append_ms": round(acc["append_ms"], 4),
+            "append_gbs": round(acc["append_bytes"] / (acc["append_ms"] / 1e3) / 1e9, 1),
+            "decode_only_ms": round(acc["decode_only_ms"], 4),
+            "decode_only_gbs": round(dec_gbs, 1) if dec_gbs else None,
+            "decode_only_hbm_frac": round(dec_gbs / hbm, 4) if dec_gbs else None,
+            "chunk_only_ms": round(acc["chunk_only_ms"], 4),
+            "chunk_only_tflops": round(chk_tf, 1) if chk_tf else None,
+            "chunk_only_tensor_frac": round(chk_tf / tf, 4) if chk_tf else None,
+            "mixed_vs_sum_of_parts": round(acc["mixed_ms"] / (acc["decode_only_ms"] + acc["chunk_only_ms"]), 4),
+        })
+    line = {"split": "attention call per workload: mixed, decode rows only, prefill chunks only",
+            "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"], "source": peak_src,
+                      "note": "each call timed alone, back to back: the burst tensor peak applies"},
+            "reps": reps, "configs": out}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -607,6 +725,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--timeline", action="store_true",
                     help="step-latency timeline around a long prompt's arrival (one JSON line)")
+    ap.add_argument("--split", action="store_true",
+                    help="decode-only / chunk-only / mixed attention timings per workload (one JSON line)")
+    ap.add_argument("--split-configs", nargs="+", default=SPLIT_CONFIGS, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--split-reps", type=int, default=20)
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     world, rank, local = dist_env()
@@ -616,6 +738,10 @@ def main(argv=None):
     if args.timeline:
         if rank == 0:
             run_timeline(args, local)
+        return
+    if args.split:
+        if rank == 0:
+            run_split(args, local)
         return
     run_ours(args, world, rank, local)
 
