@@ -1049,7 +1049,7 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
           ok = false;
           break;
         }
-        const ChItem it = bars->items[slot];
+        const ChItem& it = bars->items[slot];  // stable until this role arrives on item_empty
         if (it.row < 0) break;
         if (it.nkt[t] > 0 && !mbar_wait(&bars->q_full, n & 1, abort_flag)) {
           ok = false;
@@ -1100,7 +1100,7 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
           ok = false;
           break;
         }
-        const ChItem it = bars->items[slot];
+        const ChItem& it = bars->items[slot];  // stable until this role arrives on item_empty
         if (it.row < 0) break;
         const int kv_max = max(it.kv_end[0], it.kv_end[1]);
         for (int j = 0; j < it.n_kt && ok; ++j) {
@@ -1169,7 +1169,7 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
         ok = false;
         break;
       }
-      const ChItem it = bars->items[slot];
+      const ChItem& it = bars->items[slot];  // stable until this role arrives on item_empty
       if (it.row < 0) break;
       const int nkt = it.nkt[t];
       if (nkt > 0) {
@@ -1222,6 +1222,16 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
           }
           l = l * alpha + ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3]));
           m_use = m_new;
+          // P (bf16 pairs) over the first 32 columns of the S values it came from.
+          // Packing before the rescale keeps 32 registers live through it instead of
+          // 64, and the store runs while O is rescaled.
+          uint32_t pw[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * j], sv[2 * j + 1]);
+            pw[j] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          tmem_st32u(ts, pw);
           if (kt > 0 && __any_sync(0xffffffffu, grow)) {  // rescale this row's O
             // the PV MMA of the previous tile must be done with O first
             if (!warp_wait(&bars->o_done[t][(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag)) {
@@ -1235,21 +1245,11 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
               tmem_ld32(tO + cc * 32, rr);
               tmem_wait_ld();
               reg_fence32(rr);
-              float o[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(rr[j]) * alpha;
-              tmem_st32(tO + cc * 32, o);
+              for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+              tmem_st32u(tO + cc * 32, rr);
             }
-            tmem_wait_st();
           }
-          // P (bf16 pairs) over the first 32 columns of the S values it came from
-          uint32_t pw[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * j], sv[2 * j + 1]);
-            pw[j] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          tmem_st32u(ts, pw);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bars->p_full[t][b]);
