@@ -1039,9 +1039,18 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
     // the tiles its Q tile needs.  It waits for each stage to be full even
     // when it has no MMA for it: that keeps its commits in step with the
     // producer, so a phase can never complete on commits meant for a later one.
+    // The issue loops keep every per-item value in registers, step through the
+    // stage rings with counters, and build each operand descriptor once per tile:
+    // a k-step or a stage only moves the descriptor's start-address field
+    // (bytes >> 4, 14 bits, no carry below 256 KB) by a constant.
     const int t = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      const uint32_t sq = sbase + C::Q_OFF + t * C::Q_BYTES;
+      const uint64_t qdesc = smem_desc_sw128(sbase + C::Q_OFF + t * C::Q_BYTES, 16, 1024);
+      const uint64_t kdesc0 = smem_desc_sw128(sbase + C::KV_OFF, 16, 1024);
+      const uint32_t s_tm = tmem + C::S_COL + 2 * t * 64;
+      constexpr uint32_t idesc_full = idesc_bf16_f32(128, kKeys, 0);
+      int bk = 0;        // K stage of the next tile
+      uint32_t kph = 0;  // its phase parity
       bool ok = true;
       for (int n = 0; ok; ++n) {
         const int slot = n & 1;
@@ -1050,36 +1059,45 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
           break;
         }
         const ChItem& it = bars->items[slot];  // stable until this role arrives on item_empty
-        if (it.row < 0) break;
-        if (it.nkt[t] > 0 && !mbar_wait(&bars->q_full, n & 1, abort_flag)) {
+        const int row = it.row;
+        if (row < 0) break;
+        const int nkt = it.nkt[t], t0 = it.t0[t], n_kt = it.n_kt;
+        const int kv_max = max(it.kv_end[0], it.kv_end[1]);
+        if (nkt > 0 && !mbar_wait(&bars->q_full, n & 1, abort_flag)) {
           ok = false;
           break;
         }
-        const int kv_max = max(it.kv_end[0], it.kv_end[1]);
-        for (int kt = 0; kt < it.n_kt; ++kt) {
-          const int g = it.kv0 + kt, bk = g % KVS;
-          if (!mbar_wait(&bars->k_full[bk], (g / KVS) & 1, abort_flag)) {
+        for (int kt = 0; kt < n_kt; ++kt) {
+          if (!mbar_wait(&bars->k_full[bk], kph, abort_flag)) {
             ok = false;
             break;
           }
-          if (kt < it.nkt[t]) {
-            const int gt = it.t0[t] + kt, b = gt & 1;
+          if (kt < nkt) {
+            const int gt = t0 + kt, b = gt & 1;
             // S buffer b last held P of the group's tile gt - 2: its PV MMA must be done
             if (gt >= 2 && !mbar_wait(&bars->o_done[t][b], ((gt - 2) >> 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const int keys = min(kKeys, kv_max - kt * kKeys);
-            const uint32_t idesc_s = idesc_bf16_f32(128, (keys + 15) & ~15, 0);
+            const int keys = kv_max - kt * kKeys;  // at least kKeys but on the last tile
+            const uint32_t idesc_s = keys >= kKeys ? idesc_full : idesc_bf16_f32(128, (keys + 15) & ~15, 0);
+            const uint64_t kd = kdesc0 + static_cast<uint64_t>((bk * 2 * NSL * kKVSlab) >> 4);
+            const uint32_t dcol = s_tm + b * 64;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_bf16_ss(s_col(t, b), kmajor_desc(sq, kk, kQSlab), kmajor_desc(sbase + k_off(bk), kk, kKVSlab),
-                          idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t qo = static_cast<uint64_t>(((kk >> 2) * kQSlab + (kk & 3) * 32) >> 4);
+              const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * kKVSlab + (kk & 3) * 32) >> 4);
+              mma_bf16_ss(dcol, qdesc + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
+            }
             mma_commit(&bars->s_full[t][b]);
           }
           mma_commit(&bars->k_empty[bk]);
-          if (kt == it.n_kt - 1) mma_commit(&bars->q_empty);
+          if (kt == n_kt - 1) mma_commit(&bars->q_empty);
+          if (++bk == KVS) {
+            bk = 0;
+            kph ^= 1u;
+          }
         }
         if (!ok) break;
         mbar_arrive(&bars->item_empty[slot]);
@@ -1093,6 +1111,12 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
     // ---------------------------------------------------------------- PV issuer of both groups
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
+      // V is the MN-major B operand: 64-column slabs one slab apart (LBO), 8-key row
+      // groups 1024 B apart (SBO), 16 keys = 2048 B per k-step.  P (A operand) is in
+      // TMEM: 16 keys = 8 packed columns per k-step.
+      const uint64_t vdesc0 = smem_desc_sw128(sbase + C::KV_OFF + NSL * kKVSlab, kKVSlab, 1024);
+      int bv = 0;        // V stage of the next tile
+      uint32_t vph = 0;  // its phase parity
       bool ok = true;
       for (int n = 0; ok; ++n) {
         const int slot = n & 1;
@@ -1101,47 +1125,61 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
           break;
         }
         const ChItem& it = bars->items[slot];  // stable until this role arrives on item_empty
-        if (it.row < 0) break;
-        const int kv_max = max(it.kv_end[0], it.kv_end[1]);
-        for (int j = 0; j < it.n_kt && ok; ++j) {
-          const int gj = it.kv0 + j, bv = gj % KVS;
-          if (!mbar_wait(&bars->v_full[bv], (gj / KVS) & 1, abort_flag)) {
+        const int row = it.row;
+        if (row < 0) break;
+        const int n_kt = it.n_kt;
+        const int nkt_[2] = {it.nkt[0], it.nkt[1]}, t0_[2] = {it.t0[0], it.t0[1]};
+        const int ke_[2] = {it.kv_end[0], it.kv_end[1]};
+        const int kv_max = max(ke_[0], ke_[1]);
+        for (int j = 0; j < n_kt && ok; ++j) {
+          if (!mbar_wait(&bars->v_full[bv], vph, abort_flag)) {
             ok = false;
             break;
           }
           const int keys = min(kKeys, kv_max - j * kKeys);  // keys loaded in this tile
-          const int nk = (keys + 15) >> 4;
-          if (keys != nk * 16) {
+          if ((keys & 15) != 0) {
             // rows past the context in the last page may hold stale (even non-finite)
             // data: zero them in V so that P = 0 times V stays 0
             uint8_t* v0 = smem + v_off(bv);
-            for (int r = keys; r < nk * 16; ++r)
+            for (int r = keys; r < ((keys + 15) & ~15); ++r)
               for (int s = 0; s < NSL; ++s)
                 for (int q16 = 0; q16 < 8; ++q16)
                   *reinterpret_cast<uint4*>(v0 + s * kKVSlab + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
           }
-          const uint32_t vbase = sbase + v_off(bv);
+          const uint64_t vd = vdesc0 + static_cast<uint64_t>((bv * 2 * NSL * kKVSlab) >> 4);
+#pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (j >= it.nkt[t]) continue;
-            const int gt = it.t0[t] + j, b = gt & 1;
-            if (!mbar_wait(&bars->p_full[t][b], (gt >> 1) & 1, abort_flag)) {
-              ok = false;
-              break;
+            if (j < nkt_[t]) {
+              const int gt = t0_[t] + j, b = gt & 1;
+              if (!mbar_wait(&bars->p_full[t][b], (gt >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t dcol = tmem + t * C::O_COL;
+              const uint32_t acol = s_col(t, b);
+              const int kr = ke_[t] - j * kKeys;  // keys this Q tile sees in the tile
+              if (kr >= kKeys) {
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk)
+                  mma_bf16_ts(dcol, acol + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+              } else {
+                const int nk_t = (kr + 15) >> 4;
+                for (int kk = 0; kk < nk_t; ++kk)
+                  mma_bf16_ts(dcol, acol + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(&bars->o_done[t][b]);
             }
-            tc_fence_after();
-            const int nk_t = (min(kKeys, it.kv_end[t] - j * kKeys) + 15) >> 4;  // key steps this Q tile sees
-            for (int kk = 0; kk < nk_t; ++kk) {
-              // P (A operand) from TMEM: 16 keys = 8 packed columns per k-step.  V is the
-              // MN-major B operand: 64-column slabs one slab apart (LBO), 8-key row groups
-              // 1024 B apart (SBO), 16 keys = 2048 B per k-step
-              const uint64_t vdesc = smem_desc_sw128(vbase + kk * 2048, kKVSlab, 1024);
-              mma_bf16_ts(tmem + t * C::O_COL, s_col(t, b) + kk * 8, vdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&bars->o_done[t][b]);
           }
           if (!ok) break;
           mma_commit(&bars->v_empty[bv]);
+          if (++bv == KVS) {
+            bv = 0;
+            vph ^= 1u;
+          }
         }
         if (!ok) break;
         mbar_arrive(&bars->item_empty[slot]);
