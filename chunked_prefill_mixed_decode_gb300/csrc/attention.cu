@@ -527,8 +527,10 @@ __device__ __forceinline__ void merge_splits(const AttnParams& p, int k, int h0,
 // not fit here: its M is at least 64 rows and one thread issues an MMA only
 // every 110-140 cycles, while a decode page is 16 rows per warp.
 
+// Out of line, as is chunk_phase: each phase gets its own register allocation
+// (inlined into one kernel body the two spill).
 template <int D, int G>
-__device__ __forceinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem, const CUtensorMap* tm_k,
+__device__ __noinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem, const CUtensorMap* tm_k,
                                              const CUtensorMap* tm_v) {
   using C = DecCfg<D, G>;
   constexpr int NST = C::NST;
@@ -845,7 +847,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // overlap the other group's MMAs.  Returns when the chunk queue is empty; the
 // caller owns TMEM and the barrier invalidation.
 template <int D, int G>
-__device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtensorMap* tm_k_p,
+__device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtensorMap* tm_k_p,
                                             const CUtensorMap* tm_v_p, const AttnParams& p, uint8_t* smem,
                                             uint32_t tmem) {
   using C = ChCfg<D>;
@@ -1242,23 +1244,33 @@ __device__ __forceinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUt
             for (int j = 0; j < 64; ++j)
               if (key0 + j > pos) sv[j] = -INFINITY;
           }
-          float mxa[4] = {sv[0], sv[1], sv[2], sv[3]};
+          // row max: four chains of three-input maxima
+          float mxa[4];
 #pragma unroll
-          for (int j = 4; j < 64; ++j) mxa[j & 3] = fmaxf(mxa[j & 3], sv[j]);
+          for (int c = 0; c < 4; ++c) {
+            float m = fmax3(sv[c], sv[c + 4], sv[c + 8]);
+#pragma unroll
+            for (int j = 12; j < 60; j += 8) m = fmax3(m, sv[j + c], sv[j + 4 + c]);
+            mxa[c] = fmaxf(m, sv[60 + c]);
+          }
           const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
           const float mx_s = mx * sl2;
           const bool grow = mx_s > m_use + kRescaleLog2;
           const float m_new = grow ? mx_s : m_use;
           const float alpha = grow ? ex2(m_use - m_new) : 1.f;
           const float neg_m = -m_new;
-          float rsa[4] = {0.f, 0.f, 0.f, 0.f};
+          // exponentials, two elements per packed FMA and packed add
+          const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
+          float2 rsa[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const float e = ex2(fmaf(sv[j], sl2, neg_m));
-            sv[j] = e;
-            rsa[j & 3] += e;
+          for (int j = 0; j < 64; j += 2) {
+            const float2 x = ffma2(make_float2(sv[j], sv[j + 1]), sl2x2, negm2);
+            const float2 e = make_float2(ex2(x.x), ex2(x.y));
+            sv[j] = e.x;
+            sv[j + 1] = e.y;
+            rsa[(j >> 1) & 1] = fadd2(rsa[(j >> 1) & 1], e);
           }
-          l = l * alpha + ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3]));
+          l = l * alpha + ((rsa[0].x + rsa[0].y) + (rsa[1].x + rsa[1].y));
           m_use = m_new;
           // P (bf16 pairs) over the first 32 columns of the S values it came from.
           // Packing before the rescale keeps 32 registers live through it instead of
