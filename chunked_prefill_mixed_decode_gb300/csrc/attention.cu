@@ -1070,14 +1070,14 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
           break;
         }
         for (int kt = 0; kt < n_kt; ++kt) {
-          if (!mbar_wait(&bars->k_full[bk], kph, abort_flag)) {
+          if (!mbar_wait_fast(&bars->k_full[bk], kph, abort_flag, 16)) {
             ok = false;
             break;
           }
           if (kt < nkt) {
             const int gt = t0 + kt, b = gt & 1;
             // S buffer b last held P of the group's tile gt - 2: its PV MMA must be done
-            if (gt >= 2 && !mbar_wait(&bars->o_done[t][b], ((gt - 2) >> 1) & 1, abort_flag)) {
+            if (gt >= 2 && !mbar_wait_fast(&bars->o_done[t][b], ((gt - 2) >> 1) & 1, abort_flag, 16)) {
               ok = false;
               break;
             }
@@ -1134,7 +1134,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
         const int ke_[2] = {it.kv_end[0], it.kv_end[1]};
         const int kv_max = max(ke_[0], ke_[1]);
         for (int j = 0; j < n_kt && ok; ++j) {
-          if (!mbar_wait(&bars->v_full[bv], vph, abort_flag)) {
+          if (!mbar_wait_fast(&bars->v_full[bv], vph, abort_flag, 16)) {
             ok = false;
             break;
           }
@@ -1154,7 +1154,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
           for (int t = 0; t < 2; ++t) {
             if (j < nkt_[t]) {
               const int gt = t0_[t] + j, b = gt & 1;
-              if (!mbar_wait(&bars->p_full[t][b], (gt >> 1) & 1, abort_flag)) {
+              if (!mbar_wait_fast(&bars->p_full[t][b], (gt >> 1) & 1, abort_flag, 16)) {
                 ok = false;
                 break;
               }
