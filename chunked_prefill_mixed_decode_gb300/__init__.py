@@ -169,47 +169,77 @@ def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndar
     and the batch summary.
     """
     n = len(states)
-    tables = [np.ascontiguousarray(bt, dtype=np.int32) for bt in block_tables]
-    reqs = (Request * max(n, 1))()
-    for i, ((c, rem), bt) in enumerate(zip(states, tables)):
-        reqs[i].cached_len = int(c)
-        reqs[i].remaining_prompt = int(rem)
-        reqs[i].block_table = _i32(bt) if len(bt) else None
-        reqs[i].num_pages = len(bt)
+    reqs, keep = _request_array(states, block_tables)
+    lens = reqs["num_pages"][:n]
     cfg = SchedConfig(int(token_budget), int(max_chunk_per_request), int(policy), int(min_chunk_per_request),
                       int(prefill_quota), int(decode_share_permille))
     cap_rows = max(n, 1)
     cap_tokens = max(int(token_budget), 1)
-    max_pages = max([len(bt) for bt in tables] + [1])
+    max_pages = max(int(lens.max()) if n else 0, 1)
     cap_bt = cap_rows * max_pages
-    out = {k: np.zeros(sz, dtype=np.int32) for k, sz in (
-        ("cu_seqlens_q", cap_rows + 1), ("q_start_pos", cap_rows), ("context_lens", cap_rows),
-        ("positions", cap_tokens), ("slot_mapping", cap_tokens), ("block_tables", cap_bt),
-        ("row_req", cap_rows), ("num_scheduled", max(n, 1)))}
+    # one output buffer; the returned arrays are views of it
+    sizes = (("cu_seqlens_q", cap_rows + 1), ("q_start_pos", cap_rows), ("context_lens", cap_rows),
+             ("positions", cap_tokens), ("slot_mapping", cap_tokens), ("block_tables", cap_bt),
+             ("row_req", cap_rows), ("num_scheduled", max(n, 1)))
+    buf = np.zeros(sum(sz for _, sz in sizes), dtype=np.int32)
+    out, off = {}, 0
+    for k, sz in sizes:
+        out[k] = buf[off:off + sz]
+        off += sz
     info = BatchInfo()
-    rc = lib().ms_build_batch_metadata(reqs, n, ctypes.byref(cfg), cap_rows, cap_tokens, cap_bt,
-                                       _i32(out["cu_seqlens_q"]), _i32(out["q_start_pos"]),
+    rc = lib().ms_build_batch_metadata(reqs.ctypes.data_as(ctypes.POINTER(Request)), n, ctypes.byref(cfg), cap_rows,
+                                       cap_tokens, cap_bt, _i32(out["cu_seqlens_q"]), _i32(out["q_start_pos"]),
                                        _i32(out["context_lens"]), _i32(out["positions"]),
                                        _i32(out["slot_mapping"]), _i32(out["block_tables"]), _i32(out["row_req"]),
                                        _i32(out["num_scheduled"]), ctypes.byref(info))
+    del keep
     _check(rc, "ms_build_batch_metadata")
     S, T, stride = info.num_rows, info.num_tokens, info.bt_stride
     return {
-        "cu_seqlens_q": out["cu_seqlens_q"][: S + 1].copy(),
-        "q_start_pos": out["q_start_pos"][:S].copy(),
-        "context_lens": out["context_lens"][:S].copy(),
-        "positions": out["positions"][:T].copy(),
-        "slot_mapping": out["slot_mapping"][:T].copy(),
-        "block_tables": out["block_tables"][: S * stride].reshape(S, stride).copy(),
+        "cu_seqlens_q": out["cu_seqlens_q"][: S + 1],
+        "q_start_pos": out["q_start_pos"][:S],
+        "context_lens": out["context_lens"][:S],
+        "positions": out["positions"][:T],
+        "slot_mapping": out["slot_mapping"][:T],
+        "block_tables": out["block_tables"][: S * stride].reshape(S, stride),
         "bt_stride": stride,
-        "row_req": out["row_req"][:S].copy(),
-        "num_scheduled": out["num_scheduled"][:n].copy(),
+        "row_req": out["row_req"][:S],
+        "num_scheduled": out["num_scheduled"][:n],
         "num_rows": S,
         "num_decodes": info.num_decodes,
         "num_tokens": T,
         "unused_tokens": info.unused_tokens,
         "num_deferred": info.num_deferred,
     }
+
+
+# ms_request as a numpy record: filled column by column instead of request by request
+_REQ_DTYPE = np.dtype({"names": ["cached_len", "remaining_prompt", "block_table", "num_pages"],
+                       "formats": ["<i4", "<i4", "<u8", "<i4"], "offsets": [0, 4, 8, 16],
+                       "itemsize": ctypes.sizeof(Request)})
+
+
+def _request_array(states, block_tables):
+    """ms_request records for the requests; also returns the concatenated block
+    tables, which must stay alive while the records are in use."""
+    n = len(states)
+    if n != len(block_tables):
+        raise ValueError("one block table per request")
+    reqs = np.zeros(max(n, 1), dtype=_REQ_DTYPE)
+    if n == 0:
+        return reqs, None
+    st = np.asarray(states, dtype=np.int64).reshape(n, 2)
+    lens = np.fromiter((len(bt) for bt in block_tables), dtype=np.int64, count=n)
+    if (st < np.iinfo(np.int32).min).any() or (st > np.iinfo(np.int32).max).any():
+        raise ValueError("request lengths out of int32 range")
+    flat = np.ascontiguousarray(np.concatenate([np.asarray(bt).reshape(-1) for bt in block_tables]), dtype=np.int32) \
+        if lens.sum() else np.zeros(1, dtype=np.int32)
+    starts = np.concatenate(([0], np.cumsum(lens)[:-1]))
+    reqs["cached_len"][:n] = st[:, 0]
+    reqs["remaining_prompt"][:n] = st[:, 1]
+    reqs["num_pages"][:n] = lens
+    reqs["block_table"][:n] = np.where(lens > 0, flat.ctypes.data + 4 * starts, 0).astype(np.uint64)
+    return reqs, flat
 
 
 class Engine:
@@ -258,10 +288,14 @@ class Engine:
         cap_rows = max(st["num_live"], 1)
         cap_tokens = max(self.token_budget, 1)
         cap_bt = cap_rows * max(st["max_request_pages"], 1)
-        out = {k: np.zeros(sz, dtype=np.int32) for k, sz in (
-            ("cu_seqlens_q", cap_rows + 1), ("q_start_pos", cap_rows), ("context_lens", cap_rows),
-            ("positions", cap_tokens), ("slot_mapping", cap_tokens), ("block_tables", cap_bt),
-            ("row_request_id", cap_rows))}
+        sizes = (("cu_seqlens_q", cap_rows + 1), ("q_start_pos", cap_rows), ("context_lens", cap_rows),
+                 ("positions", cap_tokens), ("slot_mapping", cap_tokens), ("block_tables", cap_bt),
+                 ("row_request_id", cap_rows))
+        buf = np.zeros(sum(sz for _, sz in sizes), dtype=np.int32)  # the returned arrays are views of it
+        out, off = {}, 0
+        for k, sz in sizes:
+            out[k] = buf[off:off + sz]
+            off += sz
         info = BatchInfo()
         rc = lib().ms_engine_plan(self._h, cap_rows, cap_tokens, cap_bt, _i32(out["cu_seqlens_q"]),
                                   _i32(out["q_start_pos"]), _i32(out["context_lens"]), _i32(out["positions"]),
@@ -270,14 +304,14 @@ class Engine:
         _check(rc, "ms_engine_plan")
         S, T, stride = info.num_rows, info.num_tokens, info.bt_stride
         return {
-            "cu_seqlens_q": out["cu_seqlens_q"][: S + 1].copy(),
-            "q_start_pos": out["q_start_pos"][:S].copy(),
-            "context_lens": out["context_lens"][:S].copy(),
-            "positions": out["positions"][:T].copy(),
-            "slot_mapping": out["slot_mapping"][:T].copy(),
-            "block_tables": out["block_tables"][: S * stride].reshape(S, stride).copy(),
+            "cu_seqlens_q": out["cu_seqlens_q"][: S + 1],
+            "q_start_pos": out["q_start_pos"][:S],
+            "context_lens": out["context_lens"][:S],
+            "positions": out["positions"][:T],
+            "slot_mapping": out["slot_mapping"][:T],
+            "block_tables": out["block_tables"][: S * stride].reshape(S, stride),
             "bt_stride": stride,
-            "row_request_id": out["row_request_id"][:S].copy(),
+            "row_request_id": out["row_request_id"][:S],
             "num_rows": S,
             "num_decodes": info.num_decodes,
             "num_tokens": T,
