@@ -278,3 +278,34 @@ def test_graph_config_errors(ms):
     bufs = ms.GraphBuffers()
     assert ms.lib().ms_graph_create(ctypes.byref(ok), ctypes.byref(bufs), None, ctypes.byref(h)) == ms.MS_ERR_ARG
     assert ms.lib().ms_graph_destroy(None) == ms.MS_OK
+
+
+def test_request_marshalling_edge_cases(ms):
+    """The binding packs requests column by column: tables of any integer dtype
+    and layout, empty tables, empty rounds, and bad lengths behave as the
+    oracle and the header say."""
+    rng = np.random.default_rng(17)
+    states = [(0, 5), (16, 0), (3, 0), (0, 0)]
+    tables = [rng.permutation(8).astype(np.int64)[:1],       # int64 input, cast to int32
+              np.arange(40, 42, dtype=np.int32)[::-1].copy(),
+              np.asarray([7]),                              # platform int
+              np.zeros(0, dtype=np.int32)]                  # empty table, no tokens scheduled
+    ref_rows, _ = oracle.schedule(states[:3], 16)
+    ref = oracle.batch_metadata(ref_rows, [np.asarray(t, dtype=np.int32) for t in tables[:3]], 3)
+    got = ms.build_batch_metadata(states[:3], tables[:3], 16)
+    for k in ("cu_seqlens_q", "q_start_pos", "context_lens", "positions", "slot_mapping"):
+        np.testing.assert_array_equal(got[k], ref[k])
+    np.testing.assert_array_equal(got["block_tables"], ref["block_tables"])
+    # the returned arrays are views of one fresh buffer per call: two calls share nothing
+    again = ms.build_batch_metadata(states[:3], tables[:3], 16)
+    again["positions"][:] = -1
+    np.testing.assert_array_equal(got["positions"], ref["positions"])
+    # an empty round
+    empty = ms.build_batch_metadata([], [], 8)
+    assert empty["num_rows"] == 0 and empty["num_tokens"] == 0
+    # one table per request
+    with pytest.raises(ValueError):
+        ms.build_batch_metadata(states[:2], tables[:1], 16)
+    # lengths beyond int32
+    with pytest.raises(ValueError):
+        ms.build_batch_metadata([(2 ** 31, 0)], [tables[1]], 16)
