@@ -360,9 +360,10 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
     hdr[H_SPLIT] = static_cast<int32_t>(split);
   }
   // 7. starting split of the SMs between chunk tiles and decode pages.  Chunk
-  // time falls as 1/n with n chunk CTAs; decode time is bytes over the
-  // bandwidth of the other SMs, capped by HBM.  Take the balance point, or,
-  // while decode stays HBM-bound, as many chunk CTAs as keep it so.
+  // time falls as 1/n with n chunk CTAs, in whole items; decode time is bytes
+  // over the bandwidth of the other SMs, capped by HBM.  Take the best split
+  // near the balance point, or, while decode stays HBM-bound, as many chunk
+  // CTAs as keep it so.
   if (tid == 0) {
     const float S = static_cast<float>(p.num_sms);
     const float T = static_cast<float>(s_tiles) * kChunkTileNs;                     // SM-ns of chunk work
@@ -376,8 +377,26 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
       n = S;
     else if (T * kHbmGBs <= B * n_hbm)  // chunk done within the HBM-bound decode time
       n = n_hbm;
-    else
-      n = fminf(S - 1.f, fmaxf(1.f, rintf(__fdividef(T * g * S, B + T * g))));
+    else {
+      // Balance point, then the nearby CTA count that minimizes the step: chunk work
+      // comes in whole items, so n chunk CTAs need ceil(items / n) rounds of about
+      // T / items each; decode runs on the other CTAs, capped by HBM.
+      const float n0 = fminf(S - 1.f, fmaxf(1.f, rintf(__fdividef(T * g * S, B + T * g))));
+      const float n_it = fmaxf(static_cast<float>(hdr[H_NCH_ITEMS]), 1.f);
+      const float t_item = T / n_it;
+      float best = 3.0e38f;
+      n = n0;
+      const int k_lo = max(1, static_cast<int>(n0) - 16), k_hi = min(static_cast<int>(S) - 1, static_cast<int>(n0) + 16);
+      for (int k = k_lo; k <= k_hi; ++k) {
+        const float tc = ceilf(n_it / k) * t_item;
+        const float td = B / fminf((S - k) * g, kHbmGBs);
+        const float tt = fmaxf(tc, td);
+        if (tt < best) {
+          best = tt;
+          n = static_cast<float>(k);
+        }
+      }
+    }
     hdr[H_CHUNK_CTAS] = static_cast<int>(n);
   }
   griddep_wait();
@@ -817,13 +836,6 @@ static_assert(DecCfg<128, 8>::SMEM <= 232448 && DecCfg<64, 8>::SMEM <= 232448 &&
 static_assert(ChCfg<128>::SMEM <= 232448 && ChCfg<64>::SMEM <= 232448,
               "chunk phase exceeds the per-CTA shared-memory limit");
 static_assert(ChCfg<128>::KVS <= 8 && ChCfg<64>::KVS <= 8, "more K/V stages than barriers");
-
-// K-major, 128-byte-swizzled operand: slab-major 64-column blocks of 128-byte
-// rows, slab_bytes apart; k-step kk (16 columns) lives in slab kk / 4 at byte
-// offset (kk % 4) * 32.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, int slab_bytes) {
-  return smem_desc_sw128(base + (kk >> 2) * slab_bytes + (kk & 3) * 32, 16, 1024);
-}
 
 // wait by lane 0, result and ordering shared with the whole warp
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
