@@ -462,6 +462,7 @@ struct DecItem {
   int tok;     // packed token index of the row's query
   int part;    // partial record of query head hk * G (+ g for the others)
   int ns;      // splits of the row
+  int w0;      // lane j: page id of the item's page j (its first window of 32 pages)
 };
 
 __device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, int split) {
@@ -479,6 +480,9 @@ __device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, i
   it.np = min(split, n_pages - it.p0);
   it.part = __ldg(p.dec_part_base + k) + sp * p.H_q + it.hk * p.G;
   it.ns = __ldg(p.dec_nsplit + k);
+  // the first window of page ids, loaded while the item waits its turn
+  const int lane = threadIdx.x & 31;
+  it.w0 = lane < it.np ? __ldg(p.bt + static_cast<int64_t>(it.row) * p.bt_stride + it.p0 + lane) : 0;
   return it;
 }
 
@@ -543,8 +547,8 @@ __device__ __forceinline__ void merge_splits(const AttnParams& p, int k, int h0,
 // independent, with its own ring of page stages, pulling decode items until
 // the queue is empty.  Per page it runs mma.sync m16n8k16 on ldmatrix
 // fragments: 16 tokens against the G query heads (padded to 8).  tcgen05 does
-// not fit here: its M is at least 64 rows and one thread issues an MMA only
-// every 110-140 cycles, while a decode page is 16 rows per warp.
+// not fit here: its M is at least 64 rows, while a decode page is 16 rows per
+// warp and a row's G query heads fill only part of N.
 
 // Out of line, as is chunk_phase: each phase gets its own register allocation
 // (inlined into one kernel body the two spill).
@@ -586,11 +590,14 @@ __device__ __noinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem, c
   uint32_t item_par = 0;  // q buffer of the current item
   bool failed = false;
 
-  int iss_bt = 0;  // lane j: page id (issue-cursor item, window start + j)
+  // lane j: page id of page (window start + j) of the issue-cursor item, and of the
+  // window after it: page ids come one coalesced load per 32 pages, a window ahead
+  int iss_bt = 0, iss_bt_next = 0;
   auto issue_page = [&](const DecItem& it, int pi, uint32_t qpar) {
-    if ((pi & 31) == 0) {  // one coalesced load per 32 pages of an item
-      const int w = pi + lane;
-      iss_bt = w < it.np ? __ldg(p.bt + static_cast<int64_t>(it.row) * p.bt_stride + it.p0 + w) : 0;
+    if ((pi & 31) == 0) {
+      iss_bt = pi == 0 ? it.w0 : iss_bt_next;
+      const int w = pi + 32 + lane;
+      if (pi + 32 < it.np) iss_bt_next = w < it.np ? __ldg(p.bt + static_cast<int64_t>(it.row) * p.bt_stride + it.p0 + w) : 0;
     }
     int phys = __shfl_sync(0xffffffffu, iss_bt, pi & 31);
     if (lane == 0) {
@@ -849,10 +856,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // Chunk phase.  Warp 0 owns the work queue and streams Q and K/V with TMA (K
 // one tile ahead of V); warps 2-5 and 6-9 are two softmax groups, group t
 // owning Q tile t of the current pair, one query row per thread over 64-key
-// tiles.  One thread issues a tcgen05.mma only about every 110-140 cycles,
-// whatever its N, well below the tensor rate at these shapes, so three
-// warps issue: warp 1 the S MMAs of group 0, warp 10 those of group 1, and
-// warp 11 the PV MMAs of both.  Each group has two S buffers in
+// tiles.  The S MMAs of the two groups and the PV MMAs are three independent
+// streams, so three warps issue them: warp 1 the S MMAs of group 0, warp 10
+// those of group 1, and warp 11 the PV MMAs of both (one issuer would queue
+// one group's PV behind the other's S).  Each group has two S buffers in
 // TMEM, so its next S is computed while it exponentiates the current one, and
 // P (bf16) overwrites the S values it came from, where the PV MMA reads it.
 // The two groups run a tile apart at most, so one group's exponentials
