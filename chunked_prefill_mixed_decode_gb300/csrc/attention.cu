@@ -17,14 +17,14 @@
 //     O^T += V^T P^T run as mma.sync m16n8k16 on ldmatrix fragments, with P
 //     transposed in registers.  Each item leaves a partial (max, sum,
 //     accumulator); the last split of a (row, KV head) to finish merges them.
-//   chunk rows (d > 1): tcgen05 tensor cores.  A CTA owns a 128-row query
-//     tile (128/G tokens x G heads of one KV head) and walks 128-key tiles of
-//     the prefix and its own chunk.  TMA loads Q and K/V pages (one 16-row box
-//     per page and 64-column slab, 128-byte swizzle); S = Q K^T lands in TMEM;
-//     eight softmax warps (two per TMEM lane quadrant, each taking half of the
-//     128 key columns) write P (bf16) back into TMEM, and O += P V runs with P
-//     as the TMEM operand, accumulating in TMEM and rescaled only when a row's
-//     maximum grows by more than a factor 2^8.
+//   chunk rows (d > 1): tcgen05 tensor cores.  A work item is a pair of
+//     128-row query tiles (128/G tokens x G heads of one KV head each) that
+//     walk 64-key tiles of the prefix and their own chunk together.  TMA loads
+//     Q and K/V pages (one 16-row box per page and 64-column slab, 128-byte
+//     swizzle); S = Q K^T lands in TMEM; two groups of four softmax warps, one
+//     per query tile and one row per thread, write P (bf16) back over S, and
+//     O += P V runs with P as the TMEM operand, accumulating in TMEM and
+//     rescaled only when a row's maximum grows by more than a factor 2^8.
 //
 // A one-CTA prologue validates the metadata, chooses the split size, orders
 // rows longest-first and decides how many CTAs start on chunk tiles; a second
