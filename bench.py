@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 import types
 
@@ -127,7 +128,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"ms_bench_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def start(self):
         try:
