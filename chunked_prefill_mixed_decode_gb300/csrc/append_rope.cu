@@ -66,6 +66,9 @@ __device__ __forceinline__ void rotate8(const uint4& a, const uint4& b, const fl
   yb = make_uint4(ob[0], ob[1], ob[2], ob[3]);
 }
 
+// Idx: the flat work index type, 32-bit whenever the step's work fits (the
+// divisions by per_row and heads then cost a fraction of 64-bit ones).
+template <typename Idx>
 __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendArgs a) {
   // the attention call that follows may start its launch now; it waits for
   // this kernel before it reads q_rot or the pages
@@ -73,11 +76,11 @@ __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendArgs a) {
   const int half = a.D >> 1;
   const int per_row = half / kVec;                 // threads per (token, head) row
   const int heads = a.H_q + 2 * a.H_kv;
-  const int64_t total = static_cast<int64_t>(a.T) * heads * per_row;
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < total;
-       g += static_cast<int64_t>(gridDim.x) * kThreads) {
+  const Idx total = static_cast<Idx>(a.T) * heads * per_row;
+  for (Idx g = static_cast<Idx>(blockIdx.x) * kThreads + threadIdx.x; g < total;
+       g += static_cast<Idx>(gridDim.x) * kThreads) {
     const int part = static_cast<int>(g % per_row);
-    const int64_t rh = g / per_row;
+    const Idx rh = g / per_row;
     const int h = static_cast<int>(rh % heads);
     const int t = static_cast<int>(rh / heads);
     const int i0 = part * kVec;
@@ -179,6 +182,11 @@ extern "C" MS_API int ms_kv_append_rope(const void* q, const void* k, const void
   const int64_t work = static_cast<int64_t>(T) * (H_q + 2 * H_kv) * (D / 2 / kVec);
   int64_t blocks = (work + kThreads - 1) / kThreads;
   if (blocks > 152 * 16) blocks = 152 * 16;  // grid-stride beyond 16 blocks per SM
-  append_rope_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  if (work + static_cast<int64_t>(blocks) * kThreads < (int64_t{1} << 31))
+    append_rope_kernel<uint32_t>
+        <<<static_cast<unsigned>(blocks), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  else
+    append_rope_kernel<int64_t>
+        <<<static_cast<unsigned>(blocks), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? MS_OK : MS_ERR_CUDA;
 }
