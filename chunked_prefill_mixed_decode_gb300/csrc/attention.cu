@@ -29,8 +29,8 @@
 // A one-CTA prologue validates the metadata, chooses the split size, orders
 // rows longest-first and decides how many CTAs start on chunk tiles; a second
 // small kernel expands the per-row item counts into flat item tables.  One
-// persistent kernel (a CTA per SM) then runs both queues: CTAs below the split
-// start on chunk tiles, the rest on decode items, and each moves to the other
+// persistent kernel (a CTA per SM) then runs both queues: CTAs on SMs below the
+// split start on chunk tiles, the rest on decode items, and each moves to the other
 // queue when its own runs dry.  Work comes from atomic counters; no CTA waits
 // on another.
 #include <cuda.h>
@@ -1388,7 +1388,7 @@ __device__ __forceinline__ void invalidate_phase_barriers(uint8_t* smem, bool ch
   }
 }
 
-// One persistent CTA per SM.  CTAs below hdr[H_CHUNK_CTAS] start on chunk
+// One persistent CTA per SM.  CTAs on SMs below hdr[H_CHUNK_CTAS] start on chunk
 // tiles (tensor cores), the others on decode items (HBM), so the two kinds of
 // work run side by side; a CTA whose queue runs dry moves to the other queue.
 template <int D, int G>
@@ -1423,7 +1423,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, ChCfg<D>::TMEM_COLS);
     return;
   }
-  const bool chunk_first = static_cast<int>(blockIdx.x) < p.hdr[H_CHUNK_CTAS];
+  // Which CTAs start on chunk work goes by the SM they run on, not by block
+  // index: as a programmatic dependent, the kernel's blocks reach SMs in an
+  // order set by the kernels still draining, and a split by block index then
+  // lands differently from step to step (up to 6 % slower on the long bimodal
+  // step).  It only sets where a CTA starts; any count of chunk-first CTAs is
+  // correct, since a CTA whose queue runs dry takes the other one.
+  uint32_t smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  const bool chunk_first = static_cast<int>(smid) < p.hdr[H_CHUNK_CTAS];
   for (int ph = 0; ph < 2; ++ph) {
     const bool chunk = (ph == 0) == chunk_first;
     if (chunk && n_ch_items > 0) {
