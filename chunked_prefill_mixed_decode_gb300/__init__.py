@@ -340,8 +340,14 @@ class StepGraph:
                  stream, scale: float = None):
         import torch
         self._h = None
+        if k_cache.dim() != 4 or cos.dim() != 2:
+            raise ValueError("k_cache must be [pages, H_kv, 16, D] and cos, sin [max_pos, D/2]")
         dev = k_cache.device
         num_pages, H_kv, _, D = k_cache.shape
+        _pools(k_cache, v_cache, H_kv, D)
+        _dev(cos, "cos", torch.float32, (cos.shape[0], D // 2))
+        _dev(sin, "sin", torch.float32, tuple(cos.shape))
+        _on_one_gpu(k_cache=k_cache, v_cache=v_cache, cos=cos, sin=sin)
         self.buckets = [int(b) for b in buckets]
         B = self.buckets[-1]
         self.stream = stream
@@ -422,17 +428,99 @@ def num_sms() -> int:
 
 # ---------------------------------------------------------------------------- device
 
+def _dev(t, name: str, dtype, shape=None, min_numel: int = 0) -> None:
+    """Check a tensor before its pointer crosses the C ABI, which sees only an
+    address: dtype, dense row-major layout, shape and size."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} must hold at least {min_numel} elements, got {t.numel()}")
+
+
+def _on_one_gpu(**tensors) -> None:
+    """Every tensor on the CUDA device of the first one (None entries are skipped)."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other tensors on {dev}")
+
+
+def _pools(k_cache, v_cache, H_kv: int, D: int) -> None:
+    import torch
+    if k_cache.dim() != 4:
+        raise ValueError(f"k_cache must be [pages, H_kv, {PAGE_SIZE}, D], got {tuple(k_cache.shape)}")
+    _dev(k_cache, "k_cache", torch.bfloat16, (k_cache.shape[0], H_kv, PAGE_SIZE, D))
+    _dev(v_cache, "v_cache", torch.bfloat16, tuple(k_cache.shape))
+
+
 def kv_append_rope(q, k, v, positions, slot_mapping, cos_tab, sin_tab, k_cache, v_cache, q_rot=None,
                    dev_status=None, stream=None) -> None:
     """Rotate q, k at absolute positions; append k, v into the paged pools (ms_kv_append_rope)."""
+    import torch
+    if q.dim() != 3:
+        raise ValueError(f"q must be [T, H_q, D], got {tuple(q.shape)}")
+    if k_cache.dim() != 4:
+        raise ValueError(f"k_cache must be [pages, H_kv, {PAGE_SIZE}, D], got {tuple(k_cache.shape)}")
     T, H_q, D = q.shape
-    H_kv = k.shape[1]
+    H_kv = k_cache.shape[1]
     if q_rot is None:
         q_rot = q
+    _dev(q, "q", torch.bfloat16)
+    _dev(k, "k", torch.bfloat16, (T, H_kv, D))
+    _dev(v, "v", torch.bfloat16, (T, H_kv, D))
+    _dev(q_rot, "q_rot", torch.bfloat16, (T, H_q, D))
+    _dev(positions, "positions", torch.int32, min_numel=T)
+    _dev(slot_mapping, "slot_mapping", torch.int32, min_numel=T)
+    if cos_tab.dim() != 2:
+        raise ValueError("cos_tab must be [max_pos, D/2]")
+    _dev(cos_tab, "cos_tab", torch.float32, (cos_tab.shape[0], D // 2))
+    _dev(sin_tab, "sin_tab", torch.float32, tuple(cos_tab.shape))
+    _pools(k_cache, v_cache, H_kv, D)
+    if dev_status is not None:
+        _dev(dev_status, "dev_status", torch.int32, min_numel=1)
+    _on_one_gpu(q=q, k=k, v=v, q_rot=q_rot, positions=positions, slot_mapping=slot_mapping, cos_tab=cos_tab,
+                sin_tab=sin_tab, k_cache=k_cache, v_cache=v_cache, dev_status=dev_status)
     rc = lib().ms_kv_append_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(slot_mapping), T, _ptr(cos_tab),
                                  _ptr(sin_tab), cos_tab.shape[0], _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
                                  _ptr(q_rot), H_q, H_kv, D, PAGE_SIZE, _ptr(dev_status), _stream(stream))
     _check(rc, "ms_kv_append_rope")
+
+
+def _attention_args(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables, out):
+    """Shapes of an attention call, after checking its tensors."""
+    import torch
+    if q_rot.dim() != 3:
+        raise ValueError("q_rot must be [T, H_q, D]")
+    T, H_q, D = q_rot.shape
+    _dev(q_rot, "q_rot", torch.bfloat16)
+    if k_cache.dim() != 4:
+        raise ValueError(f"k_cache must be [pages, H_kv, {PAGE_SIZE}, D], got {tuple(k_cache.shape)}")
+    H_kv = k_cache.shape[1]
+    _pools(k_cache, v_cache, H_kv, D)
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape[0] < 1:
+        raise ValueError("cu_seqlens_q must be 1-D with rows + 1 entries")
+    S = cu_seqlens_q.shape[0] - 1
+    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _dev(q_start_pos, "q_start_pos", torch.int32, min_numel=S)
+    _dev(context_lens, "context_lens", torch.int32, min_numel=S)
+    stride = block_tables.shape[1] if block_tables.dim() == 2 else block_tables.shape[0] // max(S, 1)
+    _dev(block_tables, "block_tables", torch.int32, min_numel=S * stride)
+    _dev(out, "out", torch.bfloat16, (T, H_q, D))
+    _on_one_gpu(q_rot=q_rot, k_cache=k_cache, v_cache=v_cache, cu_seqlens_q=cu_seqlens_q, q_start_pos=q_start_pos,
+                context_lens=context_lens, block_tables=block_tables, out=out)
+    return T, H_q, D, H_kv, S, stride
 
 
 def mixed_step_attention(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables,
@@ -442,10 +530,10 @@ def mixed_step_attention(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, con
     Metadata arguments are device int32 tensors; ``block_tables`` is [rows, stride].
     ``context_total`` is the host-side sum of context_lens (bounds the workspace).
     """
-    T, H_q, D = q_rot.shape
-    H_kv = k_cache.shape[1]
-    S = cu_seqlens_q.shape[0] - 1
-    stride = block_tables.shape[1] if block_tables.dim() == 2 else block_tables.shape[0] // max(S, 1)
+    T, H_q, D, H_kv, S, stride = _attention_args(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens,
+                                                 block_tables, out)
+    _dev(workspace, "workspace", None)
+    _on_one_gpu(q_rot=q_rot, workspace=workspace)
     if scale is None:
         scale = float(D) ** -0.5
     rc = lib().ms_mixed_step_attention(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
@@ -466,10 +554,12 @@ def mixed_step_attention_noalloc(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_
     share that scratch, so they must not overlap on the GPU.  ``dev_status``
     (device int32, optional) receives this call's status bits.
     """
-    T, H_q, D = q_rot.shape
-    H_kv = k_cache.shape[1]
-    S = cu_seqlens_q.shape[0] - 1
-    stride = block_tables.shape[1] if block_tables.dim() == 2 else block_tables.shape[0] // max(S, 1)
+    T, H_q, D, H_kv, S, stride = _attention_args(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens,
+                                                 block_tables, out)
+    if dev_status is not None:
+        import torch
+        _dev(dev_status, "dev_status", torch.int32, min_numel=1)
+        _on_one_gpu(q_rot=q_rot, dev_status=dev_status)
     if scale is None:
         scale = float(D) ** -0.5
     rc = lib().ms_mixed_step_attention_noalloc(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],

@@ -418,6 +418,9 @@ MS_API int ms_graph_bucket(const ms_step_graph* g, int32_t num_tokens);
  * writes it) into the pinned staging buffer, copy it into the fixed device
  * buffers on `stream` and launch the bucket's graph.  The host waits only for
  * the copies of the replay before last (the staging buffers alternate).
+ * Every replay of one graph rewrites the same device metadata buffers, so
+ * the caller issues them on one stream (or orders the streams itself): a
+ * replay's copies must not start while the previous replay still runs.
  * *bucket_used (may be NULL) gets the bucket.  Device errors land in the
  * status words (ms_graph_read_status).
  * Errors: MS_ERR_ARG (num_tokens above the largest bucket, num_rows >

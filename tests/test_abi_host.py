@@ -309,3 +309,54 @@ def test_request_marshalling_edge_cases(ms):
     # lengths beyond int32
     with pytest.raises(ValueError):
         ms.build_batch_metadata([(2 ** 31, 0)], [tables[1]], 16)
+
+
+def test_device_wrappers_check_tensors_before_the_call(ms):
+    """The ABI sees only addresses, so the binding checks dtype, layout, shape,
+    size and device of every tensor first; a bad one raises ValueError and no
+    pointer reaches the library (CPU tensors end at the device check)."""
+    torch = pytest.importorskip("torch")
+    T, H_q, H_kv, D, P = 5, 4, 2, 64, 3
+    bf = torch.bfloat16
+    good = dict(q=torch.zeros((T, H_q, D), dtype=bf), k=torch.zeros((T, H_kv, D), dtype=bf),
+                v=torch.zeros((T, H_kv, D), dtype=bf), positions=torch.zeros(T, dtype=torch.int32),
+                slot_mapping=torch.zeros(T, dtype=torch.int32), cos_tab=torch.zeros((32, D // 2)),
+                sin_tab=torch.zeros((32, D // 2)), k_cache=torch.zeros((P, H_kv, 16, D), dtype=bf),
+                v_cache=torch.zeros((P, H_kv, 16, D), dtype=bf))
+    bad_append = [
+        ("q", torch.zeros((T, H_q, D)), "q must be torch.bfloat16"),
+        ("k", torch.zeros((T, H_kv + 1, D), dtype=bf), "k must have shape"),
+        ("positions", torch.zeros(T, dtype=torch.int64), "positions must be torch.int32"),
+        ("slot_mapping", torch.zeros(T - 1, dtype=torch.int32), "at least 5"),
+        ("cos_tab", torch.zeros((32, D)), "cos_tab must have shape"),
+        ("v_cache", torch.zeros((P, H_kv, D, 16), dtype=bf).transpose(2, 3), "v_cache must be contiguous"),
+        ("k_cache", torch.zeros((P, H_kv, 8, D), dtype=bf), "k_cache must have shape"),
+    ]
+    for name, t, msg in bad_append:
+        with pytest.raises(ValueError, match=msg):
+            ms.kv_append_rope(**{**good, name: t})
+    with pytest.raises(ValueError, match="CUDA"):
+        ms.kv_append_rope(**good)
+
+    S = 2
+    att = dict(q_rot=good["q"], k_cache=good["k_cache"], v_cache=good["v_cache"],
+               cu_seqlens_q=torch.tensor([0, 1, T], dtype=torch.int32),
+               q_start_pos=torch.zeros(S, dtype=torch.int32), context_lens=torch.ones(S, dtype=torch.int32),
+               block_tables=torch.zeros((S, 2), dtype=torch.int32), context_total=2,
+               out=torch.zeros((T, H_q, D), dtype=bf), workspace=torch.zeros(256, dtype=torch.uint8))
+    bad_attention = [
+        ("out", torch.zeros((T, H_q, D)), "out must be torch.bfloat16"),
+        ("out", torch.zeros((T - 1, H_q, D), dtype=bf), "out must have shape"),
+        ("context_lens", torch.ones(S - 1, dtype=torch.int32), "context_lens must hold at least 2"),
+        ("block_tables", torch.zeros((S, 2), dtype=torch.int64), "block_tables must be torch.int32"),
+        ("cu_seqlens_q", torch.zeros((1, 3), dtype=torch.int32), "cu_seqlens_q must be 1-D"),
+        ("v_cache", torch.zeros((P, H_kv, 16, D)), "v_cache must be torch.bfloat16"),
+    ]
+    for name, t, msg in bad_attention:
+        with pytest.raises(ValueError, match=msg):
+            ms.mixed_step_attention(**{**att, name: t})
+        kw = {k: v for k, v in att.items() if k != "workspace"}
+        with pytest.raises(ValueError, match=msg):
+            ms.mixed_step_attention_noalloc(**{**kw, name: t})
+    with pytest.raises(ValueError, match="CUDA"):
+        ms.mixed_step_attention(**att)
