@@ -2,6 +2,8 @@
 
 Argument marshalling only: every step of the path runs in the C++ scheduler
 and the sm_103a kernels behind the C ABI declared in include/mixed_step.h.
+Because the ABI takes bare addresses, each device wrapper checks its tensors'
+dtype, contiguity, shape, size and device first and raises ValueError.
 The functions keep the C names without the ``ms_`` prefix.  Device tensors
 are torch tensors (used for memory and streams only); host metadata is numpy.
 
