@@ -20,8 +20,9 @@
 //   chunk rows (d > 1): tcgen05 tensor cores.  A work item is a pair of
 //     128-row query tiles (128/G tokens x G heads of one KV head each) that
 //     walk 64-key tiles of the prefix and their own chunk together.  TMA loads
-//     Q and K/V pages (one 16-row box per page and 64-column slab, 128-byte
-//     swizzle); S = Q K^T lands in TMEM; two groups of four softmax warps, one
+//     Q and K pages (one 16-row box per page and 64-column slab, 128-byte
+//     swizzle) and V pages (one box per page, both slabs, at D = 128); S = Q K^T
+//     lands in TMEM; two groups of four softmax warps, one
 //     per query tile and one row per thread, write P (bf16) back over S, and
 //     O += P V runs with P as the TMEM operand, accumulating in TMEM and
 //     rescaled only when a row's maximum grows by more than a factor 2^8.
@@ -867,8 +868,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // caller owns TMEM and the barrier invalidation.
 template <int D, int G>
 __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtensorMap* tm_k_p,
-                                            const CUtensorMap* tm_v_p, const AttnParams& p, uint8_t* smem,
-                                            uint32_t tmem) {
+                                            const CUtensorMap* tm_v_p, const CUtensorMap* tm_vp_p,
+                                            const AttnParams& p, uint8_t* smem, uint32_t tmem) {
   using C = ChCfg<D>;
   constexpr int NSL = C::NSL;
   constexpr int TPT = 128 / G;  // query tokens per 128-row Q tile
@@ -876,6 +877,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
   const CUtensorMap& tm_q = *tm_q_p;
   const CUtensorMap& tm_k = *tm_k_p;
   const CUtensorMap& tm_v = *tm_v_p;
+  const CUtensorMap& tm_vp = *tm_vp_p;  // V by whole pages (D = 128)
   ChBars* bars = reinterpret_cast<ChBars*>(smem + C::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.hdr[H_NCH_ITEMS];
@@ -883,6 +885,10 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
   const uint32_t sbase = smem_u32(smem);
   auto k_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kKVSlab; };
   auto v_off = [](int b) { return C::KV_OFF + b * 2 * NSL * kKVSlab + NSL * kKVSlab; };
+  // A V stage holds its tile page by page: key k of the tile at
+  // (k / 16) * kVPage + slab * 2048 + (k % 16) * 128.  A page is one TMA box
+  // (two 2 KB boxes of K cost about as much TMA time as one 4 KB box).
+  constexpr int kVPage = NSL * 2048;
   auto s_col = [&](int t, int b) { return tmem + C::S_COL + (2 * t + b) * 64; };
 
   if (threadIdx.x == 0) {
@@ -914,13 +920,13 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
   if (warp == 0) {
     // ---------------------------------------------------------------- work queue + TMA producer
     // The whole warp runs this loop: lane 0 owns the queue, the waits and the
-    // barrier bookkeeping; a tile's K (or V) boxes -- one per (page, 64-column
-    // slab) -- go out as one warp-wide TMA instruction, lane L taking page
-    // L / NSL, slab L % NSL.
+    // barrier bookkeeping; a tile's K boxes -- one per (page, 64-column slab)
+    // -- go out as one warp-wide TMA instruction, lane L taking page L / NSL,
+    // slab L % NSL; its V boxes likewise, one per page (lanes with slab 0).
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
+      prefetch_tmap(NSL == 2 ? &tm_vp : &tm_v);
     }
     const int my_pg = lane / NSL, my_s = lane % NSL;
     const bool loader = lane < kTilePages * NSL;
@@ -941,8 +947,13 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
       if (gv >= KVS && !lane0_wait(&bars->v_empty[bv], ((gv / KVS) - 1) & 1)) return false;
       if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[bv], npg * kPage * D * 2);
       __syncwarp();
-      if (loader && my_pg < npg)
-        tma_load_2d(smem + v_off(bv) + my_s * kKVSlab + my_pg * 2048, &tm_v, my_s * 64, row0, &bars->v_full[bv]);
+      if constexpr (NSL == 2) {
+        if (loader && my_s == 0 && my_pg < npg)
+          tma_load_4d(smem + v_off(bv) + my_pg * kVPage, &tm_vp, 0, 0, 0, row0 / kPage, &bars->v_full[bv]);
+      } else {
+        if (loader && my_pg < npg)
+          tma_load_2d(smem + v_off(bv) + my_pg * kVPage, &tm_v, 0, row0, &bars->v_full[bv]);
+      }
       return true;
     };
     while (ok) {
@@ -1132,10 +1143,10 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
     // ---------------------------------------------------------------- PV issuer of both groups
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-      // V is the MN-major B operand: 64-column slabs one slab apart (LBO), 8-key row
-      // groups 1024 B apart (SBO), 16 keys = 2048 B per k-step.  P (A operand) is in
-      // TMEM: 16 keys = 8 packed columns per k-step.
-      const uint64_t vdesc0 = smem_desc_sw128(sbase + C::KV_OFF + NSL * kKVSlab, kKVSlab, 1024);
+      // V is the MN-major B operand, one page per k-step of 16 keys: the page's
+      // 64-column slabs 2048 B apart (LBO), its two 8-key row groups 1024 B apart
+      // (SBO).  P (A operand) is in TMEM: 16 keys = 8 packed columns per k-step.
+      const uint64_t vdesc0 = smem_desc_sw128(sbase + C::KV_OFF + NSL * kKVSlab, 2048, 1024);
       int bv = 0;        // V stage of the next tile
       uint32_t vph = 0;  // its phase parity
       bool ok = true;
@@ -1165,7 +1176,8 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
             for (int r = keys; r < ((keys + 15) & ~15); ++r)
               for (int s = 0; s < NSL; ++s)
                 for (int q16 = 0; q16 < 8; ++q16)
-                  *reinterpret_cast<uint4*>(v0 + s * kKVSlab + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+                  *reinterpret_cast<uint4*>(v0 + (r >> 4) * kVPage + s * 2048 + (r & 15) * 128 + q16 * 16) =
+                      make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
           }
           const uint64_t vd = vdesc0 + static_cast<uint64_t>((bv * 2 * NSL * kKVSlab) >> 4);
@@ -1184,12 +1196,12 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
               if (kr >= kKeys) {
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk)
-                  mma_bf16_ts(dcol, acol + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
+                  mma_bf16_ts(dcol, acol + kk * 8, vd + static_cast<uint64_t>((kk * kVPage) >> 4), idesc_pv,
                               (j > 0 || kk > 0) ? 1u : 0u);
               } else {
                 const int nk_t = (kr + 15) >> 4;
                 for (int kk = 0; kk < nk_t; ++kk)
-                  mma_bf16_ts(dcol, acol + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
+                  mma_bf16_ts(dcol, acol + kk * 8, vd + static_cast<uint64_t>((kk * kVPage) >> 4), idesc_pv,
                               (j > 0 || kk > 0) ? 1u : 0u);
               }
               mma_commit(&bars->o_done[t][b]);
@@ -1394,7 +1406,8 @@ __device__ __forceinline__ void invalidate_phase_barriers(uint8_t* smem, bool ch
 template <int D, int G>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, AttnParams p) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vp,
+                     AttnParams p) {
   // no static shared memory: the dynamic block starts 1024-aligned, as the
   // 128-byte-swizzled TMA tiles and MMA descriptors require
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -1435,7 +1448,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   for (int ph = 0; ph < 2; ++ph) {
     const bool chunk = (ph == 0) == chunk_first;
     if (chunk && n_ch_items > 0) {
-      chunk_phase<D, G>(&tm_q, &tm_k, &tm_v, p, smem, tmem);
+      chunk_phase<D, G>(&tm_q, &tm_k, &tm_v, &tm_vp, p, smem, tmem);
       tc_fence_before();
       __syncthreads();
       const bool aborted = reinterpret_cast<ChBars*>(smem + ChCfg<D>::BAR_OFF)->abort != 0;
@@ -1530,7 +1543,7 @@ EncodeTiledFn get_encode_fn() {
 
 bool encode_bf16(EncodeTiledFn fn, CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
                  const cuuint64_t* strides_bytes, const cuuint32_t* box) {
-  cuuint32_t elem[3] = {1, 1, 1};
+  cuuint32_t elem[5] = {1, 1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes, box, elem,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1609,12 +1622,12 @@ int dec_warps(int D, int G) {
 
 template <int D, int G>
 int launch_paths(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                 int n_ctas, cudaStream_t st) {
+                 const CUtensorMap& tvp, int n_ctas, cudaStream_t st) {
   constexpr int smem = ChCfg<D>::SMEM > DecCfg<D, G>::SMEM ? ChCfg<D>::SMEM : DecCfg<D, G>::SMEM;
   static_assert(smem <= 232448, "attention kernel exceeds the per-CTA shared-memory limit");
   const int slot = (D == 128 ? 4 : 0) + (G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3);  // one bit per instance
   if (ensure_smem_limit(attention_kernel<D, G>, slot, smem) != MS_OK) return MS_ERR_CUDA;
-  if (launch_dependent(attention_kernel<D, G>, dim3(n_ctas), dim3(kChunkThreads), smem, st, tq, tk, tv, p) !=
+  if (launch_dependent(attention_kernel<D, G>, dim3(n_ctas), dim3(kChunkThreads), smem, st, tq, tk, tv, tvp, p) !=
       cudaSuccess)
     return MS_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MS_OK : MS_ERR_CUDA;
@@ -1663,7 +1676,7 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return MS_ERR_CUDA;
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tvp;
   {
     const cuuint64_t dq[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_q),
                               static_cast<cuuint64_t>(num_tokens)};
@@ -1675,6 +1688,17 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
     if (!encode_bf16(enc, &tq, q_rot, 3, dq, sq, bq) || !encode_bf16(enc, &tk, k_cache, 2, dk, sk, bk) ||
         !encode_bf16(enc, &tv, v_cache, 2, dk, sk, bk))
       return MS_ERR_ARG;
+    tvp = tv;  // at D = 64 a page is one 2 KB box of tv
+    if (D == 128) {
+      // V by whole pages for the chunk tiles: (64 columns, 16 rows, 2 slabs, page x KV head),
+      // so that one box lands as the page's slab 0 then its slab 1
+      const cuuint64_t dv[4] = {64, static_cast<cuuint64_t>(kPage), 2,
+                                static_cast<cuuint64_t>(num_pages) * H_kv};
+      const cuuint64_t sv[3] = {static_cast<cuuint64_t>(D) * 2, 128,
+                                static_cast<cuuint64_t>(kPage) * D * 2};
+      const cuuint32_t bv[4] = {64, static_cast<cuuint32_t>(kPage), 2, 1};
+      if (!encode_bf16(enc, &tvp, v_cache, 4, dv, sv, bv)) return MS_ERR_ARG;
+    }
   }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1725,14 +1749,14 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
   const int n_ctas = sms;  // one persistent CTA per SM
   int rc = MS_ERR_ARG;
   switch (D * 100 + G) {
-    case 6401: rc = launch_paths<64, 1>(p, tq, tk, tv, n_ctas, st); break;
-    case 6402: rc = launch_paths<64, 2>(p, tq, tk, tv, n_ctas, st); break;
-    case 6404: rc = launch_paths<64, 4>(p, tq, tk, tv, n_ctas, st); break;
-    case 6408: rc = launch_paths<64, 8>(p, tq, tk, tv, n_ctas, st); break;
-    case 12801: rc = launch_paths<128, 1>(p, tq, tk, tv, n_ctas, st); break;
-    case 12802: rc = launch_paths<128, 2>(p, tq, tk, tv, n_ctas, st); break;
-    case 12804: rc = launch_paths<128, 4>(p, tq, tk, tv, n_ctas, st); break;
-    case 12808: rc = launch_paths<128, 8>(p, tq, tk, tv, n_ctas, st); break;
+    case 6401: rc = launch_paths<64, 1>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 6402: rc = launch_paths<64, 2>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 6404: rc = launch_paths<64, 4>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 6408: rc = launch_paths<64, 8>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 12801: rc = launch_paths<128, 1>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 12802: rc = launch_paths<128, 2>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 12804: rc = launch_paths<128, 4>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 12808: rc = launch_paths<128, 8>(p, tq, tk, tv, tvp, n_ctas, st); break;
     default: break;
   }
   return rc;
