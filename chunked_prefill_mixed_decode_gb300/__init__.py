@@ -348,8 +348,8 @@ class StepGraph:
         num_pages, H_kv, _, D = k_cache.shape
         _pools(k_cache, v_cache, H_kv, D)
         _dev(cos, "cos", torch.float32, (cos.shape[0], D // 2))
-        _dev(sin, "sin", torch.float32, tuple(cos.shape))
-        _on_one_gpu(k_cache=k_cache, v_cache=v_cache, cos=cos, sin=sin)
+        _dev(sin, "sin", torch.float32, cos.shape)
+        _on_one_gpu("k_cache v_cache cos sin", k_cache, v_cache, cos, sin)
         self.buckets = [int(b) for b in buckets]
         B = self.buckets[-1]
         self.stream = stream
@@ -432,31 +432,34 @@ def num_sms() -> int:
 
 def _dev(t, name: str, dtype, shape=None, min_numel: int = 0) -> None:
     """Check a tensor before its pointer crosses the C ABI, which sees only an
-    address: dtype, dense row-major layout, shape and size."""
+    address: dtype, dense row-major layout, then shape or size."""
     if t is None:
         raise ValueError(f"{name} is required")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if shape is not None and tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
-    if t.numel() < min_numel:
+    if shape is not None:
+        if t.shape != shape:
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    elif min_numel and t.numel() < min_numel:
         raise ValueError(f"{name} must hold at least {min_numel} elements, got {t.numel()}")
 
 
-def _on_one_gpu(**tensors) -> None:
-    """Every tensor on the CUDA device of the first one (None entries are skipped)."""
-    dev = None
-    for name, t in tensors.items():
+def _on_one_gpu(names: str, *tensors) -> None:
+    """Every tensor (None entries skipped) on the CUDA device of the first;
+    ``names`` lists them, space-separated, for the error message."""
+    dev = -2
+    for i, t in enumerate(tensors):
         if t is None:
             continue
-        if not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
-        if dev is None:
-            dev = t.device
-        elif t.device != dev:
-            raise ValueError(f"{name} is on {t.device}, the other tensors on {dev}")
+        d = t.get_device()
+        if d < 0 or (dev != -2 and d != dev):
+            name = names.split()[i]
+            if d < 0:
+                raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
+            raise ValueError(f"{name} is on {t.device}, the other tensors on cuda:{dev}")
+        dev = d
 
 
 def _pools(k_cache, v_cache, H_kv: int, D: int) -> None:
@@ -464,7 +467,7 @@ def _pools(k_cache, v_cache, H_kv: int, D: int) -> None:
     if k_cache.dim() != 4:
         raise ValueError(f"k_cache must be [pages, H_kv, {PAGE_SIZE}, D], got {tuple(k_cache.shape)}")
     _dev(k_cache, "k_cache", torch.bfloat16, (k_cache.shape[0], H_kv, PAGE_SIZE, D))
-    _dev(v_cache, "v_cache", torch.bfloat16, tuple(k_cache.shape))
+    _dev(v_cache, "v_cache", torch.bfloat16, k_cache.shape)
 
 
 def kv_append_rope(q, k, v, positions, slot_mapping, cos_tab, sin_tab, k_cache, v_cache, q_rot=None,
@@ -488,12 +491,12 @@ def kv_append_rope(q, k, v, positions, slot_mapping, cos_tab, sin_tab, k_cache, 
     if cos_tab.dim() != 2:
         raise ValueError("cos_tab must be [max_pos, D/2]")
     _dev(cos_tab, "cos_tab", torch.float32, (cos_tab.shape[0], D // 2))
-    _dev(sin_tab, "sin_tab", torch.float32, tuple(cos_tab.shape))
+    _dev(sin_tab, "sin_tab", torch.float32, cos_tab.shape)
     _pools(k_cache, v_cache, H_kv, D)
     if dev_status is not None:
         _dev(dev_status, "dev_status", torch.int32, min_numel=1)
-    _on_one_gpu(q=q, k=k, v=v, q_rot=q_rot, positions=positions, slot_mapping=slot_mapping, cos_tab=cos_tab,
-                sin_tab=sin_tab, k_cache=k_cache, v_cache=v_cache, dev_status=dev_status)
+    _on_one_gpu("q k v q_rot positions slot_mapping cos_tab sin_tab k_cache v_cache dev_status", q, k, v, q_rot,
+                positions, slot_mapping, cos_tab, sin_tab, k_cache, v_cache, dev_status)
     rc = lib().ms_kv_append_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(slot_mapping), T, _ptr(cos_tab),
                                  _ptr(sin_tab), cos_tab.shape[0], _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
                                  _ptr(q_rot), H_q, H_kv, D, PAGE_SIZE, _ptr(dev_status), _stream(stream))
@@ -520,8 +523,8 @@ def _attention_args(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_
     stride = block_tables.shape[1] if block_tables.dim() == 2 else block_tables.shape[0] // max(S, 1)
     _dev(block_tables, "block_tables", torch.int32, min_numel=S * stride)
     _dev(out, "out", torch.bfloat16, (T, H_q, D))
-    _on_one_gpu(q_rot=q_rot, k_cache=k_cache, v_cache=v_cache, cu_seqlens_q=cu_seqlens_q, q_start_pos=q_start_pos,
-                context_lens=context_lens, block_tables=block_tables, out=out)
+    _on_one_gpu("q_rot k_cache v_cache cu_seqlens_q q_start_pos context_lens block_tables out", q_rot, k_cache,
+                v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables, out)
     return T, H_q, D, H_kv, S, stride
 
 
@@ -535,7 +538,7 @@ def mixed_step_attention(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, con
     T, H_q, D, H_kv, S, stride = _attention_args(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens,
                                                  block_tables, out)
     _dev(workspace, "workspace", None)
-    _on_one_gpu(q_rot=q_rot, workspace=workspace)
+    _on_one_gpu("q_rot workspace", q_rot, workspace)
     if scale is None:
         scale = float(D) ** -0.5
     rc = lib().ms_mixed_step_attention(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
@@ -561,7 +564,7 @@ def mixed_step_attention_noalloc(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_
     if dev_status is not None:
         import torch
         _dev(dev_status, "dev_status", torch.int32, min_numel=1)
-        _on_one_gpu(q_rot=q_rot, dev_status=dev_status)
+        _on_one_gpu("q_rot dev_status", q_rot, dev_status)
     if scale is None:
         scale = float(D) ** -0.5
     rc = lib().ms_mixed_step_attention_noalloc(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
