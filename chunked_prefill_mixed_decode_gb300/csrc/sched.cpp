@@ -128,6 +128,11 @@ extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_
     const int32_t need = ceil_div(ctx, kPage);
     if (reqs[r.req].num_pages < need) return MS_ERR_NO_PAGES;
     if (need > stride) stride = need;
+    // every page the row reads must be a page id whose slots fit in int32: a
+    // negative id could turn into the "no write" slot -1 in slot_mapping
+    const int32_t* bt = reqs[r.req].block_table;
+    for (int32_t p = 0; p < need; ++p)
+      if (bt[p] < 0 || bt[p] > INT32_MAX / kPage - 1) return MS_ERR_ARG;
   }
   if (S > cap_rows || used > cap_tokens || static_cast<int64_t>(S) * stride > cap_bt) return MS_ERR_ARG;
   if (n_req > 0 && num_scheduled == nullptr) return MS_ERR_ARG;

@@ -152,7 +152,8 @@ typedef struct {
  *   row_req       [cap_rows]      request index of each row
  *   num_scheduled [n_req]         tokens each request got this round (0 or d)
  *   info          summary (num_rows, num_decodes, num_tokens, bt_stride, unused)
- * Errors: MS_ERR_ARG (null pointer, capacity too small, negative lengths),
+ * Errors: MS_ERR_ARG (null pointer, capacity too small, negative lengths, a
+ * page id that a scheduled row reads below 0 or above INT32_MAX / 16 - 1),
  * MS_ERR_BUDGET, MS_ERR_NO_PAGES (a block table shorter than ceil((c+d)/16)). */
 MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_req, const ms_sched_config* cfg,
                                    int32_t cap_rows, int32_t cap_tokens, int64_t cap_bt,

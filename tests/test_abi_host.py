@@ -360,3 +360,18 @@ def test_device_wrappers_check_tensors_before_the_call(ms):
             ms.mixed_step_attention_noalloc(**{**kw, name: t})
     with pytest.raises(ValueError, match="CUDA"):
         ms.mixed_step_attention(**att)
+
+
+def test_page_ids_a_row_reads_must_be_valid(ms):
+    """A page id below 0 (which could turn a slot into the "no write" value -1)
+    or one whose slots overflow int32 is refused with MS_ERR_ARG; ids the step
+    does not read are not looked at."""
+    ok = ms.build_batch_metadata([(16, 0)], [np.asarray([3, 5, -1], dtype=np.int32)], 8)
+    np.testing.assert_array_equal(ok["slot_mapping"], [5 * 16])
+    for bad in ([3, -1], [-2, 5], [3, 2 ** 31 // 16]):
+        with pytest.raises(ms.MixedStepError) as e:
+            ms.build_batch_metadata([(16, 0)], [np.asarray(bad, dtype=np.int32)], 8)
+        assert e.value.code == ms.MS_ERR_ARG
+    with pytest.raises(ms.MixedStepError) as e:  # a chunk row reads every page up to its last token
+        ms.build_batch_metadata([(0, 40)], [np.asarray([0, -1, 2], dtype=np.int32)], 64)
+    assert e.value.code == ms.MS_ERR_ARG
