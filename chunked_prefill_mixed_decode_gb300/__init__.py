@@ -183,7 +183,8 @@ def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndar
     sizes = (("cu_seqlens_q", cap_rows + 1), ("q_start_pos", cap_rows), ("context_lens", cap_rows),
              ("positions", cap_tokens), ("slot_mapping", cap_tokens), ("block_tables", cap_bt),
              ("row_req", cap_rows), ("num_scheduled", max(n, 1)))
-    buf = np.zeros(sum(sz for _, sz in sizes), dtype=np.int32)
+    # every element a returned view covers is written by the call
+    buf = np.empty(sum(sz for _, sz in sizes), dtype=np.int32)
     out, off = {}, 0
     for k, sz in sizes:
         out[k] = buf[off:off + sz]
@@ -293,7 +294,8 @@ class Engine:
         sizes = (("cu_seqlens_q", cap_rows + 1), ("q_start_pos", cap_rows), ("context_lens", cap_rows),
                  ("positions", cap_tokens), ("slot_mapping", cap_tokens), ("block_tables", cap_bt),
                  ("row_request_id", cap_rows))
-        buf = np.zeros(sum(sz for _, sz in sizes), dtype=np.int32)  # the returned arrays are views of it
+        # the returned arrays are views of it; every element they cover is written by the call
+        buf = np.empty(sum(sz for _, sz in sizes), dtype=np.int32)
         out, off = {}, 0
         for k, sz in sizes:
             out[k] = buf[off:off + sz]

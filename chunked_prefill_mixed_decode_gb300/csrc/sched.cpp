@@ -12,6 +12,7 @@
 // order".  The metadata is the zwjcode page's section 06 list: absolute
 // positions, one physical slot per new token, the block table, and the context
 // length after the round.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -158,7 +159,8 @@ extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_
     }
     const int32_t need = ceil_div(static_cast<int64_t>(r.c) + r.d, kPage);
     int32_t* dst = block_tables + static_cast<int64_t>(s) * stride;
-    for (int32_t p = 0; p < stride; ++p) dst[p] = p < need ? bt[p] : -1;
+    std::memcpy(dst, bt, static_cast<size_t>(need) * sizeof(int32_t));
+    std::fill(dst + need, dst + stride, -1);
   }
   info->num_rows = S;
   info->num_decodes = num_decodes;
