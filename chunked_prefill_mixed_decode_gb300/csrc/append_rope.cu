@@ -87,23 +87,25 @@ __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendArgs a) {
     const int pos = __ldg(a.positions + t);
     const int slot = __ldg(a.slot_mapping + t);
 
-    if (h >= a.H_q + a.H_kv) {  // V: plain copy into the slot
-      const int hv = h - a.H_q - a.H_kv;
-      if (slot < 0) continue;
-      if (static_cast<int64_t>(slot) >= a.n_slots) {
+    if (h >= a.H_q) {  // K or V: the slot first; -1 is the one "no write" value
+      if (slot == -1) continue;
+      if (slot < 0 || static_cast<int64_t>(slot) >= a.n_slots) {
         if (a.status && part == 0) atomicOr(a.status, MS_STATUS_BAD_SLOT);
         continue;
       }
+    }
+    // a token at a position outside the table writes nothing: no q_rot, no K, no V
+    if (pos < 0 || pos >= a.max_pos) {
+      if (a.status && part == 0) atomicOr(a.status, MS_STATUS_BAD_POSITION);
+      continue;
+    }
+    if (h >= a.H_q + a.H_kv) {  // V: plain copy into the slot
+      const int hv = h - a.H_q - a.H_kv;
       const __nv_bfloat16* src = a.v + (static_cast<int64_t>(t) * a.H_kv + hv) * a.D;
       const int64_t page = slot / a.page, off = slot % a.page;
       __nv_bfloat16* dst = a.v_cache + ((page * a.H_kv + hv) * a.page + off) * a.D;
       *reinterpret_cast<uint4*>(dst + i0) = __ldg(reinterpret_cast<const uint4*>(src + i0));
       *reinterpret_cast<uint4*>(dst + i0 + half) = __ldg(reinterpret_cast<const uint4*>(src + i0 + half));
-      continue;
-    }
-
-    if (pos < 0 || pos >= a.max_pos) {
-      if (a.status && part == 0) atomicOr(a.status, MS_STATUS_BAD_POSITION);
       continue;
     }
     float c[kVec], s[kVec];
@@ -124,11 +126,6 @@ __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendArgs a) {
       *reinterpret_cast<uint4*>(a.q_rot + base + i0 + half) = yb;
     } else {  // k -> rotated into the slot
       const int hk = h - a.H_q;
-      if (slot < 0) continue;
-      if (static_cast<int64_t>(slot) >= a.n_slots) {
-        if (a.status && part == 0) atomicOr(a.status, MS_STATUS_BAD_SLOT);
-        continue;
-      }
       const int64_t base = (static_cast<int64_t>(t) * a.H_kv + hk) * a.D;
       const uint4 xa = __ldg(reinterpret_cast<const uint4*>(a.k + base + i0));
       const uint4 xb = __ldg(reinterpret_cast<const uint4*>(a.k + base + i0 + half));
