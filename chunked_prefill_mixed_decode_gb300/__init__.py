@@ -110,6 +110,11 @@ def lib() -> ctypes.CDLL:
                                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                   ctypes.c_float, _VP, _VP, _VP]
+    h.ms_test_attention_stall.restype = ctypes.c_int
+    h.ms_test_attention_stall.argtypes = [_VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP, _VP, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _VP, _VP,
+                                          ctypes.c_size_t, ctypes.c_int64, _VP]
     h.ms_read_status.restype = ctypes.c_int
     h.ms_read_status.argtypes = [_VP, _VP, _I32P]
     h.ms_num_sms.restype = ctypes.c_int
@@ -575,6 +580,27 @@ def mixed_step_attention_noalloc(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_
                                                PAGE_SIZE, float(scale), _ptr(out), _ptr(dev_status),
                                                _stream(stream))
     _check(rc, "ms_mixed_step_attention_noalloc")
+
+
+def test_attention_stall(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables,
+                         context_total: int, out, workspace, wait_limit_ns: int, scale: float = None,
+                         stream=None) -> None:
+    """Test hook of the bounded device waits (ms_test_attention_stall): the attention call with every
+    chunk-phase producer stopped, so the chunk phase's waits run out after ``wait_limit_ns`` and set
+    STATUS_TIMEOUT in the workspace's status word.  Not for production use."""
+    T, H_q, D, H_kv, S, stride = _attention_args(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens,
+                                                 block_tables, out)
+    _dev(workspace, "workspace", None)
+    _on_one_gpu("q_rot workspace", q_rot, workspace)
+    if scale is None:
+        scale = float(D) ** -0.5
+    rc = lib().ms_test_attention_stall(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                       _ptr(cu_seqlens_q), _ptr(q_start_pos), _ptr(context_lens),
+                                       _ptr(block_tables), stride, S, T, int(context_total), H_q, H_kv, D,
+                                       PAGE_SIZE, float(scale), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), int(wait_limit_ns),
+                                       _stream(stream))
+    _check(rc, "ms_test_attention_stall")
 
 
 def read_status(dev_status, stream=None) -> int:

@@ -110,6 +110,9 @@ struct AttnParams {
   int32_t H_q, H_kv, D, G;
   int32_t dec_workers;  // decode worker warps in the grid
   int32_t num_sms;
+  int32_t clear_status;  // the prologue zeroes the status word first (scratch owned by the library)
+  int32_t test_stall;    // test hook: chunk-phase producers publish no work item (0 in every real call)
+  uint64_t wait_limit_ns;  // bound of every chunk-phase wait
   float scale_log2;
 };
 
@@ -205,7 +208,12 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
   const int S = p.num_rows;
   int32_t* hdr = p.hdr;
   griddep_launch_dependents();
-  if (tid == 0) s_tiles = 0;
+  if (tid == 0) {
+    s_tiles = 0;
+    // a library-owned scratch keeps the previous call's status: start this call at zero
+    // (before the first __syncthreads, so ahead of every status write of this call)
+    if (p.clear_status) hdr[H_STATUS] = 0;
+  }
   // 1. this thread's rows s = tid + i * 1024: load, validate, count (block sums, no atomics)
   int rd[R], rc[R];
   int64_t my_ctx = 0, my_pages = 0;
@@ -846,9 +854,10 @@ static_assert(ChCfg<128>::SMEM <= 232448 && ChCfg<64>::SMEM <= 232448,
 static_assert(ChCfg<128>::KVS <= 8 && ChCfg<64>::KVS <= 8, "more K/V stages than barriers");
 
 // wait by lane 0, result and ordering shared with the whole warp
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t limit_ns) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, limit_ns) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
@@ -916,6 +925,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
   }
   __syncthreads();
   volatile int* abort_flag = &bars->abort;
+  const uint64_t lim = p.wait_limit_ns;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- work queue + TMA producer
@@ -934,10 +944,15 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
     int g_v = 0;             // tiles whose V has been issued
     int n_done = 0;          // items taken by this CTA
     int t_run[2] = {0, 0};   // KV tiles run by each softmax group so far
-    bool ok = true;
+    // Test hook (never set by a real call): publish no work item and issue no
+    // copy, as a producer that stopped would.  Every other role then waits on
+    // an item that never comes until its bounded wait gives up, with nothing
+    // in flight: the timeout path runs exactly as it would in a real stall.
+    const bool stalled = p.test_stall != 0;
+    bool ok = !stalled;
     auto lane0_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
       int r = 1;
-      if (lane == 0) r = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+      if (lane == 0) r = mbar_wait(bar, parity, abort_flag, lim) ? 1 : 0;
       r = __shfl_sync(0xffffffffu, r, 0);
       return r != 0;
     };
@@ -1057,7 +1072,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
       g_v = g;
     }
     if (lane == 0) {
-      if (!ok) *abort_flag = 1;
+      if (!ok && !stalled) *abort_flag = 1;
       // copies still in flight must land before the CTA moves on
       for (int t = (g > KVS ? g - KVS : 0); t < g; ++t)
         mbar_wait(&bars->k_full[t % KVS], (t / KVS) & 1, nullptr, 200000000ull);
@@ -1086,7 +1101,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
       bool ok = true;
       for (int n = 0; ok; ++n) {
         const int slot = n & 1;
-        if (!mbar_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag)) {
+        if (!mbar_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag, lim)) {
           ok = false;
           break;
         }
@@ -1095,19 +1110,19 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
         if (row < 0) break;
         const int nkt = it.nkt[t], t0 = it.t0[t], n_kt = it.n_kt;
         const int kv_max = max(it.kv_end[0], it.kv_end[1]);
-        if (nkt > 0 && !mbar_wait(&bars->q_full, n & 1, abort_flag)) {
+        if (nkt > 0 && !mbar_wait(&bars->q_full, n & 1, abort_flag, lim)) {
           ok = false;
           break;
         }
         for (int kt = 0; kt < n_kt; ++kt) {
-          if (!mbar_wait_fast(&bars->k_full[bk], kph, abort_flag, 16)) {
+          if (!mbar_wait_fast(&bars->k_full[bk], kph, abort_flag, 16, lim)) {
             ok = false;
             break;
           }
           if (kt < nkt) {
             const int gt = t0 + kt, b = gt & 1;
             // S buffer b last held P of the group's tile gt - 2: its PV MMA must be done
-            if (gt >= 2 && !mbar_wait_fast(&bars->o_done[t][b], ((gt - 2) >> 1) & 1, abort_flag, 16)) {
+            if (gt >= 2 && !mbar_wait_fast(&bars->o_done[t][b], ((gt - 2) >> 1) & 1, abort_flag, 16, lim)) {
               ok = false;
               break;
             }
@@ -1152,7 +1167,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
       bool ok = true;
       for (int n = 0; ok; ++n) {
         const int slot = n & 1;
-        if (!mbar_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag)) {
+        if (!mbar_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag, lim)) {
           ok = false;
           break;
         }
@@ -1164,7 +1179,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
         const int ke_[2] = {it.kv_end[0], it.kv_end[1]};
         const int kv_max = max(ke_[0], ke_[1]);
         for (int j = 0; j < n_kt && ok; ++j) {
-          if (!mbar_wait_fast(&bars->v_full[bv], vph, abort_flag, 16)) {
+          if (!mbar_wait_fast(&bars->v_full[bv], vph, abort_flag, 16, lim)) {
             ok = false;
             break;
           }
@@ -1185,7 +1200,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
           for (int t = 0; t < 2; ++t) {
             if (j < nkt_[t]) {
               const int gt = t0_[t] + j, b = gt & 1;
-              if (!mbar_wait_fast(&bars->p_full[t][b], (gt >> 1) & 1, abort_flag, 16)) {
+              if (!mbar_wait_fast(&bars->p_full[t][b], (gt >> 1) & 1, abort_flag, 16, lim)) {
                 ok = false;
                 break;
               }
@@ -1236,7 +1251,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int slot = n & 1;
-      if (!warp_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag)) {
+      if (!warp_wait(&bars->item_full[slot], (n >> 1) & 1, abort_flag, lim)) {
         ok = false;
         break;
       }
@@ -1251,7 +1266,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
         float m_use = -INFINITY, l = 0.f;
         for (int kt = 0; kt < nkt; ++kt) {
           const int gt = it.t0[t] + kt, b = gt & 1;
-          if (!warp_wait(&bars->s_full[t][b], (gt >> 1) & 1, abort_flag)) {
+          if (!warp_wait(&bars->s_full[t][b], (gt >> 1) & 1, abort_flag, lim)) {
             ok = false;
             break;
           }
@@ -1315,7 +1330,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
           tmem_st32u(ts, pw);
           if (kt > 0 && __any_sync(0xffffffffu, grow)) {  // rescale this row's O
             // the PV MMA of the previous tile must be done with O first
-            if (!warp_wait(&bars->o_done[t][(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag)) {
+            if (!warp_wait(&bars->o_done[t][(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag, lim)) {
               ok = false;
               break;
             }
@@ -1337,7 +1352,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
         }
         if (!ok) break;
         const int gl = it.t0[t] + nkt - 1;
-        if (!warp_wait(&bars->o_done[t][gl & 1], (gl >> 1) & 1, abort_flag)) {
+        if (!warp_wait(&bars->o_done[t][gl & 1], (gl >> 1) & 1, abort_flag, lim)) {
           ok = false;
           break;
         }
@@ -1650,13 +1665,22 @@ extern "C" MS_API int ms_num_sms(void) {
   return n > 0 ? n : MS_ERR_CUDA;
 }
 
-extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_cache, const void* v_cache,
-                                              int32_t num_pages, const int32_t* cu_seqlens_q,
-                                              const int32_t* q_start_pos, const int32_t* context_lens,
-                                              const int32_t* block_tables, int32_t bt_stride, int32_t num_rows,
-                                              int32_t num_tokens, int64_t context_total, int32_t H_q, int32_t H_kv,
-                                              int32_t D, int32_t page_size, float scale, void* out, void* workspace,
-                                              size_t ws_bytes, ms_stream_t stream) {
+namespace {
+
+// The attention call behind both entry points.  Every argument check comes
+// before the first enqueue, so a call that returns an error has put nothing on
+// the stream.  *launched tells whether kernels were enqueued (a step with no
+// tokens enqueues none); clear_status makes the prologue zero the status word
+// before anything of this call can set it.  stall_limit_ns > 0 is the test
+// hook of ms_test_attention_stall: chunk-phase producers publish nothing and
+// every chunk-phase wait gives up after that many nanoseconds.
+int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, int32_t num_pages,
+                   const int32_t* cu_seqlens_q, const int32_t* q_start_pos, const int32_t* context_lens,
+                   const int32_t* block_tables, int32_t bt_stride, int32_t num_rows, int32_t num_tokens,
+                   int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
+                   void* out, void* workspace, size_t ws_bytes, ms_stream_t stream, bool clear_status,
+                   int64_t stall_limit_ns, bool* launched) {
+  *launched = false;
   if (num_rows < 0 || num_tokens < 0 || context_total < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 ||
       (D != 64 && D != 128) || page_size != kPage || bt_stride < 0 || num_pages < 0 || !(scale > 0.f))
     return MS_ERR_ARG;
@@ -1669,6 +1693,7 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
   if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return MS_ERR_ARG;
+  if (num_rows > kMaxRows) return MS_ERR_ARG;
   const WsLayout w = ws_layout(num_rows, num_tokens, context_total, H_q, H_kv, D);
   if (ws_bytes < w.total) return MS_ERR_ARG;
   const int sms = num_sms();
@@ -1737,11 +1762,14 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
   p.G = G;
   p.dec_workers = sms * dec_warps(D, G);
   p.num_sms = sms;
+  p.clear_status = clear_status ? 1 : 0;
+  p.test_stall = stall_limit_ns > 0 ? 1 : 0;
+  p.wait_limit_ns = stall_limit_ns > 0 ? static_cast<uint64_t>(stall_limit_ns) : 2000000000ull;
   p.scale_log2 = scale * 1.4426950408889634f;
 
-  if (num_rows > kMaxRows) return MS_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (ensure_smem_limit(prologue_kernel, 8, static_cast<int>(sizeof(PrologueSmem))) != MS_OK) return MS_ERR_CUDA;
+  *launched = true;  // from here on, kernels may be on the stream
   if (launch_dependent(prologue_kernel, dim3(1), dim3(kPrologueThreads), sizeof(PrologueSmem), st, p) !=
           cudaSuccess ||
       launch_dependent(items_kernel, dim3(sms < 64 ? sms : 64), dim3(kItemThreads), 0, st, p) != cudaSuccess)
@@ -1760,6 +1788,35 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
     default: break;
   }
   return rc;
+}
+
+}  // namespace
+
+extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_cache, const void* v_cache,
+                                              int32_t num_pages, const int32_t* cu_seqlens_q,
+                                              const int32_t* q_start_pos, const int32_t* context_lens,
+                                              const int32_t* block_tables, int32_t bt_stride, int32_t num_rows,
+                                              int32_t num_tokens, int64_t context_total, int32_t H_q, int32_t H_kv,
+                                              int32_t D, int32_t page_size, float scale, void* out, void* workspace,
+                                              size_t ws_bytes, ms_stream_t stream) {
+  bool launched = false;
+  return attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens, block_tables,
+                        bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D, page_size, scale, out,
+                        workspace, ws_bytes, stream, false, 0, &launched);
+}
+
+extern "C" MS_API int ms_test_attention_stall(const void* q_rot, const void* k_cache, const void* v_cache,
+                                              int32_t num_pages, const int32_t* cu_seqlens_q,
+                                              const int32_t* q_start_pos, const int32_t* context_lens,
+                                              const int32_t* block_tables, int32_t bt_stride, int32_t num_rows,
+                                              int32_t num_tokens, int64_t context_total, int32_t H_q, int32_t H_kv,
+                                              int32_t D, int32_t page_size, float scale, void* out, void* workspace,
+                                              size_t ws_bytes, int64_t wait_limit_ns, ms_stream_t stream) {
+  if (wait_limit_ns < 100000 || wait_limit_ns > 2000000000ll) return MS_ERR_ARG;  // 0.1 ms .. 2 s
+  bool launched = false;
+  return attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens, block_tables,
+                        bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D, page_size, scale, out,
+                        workspace, ws_bytes, stream, false, wait_limit_ns, &launched);
 }
 
 extern "C" MS_API int ms_read_status(int32_t* dev_status, ms_stream_t stream, int32_t* host_status) {
@@ -1824,22 +1881,25 @@ extern "C" MS_API int ms_mixed_step_attention_noalloc(const void* q_rot, const v
   if (num_rows < 0 || num_tokens < 0 || context_total < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 ||
       (D != 64 && D != 128))
     return MS_ERR_ARG;
-  if (num_rows == 0) return MS_OK;
   const size_t need = ws_layout(num_rows, num_tokens, context_total, H_q, H_kv, D).total;
   if (need > kNoAllocScratchBytes) return MS_ERR_SCRATCH;
   void* scratch = nullptr;
   const int rc0 = scratch_address(&scratch);
   if (rc0 != MS_OK) return rc0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents: its status word and queue
-  // counters must start this call at zero
-  if (cudaMemsetAsync(scratch, 0, H_WORDS * sizeof(int32_t), st) != cudaSuccess) return MS_ERR_CUDA;
-  const int rc = ms_mixed_step_attention(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos,
-                                         context_lens, block_tables, bt_stride, num_rows, num_tokens, context_total,
-                                         H_q, H_kv, D, page_size, scale, out, scratch, kNoAllocScratchBytes, stream);
+  // The array keeps the previous call's contents.  The prologue zeroes its
+  // status word before this call can set a bit (it also resets the queue
+  // counters); no separate clearing launch sits between the append and the
+  // prologue, so the prologue still overlaps the append.
+  bool launched = false;
+  const int rc = attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens,
+                                block_tables, bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D,
+                                page_size, scale, out, scratch, kNoAllocScratchBytes, stream, true, 0, &launched);
   if (rc != MS_OK) return rc;
-  if (dev_status != nullptr &&
-      cudaMemcpyAsync(dev_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return MS_ERR_CUDA;
+  if (dev_status != nullptr) {
+    const cudaError_t e = launched ? cudaMemcpyAsync(dev_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, st)
+                                   : cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return MS_ERR_CUDA;
+  }
   return MS_OK;
 }

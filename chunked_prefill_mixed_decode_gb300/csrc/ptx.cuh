@@ -126,10 +126,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 
 // As mbar_wait, with n polls before the clock starts: a wait on the latency-critical
 // path then reads no timer (about 100 cycles) when the phase completes soon.
-__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity, const volatile int* abort, int n) {
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity, const volatile int* abort, int n,
+                                               uint64_t limit_ns = 2000000000ull) {
   for (int i = 0; i < n; ++i)
     if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait(bar, parity, abort);
+  return mbar_wait(bar, parity, abort, limit_ns);
 }
 
 // named barrier among `count` threads (a multiple of 32); id 0 is __syncthreads

@@ -181,9 +181,14 @@ MS_API int ms_rope_table(int32_t max_pos, int32_t D, double base, float* cos_tab
  *   positions, slot_mapping  device int32 [T]
  *   cos_tab, sin_tab         device fp32 [max_pos, D/2] (ms_rope_table)
  *   k_cache, v_cache         device bf16 [num_pages, H_kv, 16, D]
- *   dev_status               device int32 status word or NULL; out-of-range
- *                            slots and positions are skipped and, when given,
- *                            recorded there (MS_STATUS_BAD_SLOT / _POSITION)
+ *   dev_status               device int32 status word or NULL.  Slot -1 is
+ *                            the one "no write" value; any other negative
+ *                            slot, or one past the pool, writes nothing and
+ *                            sets MS_STATUS_BAD_SLOT.  A token whose position
+ *                            lies outside the table writes nothing at all
+ *                            (no q_rot row, no K, no V) and sets
+ *                            MS_STATUS_BAD_POSITION.  Bits are recorded only
+ *                            when dev_status is given.
  * All tensor pointers 16-byte aligned.  T == 0 is a no-op.
  * Errors: MS_ERR_ARG, MS_ERR_CUDA. */
 MS_API int ms_kv_append_rope(const void* q, const void* k, const void* v,
@@ -252,9 +257,11 @@ MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_cache, const
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array per device and it keeps the last
- * call's contents: each call clears its status word and work counters on
- * `stream` before the kernels run, so calls that overlap on the GPU (other
- * streams, other host threads) race and must be serialised by the caller.
+ * call's contents: each call's first kernel clears the status word and the
+ * work counters before anything of the call can set them, so calls that
+ * overlap on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller.  All argument checks come before anything is
+ * enqueued: a call that returns an error has put nothing on the stream.
  *
  * Arguments are those of ms_mixed_step_attention without the workspace, plus
  * dev_status: device int32 or NULL; when given, it is overwritten on `stream`
@@ -270,6 +277,31 @@ MS_API int ms_mixed_step_attention_noalloc(const void* q_rot, const void* k_cach
                                            int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D,
                                            int32_t page_size, float scale, void* out, int32_t* dev_status,
                                            ms_stream_t stream);
+
+/* ms_test_attention_stall -- test hook for the bounded device waits, not for
+ * production use.  It enqueues ms_mixed_step_attention exactly as that call
+ * would, except that the producer warp of every CTA's chunk phase publishes no
+ * work item and issues no copy, as a producer that had stopped would, and
+ * every chunk-phase wait gives up after wait_limit_ns (instead of 2 s).  The
+ * other roles of each CTA then wait for an item that never comes: the first
+ * wait that runs out sets MS_STATUS_TIMEOUT in the workspace's status word,
+ * the CTA unwinds (nothing is in flight), frees its tensor memory and
+ * returns.  The chunk rows' outputs are left unwritten.  The workspace stays
+ * usable: the next ms_mixed_step_attention on it computes the step normally.
+ * It checks the library's own failure detection (the pages have no
+ * counterpart) and faults nothing.  Arguments as ms_mixed_step_attention,
+ * plus wait_limit_ns in
+ * [100000, 2000000000].
+ * Errors: MS_ERR_ARG, MS_ERR_CUDA. */
+MS_API int ms_test_attention_stall(const void* q_rot, const void* k_cache, const void* v_cache,
+                                   int32_t num_pages,
+                                   const int32_t* cu_seqlens_q, const int32_t* q_start_pos,
+                                   const int32_t* context_lens, const int32_t* block_tables,
+                                   int32_t bt_stride, int32_t num_rows, int32_t num_tokens,
+                                   int64_t context_total,
+                                   int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
+                                   void* out, void* workspace, size_t ws_bytes, int64_t wait_limit_ns,
+                                   ms_stream_t stream);
 
 /* ---- Multi-round engine (host) ------------------------------------------
  * A page pool with full-input admission and a plan/commit round driver over
