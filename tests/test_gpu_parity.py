@@ -5,6 +5,8 @@ Bar: metadata, K/V pool and q_rot bit-exact; attention output within
 bf16 out); the GPU's chunked prefill matches its own full prefill within the
 same bound.
 """
+import time
+
 import numpy as np
 import pytest
 
@@ -251,6 +253,111 @@ def test_inconsistent_metadata_is_flagged(env):
     assert ms.read_status(case.ws) & ms.STATUS_BAD_META
 
 
+def test_append_bad_position_and_negative_slot(env):
+    """A token whose position lies outside the cos/sin table writes nothing (no K, no V) and sets
+    BAD_POSITION; slot -1 is the one silent "no write" value, any other negative slot sets BAD_SLOT."""
+    torch, ms, step = env
+    wl = workloads.small_mixed(seed=43, H_q=4, H_kv=2, D=64, dec_ctx=(20, 33), prompts=((0, 6),))
+    case = Case(env, wl, _states(wl), seed=4)
+    b = case.batch
+    bad_pos = torch.full_like(b.positions, case.cos.shape[0] + 3)
+    ms.kv_append_rope(case.q, case.k, case.v, bad_pos, b.slot_mapping, case.cos, case.sin, case.k_cache,
+                      case.v_cache, q_rot=case.q_rot, dev_status=case.status)
+    torch.cuda.synchronize()
+    st = ms.read_status(case.status)
+    assert st & ms.STATUS_BAD_POSITION and not st & ms.STATUS_BAD_SLOT, st
+    np.testing.assert_array_equal(workloads.bf16_bits(case.k_cache), case.k_in)
+    np.testing.assert_array_equal(workloads.bf16_bits(case.v_cache), case.v_in)
+    slots = b.slot_mapping.clone()
+    slots[0] = -2
+    slots[1:] = -1
+    ms.kv_append_rope(case.q, case.k, case.v, b.positions, slots, case.cos, case.sin, case.k_cache,
+                      case.v_cache, q_rot=case.q_rot, dev_status=case.status)
+    torch.cuda.synchronize()
+    assert ms.read_status(case.status) == ms.STATUS_BAD_SLOT
+    np.testing.assert_array_equal(workloads.bf16_bits(case.k_cache), case.k_in)
+    np.testing.assert_array_equal(workloads.bf16_bits(case.v_cache), case.v_in)
+
+
+# bf16 bit patterns a recycled page may hold: quiet NaN, +Inf, -Inf, NaN with every bit set
+_GARBAGE = np.array([0x7FC0, 0x7F80, 0xFF80, 0xFFFF], dtype=np.uint16)
+
+
+def _poison_unread_slots(case):
+    """Fill every pool slot that no row of the step reads (past each row's context in its last page)
+    with non-finite bf16 patterns, on the device and in the host copies the oracle starts from."""
+    torch = pytest.importorskip("torch")
+    meta, wl = case.meta, case.wl
+    kp, vp = case.k_in.copy(), case.v_in.copy()
+    n_poison = 0
+    for s in range(meta["num_rows"]):
+        table = wl.requests[int(meta["row_req"][s])].block_table
+        L = int(meta["context_lens"][s])
+        for j in range(L, 16 * len(table)):
+            page, off = int(table[j // 16]), j % 16
+            pat = np.resize(np.roll(_GARBAGE, j), kp.shape[-1])
+            kp[page, :, off, :] = pat
+            vp[page, :, off, :] = pat[::-1]
+            n_poison += 1
+    dev = case.k_cache.device
+    case.k_cache.copy_(torch.from_numpy(kp.view(np.int16)).view(torch.bfloat16).to(dev))
+    case.v_cache.copy_(torch.from_numpy(vp.view(np.int16)).view(torch.bfloat16).to(dev))
+    case.k_in, case.v_in = kp, vp
+    return n_poison
+
+
+@pytest.mark.parametrize("H_q,H_kv,D", [(8, 2, 128), (4, 4, 64), (8, 1, 128), (8, 8, 128)])
+def test_nonfinite_garbage_past_the_context_is_never_used(env, H_q, H_kv, D):
+    """zwjcode section 07: the query at chunk index i sees keys 0..c+i and nothing else.  A recycled
+    page holds anything, so the slots past every row's context (the tail of its last page) hold NaN
+    and +-Inf bit patterns here; decode rows and chunk rows (ragged tiles at D = 64 and 128) must stay
+    within tolerance of the oracle, which never reads those slots."""
+    wl = workloads.small_mixed(seed=H_q * 7 + H_kv + D, H_q=H_q, H_kv=H_kv, D=D,
+                               dec_ctx=(0, 5, 14, 17, 40, 100, 333),
+                               prompts=((0, 70), (33, 130), (16, 5), (250, 3)))
+    case = Case(env, wl, _states(wl), seed=12)
+    assert _poison_unread_slots(case) > 0
+    case.run(env)
+    T = case.meta["num_tokens"]
+    ref_meta, (q_rot, kp, vp) = case.oracle_append()
+    np.testing.assert_array_equal(workloads.bf16_bits(case.k_cache), kp)
+    np.testing.assert_array_equal(workloads.bf16_bits(case.v_cache), vp)
+    ref = oracle.attention_all(q_rot, kp, vp, ref_meta, wl.H_kv)
+    got = workloads.bf16_bits(case.out[:T])
+    assert np.isfinite(oracle.bf16_to_f64(got)).all()
+    n_dec = case.meta["num_decodes"]
+    _check_attention(got[:n_dec], ref[:n_dec], "decode rows next to garbage")
+    _check_attention(got[n_dec:], ref[n_dec:], "chunk rows next to garbage")
+
+
+def test_stalled_chunk_phase_times_out_and_the_workspace_recovers(env):
+    """Failure detection of the persistent kernel: with every chunk-phase producer stopped (the
+    ms_test_attention_stall hook) the chunk-phase waits give up after 1 ms, the call ends, the
+    status word carries STATUS_TIMEOUT, and the next ordinary call on the same workspace (whose
+    kernel must allocate the tensor memory the stalled one held) matches the oracle again."""
+    torch, ms, step = env
+    wl = workloads.small_mixed(seed=45, H_q=8, H_kv=2, D=128)
+    case = Case(env, wl, _states(wl), seed=6).run(env)
+    T = case.meta["num_tokens"]
+    ref_meta, (q_rot, kp, vp) = case.oracle_append()
+    ref = oracle.attention_all(q_rot, kp, vp, ref_meta, wl.H_kv)
+    b = case.batch
+    args = (case.q_rot, case.k_cache, case.v_cache, b.cu_seqlens_q, b.q_start_pos, b.context_lens,
+            b.block_tables, b.context_total)
+    for attempt in range(2):
+        stalled = torch.zeros_like(case.out)
+        t0 = time.perf_counter()
+        ms.test_attention_stall(*args, stalled, case.ws, wait_limit_ns=1_000_000)
+        torch.cuda.synchronize()
+        assert time.perf_counter() - t0 < 10.0
+        assert ms.read_status(case.ws) & ms.STATUS_TIMEOUT, f"attempt {attempt}: no timeout recorded"
+        again = torch.zeros_like(case.out)
+        ms.mixed_step_attention(*args, again, case.ws)
+        torch.cuda.synchronize()
+        assert ms.read_status(case.ws) == 0
+        _check_attention(workloads.bf16_bits(again[:T]), ref, f"call after stall {attempt}")
+
+
 # ------------------------------------------------------------------ full-size configurations (sampled)
 
 def _sampled_parity(env, wl, seed, n_dec_rows=48, n_chunk_tokens=48, heads=None):
@@ -270,7 +377,11 @@ def _sampled_parity(env, wl, seed, n_dec_rows=48, n_chunk_tokens=48, heads=None)
     dec_rows = sorted(set(rng.choice(n_dec, size=min(n_dec, n_dec_rows), replace=False).tolist())) if n_dec else []
     chunk_tok = sorted(set(rng.choice(np.arange(n_dec, T), size=min(T - n_dec, n_chunk_tokens),
                                       replace=False).tolist()) | ({n_dec, T - 1} if T > n_dec else set()))
-    tokens = dec_rows + chunk_tok
+    forced = _hardest_tokens(meta, wl.H_q // wl.H_kv)
+    every = sorted(set(dec_rows) | set(chunk_tok) | forced)
+    # decodes past LONG_KEYS keys go through _long_decode_parity (one row's pages at a time)
+    long_dec = [t for t in every if t < n_dec and meta["context_lens"][t] > LONG_KEYS]
+    tokens = [t for t in every if t not in set(long_dec)]
     ref_meta = oracle.batch_metadata(oracle.schedule(states, wl.token_budget, wl.max_chunk)[0], _tables(wl),
                                      len(states), num_decodes=n_dec)
     for key in ("cu_seqlens_q", "positions", "slot_mapping", "context_lens", "q_start_pos"):
@@ -309,6 +420,74 @@ def _sampled_parity(env, wl, seed, n_dec_rows=48, n_chunk_tokens=48, heads=None)
     g = np.stack([got[t, h] for t, h in select])
     r = np.stack([ref[(t, h)] for t, h in select])
     _check_attention(g, r, wl.name)
+    if long_dec:
+        _long_decode_parity(env, case, ref_meta, long_dec, sorted({0, H_q - 1}))
+    return len(tokens) + len(long_dec)
+
+
+LONG_KEYS = 32768
+
+
+def _long_decode_parity(env, case, ref_meta, rows, heads):
+    """Decode rows too long to copy the pool around (64K-128K keys): the row's appended slot is checked
+    bit-exact against the oracle's rotation of its token, then the oracle attends over the row's own
+    pages of one KV head at a time, gathered from the device pool after the step."""
+    torch, ms, step = env
+    wl = case.wl
+    G = wl.H_q // wl.H_kv
+    dev = case.k_cache.device
+    got = workloads.bf16_bits(case.out)
+    for t in rows:  # a decode row's token index is its row index
+        ctx = int(ref_meta["context_lens"][t])
+        n_pages = -(-ctx // 16)
+        table = ref_meta["block_tables"][t][:n_pages].astype(np.int64)
+        slot = int(ref_meta["slot_mapping"][t])
+        zero = np.zeros((1,) + tuple(case.k_cache.shape[1:]), np.uint16)
+        q_rot1, k1, v1 = oracle.kv_append(workloads.bf16_bits(case.q[t:t + 1]), workloads.bf16_bits(case.k[t:t + 1]),
+                                          workloads.bf16_bits(case.v[t:t + 1]), ref_meta["positions"][t:t + 1],
+                                          np.array([slot % 16]), zero, zero)
+        np.testing.assert_array_equal(workloads.bf16_bits(case.q_rot[t:t + 1]), q_rot1)
+        page = torch.tensor([slot // 16], device=dev)
+        np.testing.assert_array_equal(workloads.bf16_bits(case.k_cache.index_select(0, page))[0, :, slot % 16],
+                                      k1[0, :, slot % 16])
+        np.testing.assert_array_equal(workloads.bf16_bits(case.v_cache.index_select(0, page))[0, :, slot % 16],
+                                      v1[0, :, slot % 16])
+        pidx = torch.from_numpy(table).to(dev)
+        for kvh in sorted({h // G for h in heads}):
+            kp = workloads.bf16_bits(case.k_cache.index_select(0, pidx)[:, kvh:kvh + 1])
+            vp = workloads.bf16_bits(case.v_cache.index_select(0, pidx)[:, kvh:kvh + 1])
+            sub = {"cu_seqlens_q": np.array([0, 1]), "q_start_pos": np.array([ctx - 1]),
+                   "block_tables": np.arange(n_pages)[None, :]}
+            hs = [h for h in heads if h // G == kvh]
+            ref = oracle.attention_rows(q_rot1[:, kvh * G:(kvh + 1) * G], kp, vp, sub, 1,
+                                        select=[(0, h - kvh * G) for h in hs])
+            g = np.stack([got[t, h] for h in hs])
+            r = np.stack([ref[(0, h - kvh * G)] for h in hs])
+            _check_attention(g, r, f"{wl.name} decode row {t} ({ctx} keys)")
+
+
+def _hardest_tokens(meta, G):
+    """Tokens every full-size check includes besides its random sample: the longest decode row
+    (which also has the most splits to merge), every decode of 64K keys or more, and the first and
+    last two tokens of the first and last 128-row query tile of every chunk row (the tile that
+    starts the causal diagonal and the one that ends the chunk, with its ragged tail)."""
+    cu, c0 = meta["cu_seqlens_q"], meta["q_start_pos"]
+    n_dec = meta["num_decodes"]
+    out = set()
+    if n_dec:
+        ctx = meta["context_lens"][:n_dec]
+        out.add(int(np.argmax(ctx)))
+        out |= {int(s) for s in np.nonzero(ctx >= 65536)[0]}
+    tpt = 128 // G
+    for s in range(n_dec, meta["num_rows"]):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b - a < 2:
+            continue
+        last_tile = a + ((b - a - 1) // tpt) * tpt
+        for t in (a, a + 1, min(a + tpt, b) - 2, min(a + tpt, b) - 1, last_tile, last_tile + 1, b - 2, b - 1):
+            if a <= t < b:
+                out.add(t)
+    return out
 
 
 @pytest.mark.slow
