@@ -2,19 +2,24 @@
 """Mixed-step attention throughput on GB300: tokens/s and fraction of the step roofline.
 
 One timed step is one pass of the whole hot path -- ms_kv_append_rope then
-ms_mixed_step_attention -- over every batch of the workload.  The default
-workload is the 7B-like MHA layer at token budget 512: 64 running decodes
-(c ~ U[512, 4096]) next to a 448-token chunk of a 4096-token prompt, at each of
-the prompt's nine prefix offsets 0, 448, ..., 3584 (nine batches per step,
-4608 tokens).  Inputs are seeded synthetic bf16 (N(0,1)); the KV pool (~2.5 GB)
-is larger than L2, so no flush is needed between steps.
+ms_mixed_step_attention -- over every batch of a workload.  By default all four
+full-size workloads run one after another and print ONE JSON line: its top level
+is the largest single-GPU step, the long-context bimodal batch (the last
+4096-token chunk of a 32768-token prompt next to 512 decodes, 10 % of them at
+64K-128K keys; 21 GB of KV read per step), and ``per_config`` carries the 7B MHA
+(budget 512, nine batches per step), 13B MHA (budget 2048) and 8B GQA (budget
+8192) steps with the same fields: value, ms_per_step, roofline (with the DRAM
+traffic of a committed ncu capture of the current source), step_roofline, e2e
+and cpu_baseline.  Inputs are seeded synthetic bf16 (N(0,1)); every KV pool is
+larger than L2, so no flush is needed between steps.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config all|NAME] [--impl ours|reference]
   python bench.py --timeline | --split   (supplementary: step-latency timeline; decode/chunk split)
 
 Under torchrun each rank runs its own replica (weak scaling); timing is the
-max over ranks.  --impl reference times the fp64 CPU oracle on a bounded sample
-of the same workload.
+max over ranks.  --impl reference times the fp64 CPU oracle on the bounded
+sample of the top-level workload that cpu_baseline also times (same rule, same
+--steps and --warmup), on one thread, and adds the same path over every host core.
 """
 from __future__ import annotations
 
@@ -176,12 +181,26 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- our arm
 
+ALL_CONFIGS = ["long_bimodal_b4608", "mha7b_b512", "mha13b_b2048", "gqa8b_b8192"]
+
+
+def config_block(name: str, wls, world: int) -> dict:
+    """The ``config`` object of a line: the same for both arms (nothing in it is measured)."""
+    wl0 = wls[0]
+    pool_gb = 2 * wl0.num_pages * wl0.H_kv * wl0.page_size * wl0.D * 2 / 1e9
+    tokens = 0
+    for wl in wls:
+        n_dec = sum(1 for r in wl.requests if r.remaining == 0)
+        tokens += min(wl.token_budget, n_dec + sum(r.remaining for r in wl.requests if r.remaining > 0))
+    return {"workload": describe(name, wls), "tokens_per_step": tokens, "batches_per_step": len(wls),
+            "l2": f"inputs larger than L2 (KV pool {pool_gb:.2f} GB); no flush", "parallelism": f"replicas x{world}"}
+
+
 def run_ours(args, world, rank, local):
     import torch
 
     import chunked_prefill_mixed_decode_gb300 as ms
     from chunked_prefill_mixed_decode_gb300 import build as msbuild
-    from chunked_prefill_mixed_decode_gb300 import roofline, step
 
     msbuild.build()
     dist = None
@@ -189,7 +208,30 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(device)
     if world > 1:
         dist = dist_init("nccl")
-    wls = load_workload(args.config)
+    names = ALL_CONFIGS if args.config == "all" else [args.config]
+    results = {}
+    for name in names:
+        results[name] = measure_config(name, args, ms, world, rank, device, dist)
+        torch.cuda.empty_cache()
+    top = dict(results[names[0]])
+    if len(names) > 1:
+        top["per_config"] = {n: {k: v for k, v in results[n].items() if k not in ("metric", "n_gpus", "steps",
+                                 "warmup", "higher_is_better", "scaling", "vs_baseline", "dtype", "data")}
+                             for n in names[1:]}
+    if rank == 0:
+        print(json.dumps(top), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def measure_config(name, args, ms, world, rank, device, dist) -> dict:
+    """Device time, roofline, end-to-end rate and CPU baseline of one workload."""
+    import torch
+
+    from chunked_prefill_mixed_decode_gb300 import roofline, step
+
+    wls = load_workload(name)
     wl0 = wls[0]
     peaks, peak_src = read_peaks()
 
@@ -235,14 +277,14 @@ def run_ours(args, world, rank, local):
         one_step()
     torch.cuda.synchronize()
     if ms.read_status(status) or ms.read_status(ws):
-        raise RuntimeError("device status set during warm-up")
+        raise RuntimeError(f"{name}: device status set during warm-up")
 
     # ---- timed device region
     n_sub = len(subs)
     attn_events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                     for _ in range(n_sub)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(device.index if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    sampler = ClockSampler(device.index if "CUDA_VISIBLE_DEVICES" not in os.environ else device.index)
     sampler.start()
     if dist is not None:
         dist.barrier()
@@ -257,7 +299,7 @@ def run_ours(args, world, rank, local):
     clocks = sampler.stop()
     elapsed_ms = t0.elapsed_time(t1)
     if ms.read_status(status) or ms.read_status(ws):
-        raise RuntimeError("device status set during the timed region")
+        raise RuntimeError(f"{name}: device status set during the timed region")
     attn_ms = [[attn_events[it][j][0].elapsed_time(attn_events[it][j][1]) for it in range(args.steps)]
                for j in range(n_sub)]
     tokens_per_step = sum(s["meta"]["num_tokens"] for s in subs)
@@ -283,16 +325,19 @@ def run_ours(args, world, rank, local):
         achieved = flops_avg / (grp_avg_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4), "traffic": None}
-    cap = captured_traffic(args.config)
-    if cap is not None and roof["bound"] == "hbm" and "append_dram_bytes" in cap:
+    cap = captured_traffic(name)
+    if cap is not None and "append_dram_bytes" in cap:
         # scale the captured batch's DRAM bytes (append + attention) to the average batch
         b = int(cap.get("batch", 0))
         scale = grp_bytes_avg / subs[b]["counts"]["step_bytes"]
         roof["traffic"] = int((cap["dram_bytes_read"] + cap["dram_bytes_write"] + cap["append_dram_bytes"]) * scale)
-        roof["traffic_source"] = f"ncu capture of batch {b} (append + attention kernels), scaled by algorithmic bytes"
+        roof["traffic_source"] = (f"ncu capture of batch {b} (append + attention kernels)"
+                                  + (", scaled by algorithmic bytes" if n_sub > 1 else ""))
+        roof["traffic_vs_alg_bytes"] = round(roof["traffic"] / grp_bytes_avg, 4)
     roof["kernel"] = ("one batch of the path: ms_kv_append_rope + ms_mixed_step_attention "
                       "(append, prologue, items and persistent attention_kernel launches)")
-    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    roof["peak_source"] = (f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+                           + ("; sustained bf16 (kernel timed inside a step)" if roof["bound"] == "tensor" else ""))
     roof["per_launch"] = {"alg_bytes": int(grp_bytes_avg), "alg_flops": int(flops_avg),
                           "avg_ms": round(grp_avg_ms, 4)}
     step_bytes = sum(s["counts"]["step_bytes"] for s in subs)
@@ -301,6 +346,8 @@ def run_ours(args, world, rank, local):
     step_roof = {"alg_bytes": int(step_bytes), "alg_flops": int(step_flops),
                  "t_roof_ms": round(t_roof * 1e3, 4), "t_meas_ms": round(ms_per_step, 4),
                  "frac_of_roofline": round(t_roof * 1e3 / ms_per_step, 4),
+                 "bound": "hbm" if step_bytes / (peaks["hbm_gbs"] * 1e9) >= step_flops / (
+                     peaks["bf16_tflops_sustained"] * 1e12) else "tensor",
                  "vs_nominal_8TBps": round(step_bytes / (8000e9) * 1e3 / ms_per_step, 4)}
 
     # ---- end to end through the public API with host buffers
@@ -310,19 +357,14 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16; KV pool larger than L2)",
-        "config": {"workload": describe(args.config, wls), "tokens_per_step": tokens_per_step,
-                   "batches_per_step": n_sub, "l2": "inputs larger than L2 (KV pool "
-                   f"{2 * k_cache.numel() * 2 / 1e9:.2f} GB); no flush", "parallelism": f"replicas x{world}"},
+        "config": config_block(name, wls, world),
         "roofline": roof, "step_roofline": step_roof, "e2e": e2e,
         "gpu_launches": 4 * n_sub * args.steps, "clocks": clocks,
     }
+    del subs, ws, pool, k_cache, v_cache
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
+        line["cpu_baseline"] = cpu_baseline(name, args)
+    return line
 
 
 def run_e2e(args, ms, step, subs, cos, sin, k_cache, v_cache, ws, status, device, stream, dist):
@@ -390,16 +432,83 @@ def run_e2e(args, ms, step, subs, cos, sin, k_cache, v_cache, ws, status, device
 
 
 # ---------------------------------------------------------------------------- oracle (CPU) timing
+#
+# Both arms time the oracle on the same sample of a workload: its first batch, with its decodes taken
+# evenly spaced in input order (so a bimodal mix keeps its shape) and each chunk row cut to its first
+# tokens, scaled by one fraction f.  f is the largest value whose estimated oracle time fits the
+# per-step budget, from a fixed cost model (seconds per gathered key per KV head, and per key per
+# (token, head) pair) -- no timing probe -- so both arms pick the same sample for the same --steps and
+# --warmup.  The budget is about two minutes over the reference arm's warm-up and timed steps.
 
-def _oracle_sample_workload(wl, n_dec: int, n_chunk: int, seed: int):
-    """The same step shape restricted to its first n_dec decodes and an n_chunk-token chunk."""
-    rng = np.random.default_rng(seed)
-    dec = [(r.cached_len, 0) for r in wl.requests if r.remaining == 0][:n_dec]
-    prm = [(r.cached_len, r.remaining) for r in wl.requests if r.remaining > 0][:1]
-    states = dec + ([(prm[0][0], min(prm[0][1], n_chunk))] if prm and n_chunk > 0 else [])
+ORACLE_S_PER_GATHERED_KEY = 1.5e-6   # one KV head, D = 128: page gather + fp64 conversion of K and V
+ORACLE_S_PER_ATTENDED_KEY = 2.0e-7   # one (token, head) pair, D = 128: scores, exponentials, weighted sum
+
+
+def _oracle_sample_states(wl, f_dec: float, f_chunk: float):
+    dec = [r for r in wl.requests if r.remaining == 0]
+    prm = [r for r in wl.requests if r.remaining > 0]
+    n_dec = min(len(dec), max(1, int(round(len(dec) * f_dec)))) if dec else 0
+    picked = [dec[(i * len(dec)) // n_dec] for i in range(n_dec)] if n_dec else []
+    left = wl.token_budget - len(dec)
+    chunks = []
+    for r in prm:  # the chunk rows the full step schedules, each cut to its first tokens
+        take = min(r.remaining, left)
+        if take <= 0:
+            break
+        left -= take
+        chunks.append((r, min(take, max(2, int(round(take * f_chunk))))))
+    return picked, chunks
+
+
+def _oracle_cost(wl, picked, chunks) -> float:
+    scale = wl.D / 128.0
+    t = 0.0
+    for r in picked:
+        keys = r.cached_len + 1
+        t += keys * (wl.H_kv * ORACLE_S_PER_GATHERED_KEY + wl.H_q * ORACLE_S_PER_ATTENDED_KEY) * scale
+    for r, n in chunks:
+        t += (r.cached_len + n) * wl.H_kv * ORACLE_S_PER_GATHERED_KEY * scale
+        t += n * wl.H_q * (r.cached_len + (n + 1) / 2) * ORACLE_S_PER_ATTENDED_KEY * scale
+    return t
+
+
+def _largest_fraction(cost, budget: float) -> float:
+    """Largest f in (0, 1] with cost(f) <= budget (bisection; the smallest sample if none fits)."""
+    if cost(1.0) <= budget:
+        return 1.0
+    lo, hi = 0.0, 1.0
+    for _ in range(30):
+        mid = (lo + hi) / 2
+        if cost(mid) <= budget:
+            lo = mid
+        else:
+            hi = mid
+    return max(lo, 1e-9)
+
+
+def oracle_sample(config: str, steps: int, warmup: int, step_seconds: float = 0.0):
+    """(sample workload, description) of the bounded oracle step for this workload and run length.
+    Decodes and chunk tokens each get half of the per-step budget (all of it when the step has
+    only one kind).  step_seconds > 0 overrides the budget derived from steps + warmup."""
+    wl = load_workload(config)[0]
+    budget = step_seconds if step_seconds > 0 else min(8.0, max(0.5, 120.0 / max(steps + warmup, 1)))
+    has_dec = any(r.remaining == 0 for r in wl.requests)
+    has_chunk = any(r.remaining > 0 for r in wl.requests)
+    share = budget / 2 if has_dec and has_chunk else budget
+    f_dec = _largest_fraction(lambda f: _oracle_cost(wl, _oracle_sample_states(wl, f, 0.0)[0], []), share)
+    f_chk = _largest_fraction(lambda f: _oracle_cost(wl, [], _oracle_sample_states(wl, 0.0, f)[1]), share)
+    picked, chunks = _oracle_sample_states(wl, f_dec, f_chk)
+    states = [(r.cached_len, 0) for r in picked] + [(r.cached_len, n) for r, n in chunks]
+    rng = np.random.default_rng(8)
     reqs, total = workloads.assign_pages(states, rng)
-    return workloads.Workload(wl.name + "_sample", wl.H_q, wl.H_kv, wl.D, len(dec) + n_chunk, reqs, total,
-                              seed=seed)
+    n_tok = len(picked) + sum(n for _, n in chunks)
+    sub = workloads.Workload(wl.name + "_sample", wl.H_q, wl.H_kv, wl.D, n_tok, reqs, total, seed=8)
+    long_dec = sum(1 for r in picked if r.cached_len >= 65536)
+    desc = (f"{len(picked)} decodes taken evenly from the first batch's {sum(1 for r in wl.requests if r.remaining == 0)}"
+            + (f" ({long_dec} of them 64K+)" if long_dec else "")
+            + f" + {', '.join(f'{n} tokens of the chunk at c = {r.cached_len}' for r, n in chunks) or 'no chunk'}"
+            + f", all {wl.H_q} heads (estimated {_oracle_cost(wl, picked, chunks):.2f} s per step)")
+    return sub, desc
 
 
 def _oracle_prepare(sub, seed):
@@ -412,54 +521,130 @@ def _oracle_prepare(sub, seed):
                 v=workloads.bf16_bits(v), kp=workloads.bf16_bits(kc), vp=workloads.bf16_bits(vc))
 
 
-def _oracle_run(prep):
-    """Time the oracle's whole path (schedule, metadata, append, attention) on one sampled step."""
+def _oracle_front(prep):
+    """Schedule, metadata and the RoPE append of the sampled step (the oracle's own order)."""
     import oracle
     sub = prep["sub"]
-    t = time.perf_counter()
     rows, _ = oracle.schedule(prep["states"], sub.token_budget)
     meta = oracle.batch_metadata(rows, prep["tables"], len(prep["states"]))
     T = meta["num_tokens"]
     q_rot, kp2, vp2 = oracle.kv_append(prep["q"][:T], prep["k"][:T], prep["v"][:T], meta["positions"],
                                        meta["slot_mapping"], prep["kp"], prep["vp"])
-    oracle.attention_all(q_rot, kp2, vp2, meta, sub.H_kv)
+    return meta, T, q_rot, kp2, vp2
+
+
+def _oracle_run(prep):
+    """Time the oracle's whole path (schedule, metadata, append, attention) on one sampled step."""
+    import oracle
+    t = time.perf_counter()
+    meta, T, q_rot, kp2, vp2 = _oracle_front(prep)
+    oracle.attention_all(q_rot, kp2, vp2, meta, prep["sub"].H_kv)
     return T, time.perf_counter() - t
 
 
-def _sample_size(wl, seconds):
-    n_dec_all = sum(1 for r in wl.requests if r.remaining == 0)
-    tok, sec = _oracle_run(_oracle_prepare(_oracle_sample_workload(wl, 2, 2, 7), 7))
-    n = int(max(2, min(seconds / max(sec / max(tok, 1), 1e-6), n_dec_all + 448)))
-    n_dec = min(n_dec_all, max(1, n // 2))
-    return n_dec, max(2, n - n_dec)
+# all-cores leg: the same oracle functions over (row, KV head) blocks in worker processes (spawned:
+# never forked from a process that holds a CUDA context).  The step's inputs -- q, k, v and the
+# cached pools, resident like the GPU's HBM copy -- are written once, untimed, to .npy files the
+# workers memory-map.  Per run the parent schedules and builds the metadata; each block appends its
+# row's new tokens for one KV head into a copy of that row's pages (oracle.kv_append) and attends a
+# share of the row's (token, head) pairs (oracle.attention_rows).
+_W = {}
 
 
-def cpu_baseline(config: str, budget_s: float = 15.0) -> dict:
-    """The oracle on one thread over a bounded sample: one batch of the workload (or the part of it that
-    fits the budget), repeated until about budget_s of CPU time has been spent."""
-    wl = load_workload(config)[0]
-    n_dec, n_chunk = _sample_size(wl, budget_s)
-    prep = _oracle_prepare(_oracle_sample_workload(wl, n_dec, n_chunk, 8), 8)
+def _worker_attend(args):
+    import oracle
+    path, t0, t1, c0, table, positions, kvh, G, tokens = args
+    if _W.get("path") != path:
+        _W.clear()
+        _W["path"] = path
+        _W.update({k: np.load(os.path.join(path, k + ".npy"), mmap_mode="r") for k in ("q", "k", "v", "kp", "vp")})
+    n = len(table)
+    mk = np.ascontiguousarray(_W["kp"][table, kvh:kvh + 1])
+    mv = np.ascontiguousarray(_W["vp"][table, kvh:kvh + 1])
+    # in the copy, logical page i of the row is page i, so a token's slot is its position
+    q_rot, mk, mv = oracle.kv_append(np.asarray(_W["q"][t0:t1, kvh * G:(kvh + 1) * G]),
+                                     np.asarray(_W["k"][t0:t1, kvh:kvh + 1]), np.asarray(_W["v"][t0:t1, kvh:kvh + 1]),
+                                     positions, positions, mk, mv)
+    meta = {"cu_seqlens_q": np.array([0, t1 - t0]), "q_start_pos": np.array([c0]),
+            "block_tables": np.arange(n)[None, :]}
+    res = oracle.attention_rows(q_rot, mk, mv, meta, 1, select=[(t - t0, h) for t in tokens for h in range(G)])
+    return len(res)
+
+
+def _oracle_run_parallel(prep, pool, n_workers, tmpdir):
+    """The oracle's path with its append and attention spread over worker processes."""
+    import oracle
+    t = time.perf_counter()
+    sub = prep["sub"]
+    rows, _ = oracle.schedule(prep["states"], sub.token_budget)
+    meta = oracle.batch_metadata(rows, prep["tables"], len(prep["states"]))
+    T = meta["num_tokens"]
+    H_q, H_kv = prep["q"].shape[1], sub.H_kv
+    G = H_q // H_kv
+    cu, c0, bt = meta["cu_seqlens_q"], meta["q_start_pos"], meta["block_tables"]
+    tasks = []
+    per_block = max(1, -(-T * H_kv // (4 * n_workers)))  # about four blocks of (token, KV head) per worker
+    for s in range(meta["num_rows"]):
+        a, b = int(cu[s]), int(cu[s + 1])
+        table = bt[s][: -(-(int(c0[s]) + b - a) // 16)].astype(np.int64)
+        pos = meta["positions"][a:b]
+        for kvh in range(H_kv):
+            for x in range(a, b, per_block):
+                tasks.append((tmpdir, a, b, int(c0[s]), table, pos, kvh, G, list(range(x, min(b, x + per_block)))))
+    tasks.sort(key=lambda tk: -(tk[3] + tk[2] - tk[1]) * len(tk[8]))  # longest first
+    n = sum(pool.map(_worker_attend, tasks, chunksize=1))
+    assert n == T * H_q
+    return T, time.perf_counter() - t
+
+
+def cpu_baseline(config: str, args) -> dict:
+    """The oracle on the bounded sample the reference arm times (same rule, same --steps/--warmup):
+    one thread, repeated for about args.cpu_seconds; then the same path with its attention over
+    every host core (worker processes), repeated likewise."""
+    sub, desc = oracle_sample(config, args.steps, args.warmup, args.oracle_step_seconds)
+    prep = _oracle_prepare(sub, 8)
     tok = sec = 0.0
     reps = 0
-    while sec < budget_s:
-        t, s = _oracle_run(prep)
+    while sec < args.cpu_seconds or reps == 0:
+        t, s_ = _oracle_run(prep)
         tok += t
-        sec += s
+        sec += s_
         reps += 1
-    return {"value": round(tok / sec, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n_dec} decodes + a {n_chunk}-token chunk of {config} (all {wl.H_q} heads), "
-                      f"run {reps} times, fp64 numpy, one thread, {sec:.1f} s"}
+    out = {"value": round(tok / sec, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": f"{desc}; fp64 numpy, one thread, {reps} runs, {sec:.1f} s"}
+    if not args.no_parallel_oracle:
+        out["all_cores"] = parallel_oracle(prep, args.cpu_seconds / 2)
+    return out
+
+
+def parallel_oracle(prep, seconds: float) -> dict:
+    import multiprocessing as mp
+    n_workers = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    with tempfile.TemporaryDirectory(prefix="ms_oracle_") as tmpdir, ctx.Pool(n_workers) as pool:
+        for k in ("q", "k", "v", "kp", "vp"):  # the step's inputs, resident before the clock starts
+            np.save(os.path.join(tmpdir, k + ".npy"), np.ascontiguousarray(prep[k]))
+        _oracle_run_parallel(prep, pool, n_workers, tmpdir)  # untimed: workers import numpy and the oracle
+        tok = sec = 0.0
+        reps = 0
+        while sec < seconds or reps == 0:
+            t, s_ = _oracle_run_parallel(prep, pool, n_workers, tmpdir)
+            tok += t
+            sec += s_
+            reps += 1
+    return {"value": round(tok / sec, 2), "unit": "tokens/s", "cores": n_workers, "kind": "oracle",
+            "how": f"append and attention over {n_workers} spawned worker processes by (row, KV head, token "
+                   f"block); schedule and metadata in the parent; {reps} runs, {sec:.1f} s"}
 
 
 def run_reference(args, world, rank):
-    """The oracle as the reference arm: each step a bounded sample of the same workload."""
+    """The oracle as the reference arm: each step the bounded sample that cpu_baseline also times."""
     if rank != 0:
         return
-    wl = load_workload(args.config)[0]
-    per_step = args.cpu_seconds * 6.0 / max(args.steps + args.warmup, 1)  # whole run within a few minutes
-    n_dec, n_chunk = _sample_size(wl, per_step)
-    prep = _oracle_prepare(_oracle_sample_workload(wl, n_dec, n_chunk, 8), 8)
+    name = ALL_CONFIGS[0] if args.config == "all" else args.config
+    wls = load_workload(name)
+    sub, desc = oracle_sample(name, args.steps, args.warmup, args.oracle_step_seconds)
+    prep = _oracle_prepare(sub, 8)
     for _ in range(args.warmup):
         _oracle_run(prep)
     tot_tok = tot_s = 0.0
@@ -468,14 +653,14 @@ def run_reference(args, world, rank):
         tot_tok += tk
         tot_s += s
     value = tot_tok / tot_s
-    sample = (f"{n_dec} decodes + a {n_chunk}-token chunk of {args.config} per step (all {wl.H_q} heads), "
-              f"fp64 numpy, one thread")
+    cpu = {"value": round(value, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": f"{desc}; fp64 numpy, one thread, {args.steps} runs"}
+    if not args.no_parallel_oracle:
+        cpu["all_cores"] = parallel_oracle(prep, min(args.cpu_seconds / 2, 8.0))
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(args.config, load_workload(args.config))}, "impl": "reference",
-            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "config": config_block(name, wls, world), "impl": "reference", "cpu_baseline": cpu,
             "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -717,12 +902,18 @@ def run_split(args, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="mha7b_b512", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--config", default="all", choices=["all"] + sorted(workloads.CONFIGS),
+                    help="one workload, or all four (the default): the line's top level is the long bimodal "
+                         "step, the others go under per_config")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-parallel-oracle", action="store_true", help="skip the all-cores oracle leg")
+    ap.add_argument("--oracle-step-seconds", type=float, default=0.0,
+                    help="estimated oracle seconds of one sampled step (default: about two minutes over "
+                         "--steps + --warmup, at most 8 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--timeline", action="store_true",
                     help="step-latency timeline around a long prompt's arrival (one JSON line)")
