@@ -112,8 +112,6 @@ struct AttnParams {
   int32_t num_sms;
   int32_t clear_status;  // the prologue zeroes the status word first (scratch owned by the library)
   int32_t test_stall;    // test hook: chunk-phase producers publish no work item (0 in every real call)
-  int32_t qt_per_item;   // 128-row Q tiles per chunk work item: 2 (one CTA) or 4 (a pair of CTAs)
-  int32_t ctas_per_item; // CTAs that run one chunk work item together: 1 or 2
   uint64_t wait_limit_ns;  // bound of every chunk-phase wait
   float scale_log2;
 };
@@ -174,11 +172,11 @@ __device__ __forceinline__ int find_in_prefix(const int32_t* pref, int n, int it
   return lo;
 }
 
-// Work items of one row: decode splits of `split` pages, or groups of qpi 128-row Q tiles.
-__device__ __forceinline__ int row_items(int kind, int c, int d, int tpt, unsigned split, int qpi) {
+// Work items of one row: decode splits of `split` pages, or pairs of 128-row Q tiles.
+__device__ __forceinline__ int row_items(int kind, int c, int d, int tpt, unsigned split) {
   if (kind == 0) return static_cast<int>((static_cast<unsigned>(c + kPage) / kPage + split - 1) / split);
   const int n_qt = (d + tpt - 1) / tpt;
-  return (n_qt + qpi - 1) / qpi;
+  return (n_qt + 1) >> 1;
 }
 
 // 128x128 tiles of a chunk row's Q tiles against their causal key ranges (the
@@ -308,7 +306,7 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
         sm.c[pos] = static_cast<int32_t>(c);
       } else {
         rows[pos] = s;
-        sm.pref[pos] = row_items(kind, c, d, tpt, split32, p.qt_per_item);
+        sm.pref[pos] = row_items(kind, c, d, tpt, split32);
         if (kind == 1) atomicAdd(&s_tiles, static_cast<unsigned long long>(chunk_tiles(c, d, tpt)) * p.H_kv);
       }
     }
@@ -320,7 +318,7 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
         for (int m = 0; m < n; ++m) rank += sm.key[m] > k;
         rows[rank] = sm.id[j];
         const int c = sm.c[j], d = sm.d[j];
-        sm.pref[rank] = row_items(kind, c, d, tpt, split32, p.qt_per_item);
+        sm.pref[rank] = row_items(kind, c, d, tpt, split32);
         if (kind == 1) atomicAdd(&s_tiles, static_cast<unsigned long long>(chunk_tiles(c, d, tpt)) * p.H_kv);
       }
       __syncthreads();
@@ -393,8 +391,7 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
       // comes in whole items, so n chunk CTAs need ceil(items / n) rounds of about
       // T / items each; decode runs on the other CTAs, capped by HBM.
       const float n0 = fminf(S - 1.f, fmaxf(1.f, rintf(__fdividef(T * g * S, B + T * g))));
-      // an item occupies ctas_per_item CTAs: count CTA-items of equal SM time
-      const float n_it = fmaxf(static_cast<float>(hdr[H_NCH_ITEMS]) * p.ctas_per_item, 1.f);
+      const float n_it = fmaxf(static_cast<float>(hdr[H_NCH_ITEMS]), 1.f);
       const float t_item = T / n_it;
       float best = 3.0e38f;
       n = n0;
@@ -852,8 +849,9 @@ struct ChBars {
 static_assert(sizeof(ChBars) <= 1024, "chunk-phase barrier block exceeds its reserved space");
 static_assert(DecCfg<128, 8>::SMEM <= 232448 && DecCfg<64, 8>::SMEM <= 232448 && DecCfg<128, 4>::WARPS == 12,
               "decode rings exceed the per-CTA shared-memory limit");
-static_assert(ChCfg<64>::SMEM <= 232448, "chunk phase exceeds the per-CTA shared-memory limit");
-static_assert(ChCfg<64>::KVS <= 8, "more K/V stages than barriers");
+static_assert(ChCfg<128>::SMEM <= 232448 && ChCfg<64>::SMEM <= 232448,
+              "chunk phase exceeds the per-CTA shared-memory limit");
+static_assert(ChCfg<128>::KVS <= 8 && ChCfg<64>::KVS <= 8, "more K/V stages than barriers");
 
 // wait by lane 0, result and ordering shared with the whole warp
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
@@ -1400,588 +1398,18 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
   (void)n_items;
 }
 
-// ----------------------------------------------------------------------------
-// chunk rows on a pair of CTAs (D = 128): cta_group::2 tensor cores
-// ----------------------------------------------------------------------------
-//
-// The two CTAs of a cluster share every K/V tile.  A work item is four
-// consecutive 128-row Q tiles of one chunk row and KV head, run as two
-// streams of M = 256 rows: stream t holds Q tile 4i + 2t in the leader (rank
-// 0) and 4i + 2t + 1 in the other CTA, each in its own shared and tensor
-// memory.  Each CTA loads half of each 64-key K/V tile: K pages 2r and 2r + 1
-// (the B operand of S = Q K^T is split by keys) and V columns 64r .. 64r + 63
-// of all four pages (the B operand of O += P V is split by columns), so an SM
-// moves 16 KB per tile for 256 query rows instead of 32 KB.  The leader issues
-// every MMA (three issuer warps, as in the single-CTA layout); the completions
-// arrive in both CTAs, and each CTA's two softmax groups work on their own
-// rows, reporting P to the leader's barriers.  Every wait is bounded; the
-// copies of both CTAs count on the leader's barriers.
-struct PairCfg {
-  static constexpr int Q_BYTES = 2 * kQSlab;             // one 128-row Q tile, two 64-column slabs (32 KB)
-  static constexpr int BOX = kPage * 128;                // one TMA box: 16 rows x 64 columns (2 KB)
-  static constexpr int K_SLAB = 32 * 128;                // this CTA's 32 keys of one 64-column slab
-  static constexpr int K_BYTES = 2 * K_SLAB;
-  static constexpr int V_PAGE = BOX;                     // one page of this CTA's 64 V columns
-  static constexpr int V_BYTES = kTilePages * V_PAGE;
-  static constexpr int STAGE = K_BYTES + V_BYTES;        // 16 KB per K/V tile
-  static constexpr int KVS = 8;                          // K/V pipeline stages
-  static constexpr int KV_OFF = 2 * Q_BYTES;             // the Q tile of stream t at t * Q_BYTES
-  static constexpr int BAR_OFF = KV_OFF + KVS * STAGE;
-  static constexpr int SMEM = BAR_OFF + 1024;
-};
-
-struct PairItem {
-  int row, c, hk, tb;          // chunk row, its cached prefix, KV head, its first packed token
-  int n_kt, kv_max;            // KV tiles and keys of the item (its longer stream)
-  int nkt[2], t0[2], kv_end[2];  // per stream: KV tiles, index of its first tile among the stream's tiles, keys
-  int tok0[2][2], ntok[2][2];  // [stream][CTA]: first token of the Q tile within the chunk, valid tokens
-};
-
-struct PairBars {
-  uint64_t q_full, q_empty;          // q_full: leader, one arrival per CTA; q_empty: both, one commit per issuer
-  uint64_t kv_full[8], kv_empty[8];  // one K/V tile per stage: kv_full at the leader, one arrival per CTA;
-                                     // kv_empty in both, one commit per issuer after the tile's PV MMA
-  uint64_t s_full[2][2], p_full[2][2];  // [stream][S/P buffer]; p_full: leader, one arrival per softmax warp
-  uint64_t o_done[2][2];             // [stream][S/P buffer]: the PV MMA that read that buffer is done
-  uint64_t item_full[2], item_empty[2];  // item_full: both (the leader's producer); item_empty: leader
-  uint64_t mma_done[2];
-  uint32_t tmem;
-  int abort;
-  int issued[2][2];                  // [CTA]: K/V tiles and Q loads issued (read by the leader's drain)
-  PairItem items[2];
-};
-
-static_assert(sizeof(PairBars) <= 1024, "pair barrier block exceeds its reserved space");
-static_assert(PairCfg::KVS <= 8, "more K/V stages than barriers");
-
-constexpr int kPairItemEmpty = 2 + 2 * kSoftmaxWarps + 1;  // issuers, softmax warps of both CTAs, peer producer
-
-// wait by lane 0 on this CTA's barrier, result and ordering shared with the warp
-__device__ __forceinline__ bool warp_wait_cl(uint64_t* bar, uint32_t parity, const volatile int* abort,
-                                             uint64_t limit_ns, bool cluster_acquire = false) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_cl(bar, parity, abort, limit_ns, cluster_acquire) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0;
-}
-
-template <int G>
-__device__ __noinline__ void chunk_phase_pair(const CUtensorMap* tm_q_p, const CUtensorMap* tm_k_p,
-                                              const CUtensorMap* tm_v_p, const AttnParams& p, uint8_t* smem,
-                                              uint32_t tmem, uint32_t rank) {
-  using C = PairCfg;
-  constexpr int TPT = 128 / G;  // query tokens per 128-row Q tile
-  constexpr int KVS = C::KVS;
-  const CUtensorMap& tm_q = *tm_q_p;
-  const CUtensorMap& tm_k = *tm_k_p;
-  const CUtensorMap& tm_v = *tm_v_p;
-  PairBars* bars = reinterpret_cast<PairBars*>(smem + C::BAR_OFF);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = p.hdr[H_NCH_ITEMS];
-  const bool leader = rank == 0;
-  const uint64_t lim = p.wait_limit_ns;
-  const uint32_t sbase = smem_u32(smem);
-  auto k_off = [](int b) { return C::KV_OFF + b * C::STAGE; };
-  auto v_off = [](int b) { return C::KV_OFF + b * C::STAGE + C::K_BYTES; };
-  auto s_col = [&](int t, int b) { return tmem + 256 + (2 * t + b) * 64; };
-  auto lead = [&](const void* ptr) { return mapa_shared(smem_u32(ptr), 0); };      // the leader's copy
-  auto other = [&](const void* ptr) { return mapa_shared(smem_u32(ptr), rank ^ 1u); };  // the other CTA's copy
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 2);
-    mbar_init(&bars->q_empty, 2);
-    for (int b = 0; b < 8; ++b) {  // all of them, so that all can be invalidated
-      mbar_init(&bars->kv_full[b], 2);
-      mbar_init(&bars->kv_empty[b], 2);
-    }
-    for (int t = 0; t < 2; ++t) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&bars->s_full[t][b], 1);
-        mbar_init(&bars->p_full[t][b], 2 * (kSoftmaxWarps / 2));  // the group's four warps in each CTA
-        mbar_init(&bars->o_done[t][b], 1);
-      }
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->item_full[b], 1);
-      mbar_init(&bars->item_empty[b], kPairItemEmpty);
-    }
-    for (int i = 0; i < 2; ++i) mbar_init(&bars->mma_done[i], 1);
-    bars->abort = 0;
-    for (int r = 0; r < 2; ++r)
-      for (int i = 0; i < 2; ++i) bars->issued[r][i] = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  cluster_sync();  // both CTAs' barriers exist before either reaches into the other
-  volatile int* abort_flag = &bars->abort;
-  auto set_abort = [&]() {
-    *abort_flag = 1;
-    st_cluster_u32(other(&bars->abort), 1u);
-  };
-
-  if (warp == 0) {
-    // ---------------------------------------------------------------- work queue (leader) + TMA producer (both)
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-    }
-    // Test hook (never set by a real call): publish no work item and issue no copy, as a
-    // producer that stopped would; the other roles' bounded waits then run out.
-    const bool stalled = p.test_stall != 0;
-    bool ok = !stalled;
-    int g = 0;             // K/V tiles issued by this CTA
-    int n_q = 0;           // Q loads issued by this CTA
-    int n_done = 0;        // items taken
-    int t_run[2] = {0, 0};  // KV tiles run by each stream so far (leader)
-    auto lane0_wait = [&](uint64_t* bar, uint32_t parity, bool cluster_acquire = false) -> bool {
-      int r = 1;
-      if (lane == 0) r = mbar_wait_cl(bar, parity, abort_flag, lim, cluster_acquire) ? 1 : 0;
-      return __shfl_sync(0xffffffffu, r, 0) != 0;
-    };
-    while (ok) {
-      const int slot = n_done & 1;
-      PairItem it;
-      it.row = -1;
-      if (leader) {
-        int item = 0;
-        if (lane == 0) item = atomicAdd(p.hdr + H_CH_CTR, 1);
-        item = __shfl_sync(0xffffffffu, item, 0);
-        if (n_done >= 2 && !lane0_wait(&bars->item_empty[slot], ((n_done >> 1) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        if (item < n_items) {
-          const int2 kl = __ldg(p.ch_items + item);  // (chunk row index, item within the row)
-          const int k = kl.x, local = kl.y;
-          it.row = __ldg(p.ch_rows + k);
-          it.tb = __ldg(p.cu + it.row);
-          const int d = __ldg(p.cu + it.row + 1) - it.tb;
-          it.c = __ldg(p.q_start + it.row);
-          const int n_qt = (d + TPT - 1) / TPT;
-          const int n_quad = (n_qt + 3) >> 2;
-          const int quad = n_quad - 1 - local / p.H_kv;  // later tiles see more keys: run them first
-          it.hk = local % p.H_kv;
-          it.n_kt = 0;
-          it.kv_max = 0;
-          for (int t = 0; t < 2; ++t) {
-            it.kv_end[t] = 0;
-            for (int r = 0; r < 2; ++r) {
-              const int qt = 4 * quad + 2 * t + r;
-              it.tok0[t][r] = qt * TPT;
-              it.ntok[t][r] = qt < n_qt ? min(TPT, d - qt * TPT) : 0;
-              if (qt < n_qt) it.kv_end[t] = it.c + qt * TPT + it.ntok[t][r];
-            }
-            it.nkt[t] = (it.kv_end[t] + kKeys - 1) / kKeys;
-            it.t0[t] = t_run[t];
-            t_run[t] += it.nkt[t];
-            it.n_kt = max(it.n_kt, it.nkt[t]);
-            it.kv_max = max(it.kv_max, it.kv_end[t]);
-          }
-        }
-        if (lane == 0) {
-          bars->items[slot] = it;
-          const uint32_t* w = reinterpret_cast<const uint32_t*>(&it);
-          const uint32_t dst = other(&bars->items[slot]);
-          for (int i = 0; i < static_cast<int>(sizeof(PairItem) / 4); ++i) st_cluster_u32(dst + 4 * i, w[i]);
-          mbar_arrive(&bars->item_full[slot]);
-          mbar_arrive_cl_publish(other(&bars->item_full[slot]));  // orders the stores above
-        }
-      } else {
-        if (!lane0_wait(&bars->item_full[slot], (n_done >> 1) & 1, true)) {
-          ok = false;
-          break;
-        }
-        __syncwarp();
-        it = bars->items[slot];
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cl(lead(&bars->item_empty[slot]));
-      }
-      ++n_done;
-      if (it.row < 0) break;
-      // Q tiles of this CTA (one per stream): the previous item's S MMAs must be done with them
-      if (n_q >= 1 && !lane0_wait(&bars->q_empty, (n_q - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      const int nq = it.nkt[1] > 0 ? 2 : 1;
-      const uint32_t qbar = lead(&bars->q_full);
-      if (lane == 0) mbar_arrive_expect_tx_cl(qbar, nq * C::Q_BYTES);
-      __syncwarp();
-      if (lane < nq * 2) {
-        const int t = lane >> 1, s = lane & 1;
-        tma_load_3d_pair(smem + t * C::Q_BYTES + s * kQSlab, &tm_q, s * 64, it.hk * G, it.tb + it.tok0[t][rank], qbar);
-      }
-      ++n_q;
-      const int32_t* btrow = p.bt + static_cast<int64_t>(it.row) * p.bt_stride;
-      const int n_pages = (it.kv_max + kPage - 1) / kPage;
-      // lane L < 4 holds the page id of page L of the current tile; the next tile's is in flight
-      int pg_cur = lane < kTilePages && lane < n_pages ? __ldg(btrow + lane) : 0;
-      for (int kt = 0; kt < it.n_kt; ++kt) {
-        const int lp = (kt + 1) * kTilePages + lane;
-        const int pg_nxt = lane < kTilePages && lp < n_pages ? __ldg(btrow + lp) : 0;
-        const int b = g % KVS;
-        const int keys = min(kKeys, it.kv_max - kt * kKeys);
-        const int npg = (keys + kPage - 1) / kPage;
-        int phys = pg_cur;
-        if (lane < npg && (phys < 0 || phys >= p.num_pages)) {
-          atomicOr(p.hdr + H_STATUS, MS_STATUS_BAD_PAGE);
-          phys = 0;
-        }
-        // the stage was last read by the PV MMAs of tile g - KVS (and, before them, its S MMAs)
-        if (g >= KVS && !lane0_wait(&bars->kv_empty[b], ((g / KVS) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        // K: this CTA's pages 2 rank and 2 rank + 1 of the tile, both 64-column slabs.
-        // V: this CTA's 64 columns of every page, one 2 KB box per page; a last page holding
-        // rows past the context is written with plain loads instead, those rows zeroed: they
-        // may hold stale (even non-finite) data, and P = 0 times V must stay 0.
-        const int my_k = max(0, min(2, npg - 2 * static_cast<int>(rank)));
-        const int nv_last = keys & (kPage - 1);
-        const int n_vtma = nv_last ? npg - 1 : npg;
-        const uint32_t tx = (2 * my_k + n_vtma) * C::BOX;
-        const uint32_t bar = lead(&bars->kv_full[b]);
-        if (lane == 0) {
-          if (nv_last == 0)
-            mbar_arrive_expect_tx_cl(bar, tx);
-          else if (tx > 0)
-            mbar_expect_tx_cl(bar, tx);  // the arrival follows the plain-load rows below
-        }
-        __syncwarp();
-        {
-          const int j = lane >> 1, s = lane & 1;  // lanes 0-3: K, local page j, slab s
-          const int pk = __shfl_sync(0xffffffffu, phys, (2 * static_cast<int>(rank) + j) & 3);
-          if (lane < 4 && j < my_k)
-            tma_load_2d_pair(smem + k_off(b) + s * C::K_SLAB + j * C::BOX, &tm_k, s * 64,
-                             (pk * p.H_kv + it.hk) * kPage, bar);
-        }
-        if (lane < n_vtma)
-          tma_load_2d_pair(smem + v_off(b) + lane * C::V_PAGE, &tm_v, rank * 64, (phys * p.H_kv + it.hk) * kPage, bar);
-        if (nv_last != 0) {
-          const int pv = __shfl_sync(0xffffffffu, phys, npg - 1);
-          const bf16* src = p.v_cache + static_cast<int64_t>(pv * p.H_kv + it.hk) * kPage * 128 + rank * 64;
-          uint8_t* dst = smem + v_off(b) + (npg - 1) * C::V_PAGE;
-          const int cch = lane & 7;  // 16-byte chunk of the 128-byte row
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int i = (lane >> 3) + 4 * m;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            // through L2: the append that wrote these rows may overlap this kernel's lifetime
-            if (i < nv_last) v = __ldcg(reinterpret_cast<const uint4*>(src + i * 128) + cch);
-            *reinterpret_cast<uint4*>(dst + i * 128 + ((cch ^ (i & 7)) << 4)) = v;  // 128-byte swizzle
-          }
-          fence_proxy_async_smem();  // the leader's MMAs read these rows through the async proxy
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cl_publish(bar);
-        }
-        ++g;
-        pg_cur = pg_nxt;
-      }
-    }
-    if (lane == 0) {
-      if (!ok && !stalled) set_abort();
-      const uint32_t cnt = lead(&bars->issued[rank][0]);
-      st_cluster_u32(cnt, static_cast<uint32_t>(g));
-      st_cluster_u32(cnt + 4, static_cast<uint32_t>(n_q));
-    }
-  } else if (leader && (warp == 1 || warp == 2 + kSoftmaxWarps)) {
-    // ---------------------------------------------------------------- MMA issuer of one stream (leader)
-    // One thread issues both MMAs of its stream.  Iteration j waits for tile j's K/V, then for
-    // P(j - 2), and issues PV(j - 2) followed at once by S(j): S(j) goes into the buffer that
-    // held P(j - 2), and MMAs from one thread run in issue order, so the buffer needs no wait.
-    // The K/V wait comes before the wait for the softmax, and the commits after S(j), so that
-    // nothing stands between a P becoming ready and the S two tiles on entering the pipe; the
-    // softmax meanwhile works on tile j - 1, whose S was issued one iteration earlier.  Both
-    // issuers walk every KV tile of the item and commit once per stage (two commits per
-    // phase), issuing MMAs only for their stream's tiles, so a phase never completes on
-    // commits meant for a later one.  A commit covers every earlier MMA of the thread; each
-    // barrier's phases are waited on in order, never skipping one (a parity test cannot tell
-    // a phase two ahead from one not yet complete).  Descriptors are built once per tile: a
-    // k-step or a stage only moves the start-address field (bytes >> 4, 14 bits, no carry
-    // below 256 KB) by a constant.
-    const int t = warp == 1 ? 0 : 1;
-    if (lane == 0) {
-      const uint64_t qdesc = smem_desc_sw128(sbase + t * C::Q_BYTES, 16, 1024);
-      const uint64_t kdesc0 = smem_desc_sw128(sbase + C::KV_OFF, 16, 1024);
-      // V is the MN-major B operand, this CTA's 64 columns: one 16-key page per k-step, its two
-      // 8-key row groups 1024 B apart (SBO).  P (A operand) is in tensor memory.
-      const uint64_t vdesc0 = smem_desc_sw128(sbase + C::KV_OFF + C::K_BYTES, 2048, 1024);
-      const uint32_t s_tm = tmem + 256 + 2 * t * 64;
-      const uint32_t o_tm = tmem + t * 128;
-      constexpr uint32_t idesc_s = idesc_bf16_f32(256, kKeys, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(256, 128, 1);
-      int g_item = 0;  // global index of the item's first K/V tile (stages go round-robin)
-      bool ok = true;
-      for (int n = 0; ok; ++n) {
-        const int slot = n & 1;
-        if (!mbar_wait_cl(&bars->item_full[slot], (n >> 1) & 1, abort_flag, lim)) {
-          ok = false;
-          break;
-        }
-        const PairItem& it = bars->items[slot];  // stable until this role arrives on item_empty
-        if (it.row < 0) break;
-        const int nkt = it.nkt[t], t0 = it.t0[t], n_kt = it.n_kt, kend = it.kv_end[t];
-        if (nkt > 0 && !mbar_wait_cl(&bars->q_full, n & 1, abort_flag, lim)) {
-          ok = false;
-          break;
-        }
-        for (int j = 0; j < n_kt + 2; ++j) {
-          const int gs = g_item + j, gp = g_item + j - 2;   // global tiles of S(j) and PV(j - 2)
-          const int ss = gs % KVS, sp = (gp + KVS) % KVS;    // their stages
-          if (j < n_kt && !mbar_wait_cl(&bars->kv_full[ss], (gs / KVS) & 1, abort_flag, lim)) {
-            ok = false;
-            break;
-          }
-          const int jj = j - 2;
-          const bool do_pv = jj >= 0 && jj < nkt;
-          if (do_pv) {
-            const int gt = t0 + jj, b = gt & 1;
-            if (!mbar_wait_cl(&bars->p_full[t][b], (gt >> 1) & 1, abort_flag, lim)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t vd = vdesc0 + static_cast<uint64_t>((sp * C::STAGE) >> 4);
-            const uint32_t acol = s_tm + b * 64;
-            const int kr = kend - jj * kKeys;  // keys of this stream in the tile
-            const int nk = kr >= kKeys ? kKeys / 16 : (kr + 15) >> 4;
-            for (int kk = 0; kk < nk; ++kk)
-              mma_pair_ts(o_tm, acol + kk * 8, vd + static_cast<uint64_t>((kk * C::V_PAGE) >> 4), idesc_pv,
-                          (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          if (j < nkt) {
-            tc_fence_after();
-            const uint64_t kd = kdesc0 + static_cast<uint64_t>((ss * C::STAGE) >> 4);
-            const uint32_t dcol = s_tm + ((t0 + j) & 1) * 64;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t qo = static_cast<uint64_t>(((kk >> 2) * kQSlab + (kk & 3) * 32) >> 4);
-              const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * C::K_SLAB + (kk & 3) * 32) >> 4);
-              mma_pair_ss(dcol, qdesc + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit_pair(&bars->s_full[t][(t0 + j) & 1]);
-          }
-          if (j == n_kt - 1) mma_commit_pair(&bars->q_empty);
-          if (do_pv) mma_commit_pair(&bars->o_done[t][(t0 + jj) & 1]);
-          if (jj >= 0 && jj < n_kt) mma_commit_pair(&bars->kv_empty[sp]);
-        }
-        if (!ok) break;
-        g_item += n_kt;
-        mbar_arrive(&bars->item_empty[slot]);
-      }
-      if (!ok) set_abort();
-      // every MMA this thread issued must finish before tensor memory is reused or released
-      mma_commit_pair(&bars->mma_done[t]);
-      mbar_wait(&bars->mma_done[t], 0, nullptr, 200000000ull);
-    }
-  } else if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
-    // ---------------------------------------------------------------- softmax (both CTAs, own rows)
-    const int t = (warp - 2) >> 2;              // stream of this group
-    const int quad = warp & 3;                  // tensor-memory lane quadrant this warp may access
-    const int r = quad * 32 + lane;             // row of this CTA's Q tile
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tO = tmem + t * 128 + lane_off;
-    const float sl2 = p.scale_log2;
-    constexpr float kRescaleLog2 = 8.f;
-    bool ok = true;
-    for (int n = 0; ok; ++n) {
-      const int slot = n & 1;
-      if (!warp_wait_cl(&bars->item_full[slot], (n >> 1) & 1, abort_flag, lim, !leader)) {
-        ok = false;
-        break;
-      }
-      const PairItem& it = bars->items[slot];  // stable until this warp arrives on item_empty
-      if (it.row < 0) break;
-      const int nkt = it.nkt[t];
-      if (nkt > 0) {
-        const int ntok = it.ntok[t][rank];
-        const int tl = it.tok0[t][rank] + r / G;  // token of this row within the chunk
-        const bool valid = (r / G) < ntok;
-        // a row past the chunk sees every key the stream loads (all of them real data)
-        const int pos = valid ? it.c + tl : it.kv_end[t] - 1;
-        const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
-        float m_use = -INFINITY, l = 0.f;
-        for (int kt = 0; kt < nkt; ++kt) {
-          const int gt = it.t0[t] + kt, b = gt & 1;
-          if (!warp_wait_cl(&bars->s_full[t][b], (gt >> 1) & 1, abort_flag, lim)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          uint32_t r0[32], r1[32];
-          const uint32_t ts = s_col(t, b) + lane_off;
-          tmem_ld32(ts, r0);
-          tmem_ld32(ts + 32, r1);
-          tmem_wait_ld();
-          reg_fence32(r0);
-          reg_fence32(r1);
-          float sv[64];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            sv[j] = __uint_as_float(r0[j]);
-            sv[32 + j] = __uint_as_float(r1[j]);
-          }
-          const int key0 = kt * kKeys;
-          if (key0 + kKeys - 1 > warp_min_pos) {  // diagonal or ragged tile: causal mask (warp-uniform test)
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-              if (key0 + j > pos) sv[j] = -INFINITY;
-          }
-          float mxa[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float m = fmax3(sv[c], sv[c + 4], sv[c + 8]);
-#pragma unroll
-            for (int j = 12; j < 60; j += 8) m = fmax3(m, sv[j + c], sv[j + 4 + c]);
-            mxa[c] = fmaxf(m, sv[60 + c]);
-          }
-          const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
-          const float mx_s = mx * sl2;
-          const bool grow = mx_s > m_use + kRescaleLog2;
-          const float m_new = grow ? mx_s : m_use;
-          const float alpha = grow ? ex2(m_use - m_new) : 1.f;
-          const float neg_m = -m_new;
-          const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
-          float2 rsa[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            const float2 x = ffma2(make_float2(sv[j], sv[j + 1]), sl2x2, negm2);
-            const float2 e = make_float2(ex2(x.x), ex2(x.y));
-            sv[j] = e.x;
-            sv[j + 1] = e.y;
-            rsa[(j >> 1) & 1] = fadd2(rsa[(j >> 1) & 1], e);
-          }
-          l = l * alpha + ((rsa[0].x + rsa[0].y) + (rsa[1].x + rsa[1].y));
-          m_use = m_new;
-          uint32_t pw[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * j], sv[2 * j + 1]);
-            pw[j] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          tmem_st32u(ts, pw);
-          if (kt > 0 && __any_sync(0xffffffffu, grow)) {  // rescale this row's O
-            // the PV MMA of the previous tile must be done with O first
-            const bool done = warp_wait_cl(&bars->o_done[t][(gt - 1) & 1], ((gt - 1) >> 1) & 1, abort_flag, lim);
-            if (!done) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              uint32_t rr[32];
-              tmem_ld32(tO + cc * 32, rr);
-              tmem_wait_ld();
-              reg_fence32(rr);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
-              tmem_st32u(tO + cc * 32, rr);
-            }
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cl(lead(&bars->p_full[t][b]));
-        }
-        if (!ok) break;
-        const int gl = it.t0[t] + nkt - 1;
-        if (!warp_wait_cl(&bars->o_done[t][gl & 1], (gl >> 1) & 1, abort_flag, lim)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float inv = 1.f / l;
-        bf16* dst = p.out + (static_cast<int64_t>(it.tb + tl) * p.H_q + it.hk * G + r % G) * 128;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t rr[32];
-          tmem_ld32(tO + cc * 32, rr);
-          tmem_wait_ld();
-          reg_fence32(rr);
-          if (valid) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 u;
-              __nv_bfloat162 h0 =
-                  __floats2bfloat162_rn(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv);
-              __nv_bfloat162 h1 =
-                  __floats2bfloat162_rn(__uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
-              __nv_bfloat162 h2 =
-                  __floats2bfloat162_rn(__uint_as_float(rr[j + 4]) * inv, __uint_as_float(rr[j + 5]) * inv);
-              __nv_bfloat162 h3 =
-                  __floats2bfloat162_rn(__uint_as_float(rr[j + 6]) * inv, __uint_as_float(rr[j + 7]) * inv);
-              u.x = *reinterpret_cast<uint32_t*>(&h0);
-              u.y = *reinterpret_cast<uint32_t*>(&h1);
-              u.z = *reinterpret_cast<uint32_t*>(&h2);
-              u.w = *reinterpret_cast<uint32_t*>(&h3);
-              *reinterpret_cast<uint4*>(dst + cc * 32 + j) = u;
-            }
-          }
-        }
-      }
-      // O has been read: the item's slot may be reused and the next item's first PV may overwrite O
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cl(lead(&bars->item_empty[slot]));
-    }
-    if (!ok && lane == 0) {
-      set_abort();
-      atomicOr(p.hdr + H_STATUS, MS_STATUS_TIMEOUT);
-    }
-  }
-
-  // ---- end of the phase
-  __syncwarp();
-  tc_fence_before();
-  cluster_sync();  // every role of both CTAs is done; the issue counts are at the leader
-  // In the other CTA, the leader's final commits (which follow all of its earlier ones, and whose
-  // MMAs the leader has already waited for) land before that CTA's barriers are invalidated.
-  if (!leader && threadIdx.x == 32)
-    for (int i = 0; i < 2; ++i) mbar_wait(&bars->mma_done[i], 0, nullptr, 200000000ull);
-  if (leader && threadIdx.x == 0 && *abort_flag) {
-    // After an abort, copies may still be in flight.  Both CTAs' copies count on the leader's
-    // "full" barriers: give every phase that only one CTA armed the other CTA's arrival, then
-    // wait (bounded) until each phase a copy was issued for has completed.
-    auto drain = [&](uint64_t* full, int n_lead, int n_other, int nst) {
-      const int hi = max(n_lead, n_other);
-      for (int x = max(0, hi - nst); x < hi; ++x) {
-        uint64_t* bar = full + (x % nst);
-        if (x >= n_lead) mbar_arrive(bar);
-        if (x >= n_other) mbar_arrive(bar);
-        mbar_wait(bar, (x / nst) & 1, nullptr, 200000000ull);
-      }
-    };
-    drain(bars->kv_full, bars->issued[0][0], bars->issued[1][0], KVS);
-    drain(&bars->q_full, bars->issued[0][1], bars->issued[1][1], 1);
-  }
-  cluster_sync();  // no copy of either CTA is in flight; the other CTA no longer writes here
-  (void)n_items;
-}
-
-// barriers of the pair chunk phase, invalidated before the memory is reused
-__device__ __forceinline__ void invalidate_pair_barriers(uint8_t* smem) {
-  if (threadIdx.x == 0) {
-    PairBars* bars = reinterpret_cast<PairBars*>(smem + PairCfg::BAR_OFF);
-    for (uint64_t* b = &bars->q_full; b <= &bars->mma_done[1]; ++b) mbar_inval(b);
-  }
-}
-
 // barriers of one finished phase, invalidated before the memory is reused
-template <int D>
-__device__ __forceinline__ void invalidate_chunk_barriers(uint8_t* smem) {
-  if (threadIdx.x == 0) {
-    ChBars* bars = reinterpret_cast<ChBars*>(smem + ChCfg<D>::BAR_OFF);
-    for (uint64_t* b = &bars->q_full; b <= &bars->mma_done[2]; ++b) mbar_inval(b);
-  }
-}
-
 template <int D, int G>
-__device__ __forceinline__ void invalidate_decode_barriers(uint8_t* smem) {
-  using C = DecCfg<D, G>;
-  if ((threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < C::WARPS) {
+__device__ __forceinline__ void invalidate_phase_barriers(uint8_t* smem, bool chunk) {
+  if (chunk) {
+    if (threadIdx.x == 0) {
+      ChBars* bars = reinterpret_cast<ChBars*>(smem + ChCfg<D>::BAR_OFF);
+      uint64_t* b0 = &bars->q_full;
+      uint64_t* b1 = &bars->mma_done[2];
+      for (uint64_t* b = b0; b <= b1; ++b) mbar_inval(b);
+    }
+  } else if ((threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < DecCfg<D, G>::WARPS) {
+    using C = DecCfg<D, G>;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::TAIL_OFF + (threadIdx.x >> 5) * C::TAIL_BYTES + C::T_BAR);
     for (int i = 0; i < C::NST; ++i) mbar_inval(full + i);
   }
@@ -2039,13 +1467,13 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       tc_fence_before();
       __syncthreads();
       const bool aborted = reinterpret_cast<ChBars*>(smem + ChCfg<D>::BAR_OFF)->abort != 0;
-      invalidate_chunk_barriers<D>(smem);
+      invalidate_phase_barriers<D, G>(smem, true);
       __syncthreads();
       if (aborted) break;
     } else if (!chunk && n_dec_items > 0) {
       decode_phase<D, G>(p, smem, &tm_k, &tm_v);
       __syncwarp();
-      invalidate_decode_barriers<D, G>(smem);
+      invalidate_phase_barriers<D, G>(smem, false);
       __syncthreads();
     }
   }
@@ -2055,81 +1483,6 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   }
 }
 
-
-// Shared memory of the pair kernel: the larger of the two phases' layouts, then a
-// small block both phases leave alone (tensor-memory address, SM id read by the
-// other CTA of the pair).
-template <int G>
-struct PairKernelSmem {
-  static constexpr int PHASES = PairCfg::SMEM > DecCfg<128, G>::SMEM ? PairCfg::SMEM : DecCfg<128, G>::SMEM;
-  static constexpr int SHARED_OFF = (PHASES + 63) / 64 * 64;
-  static constexpr int TOTAL = SHARED_OFF + 64;
-};
-
-// D = 128: clusters of two CTAs, one per SM.  The pair starts on chunk work when the
-// leader's SM id is below hdr[H_CHUNK_CTAS], else on decode items (each CTA on its own);
-// a CTA whose queue runs dry moves to the other queue, the pair together for chunk work.
-template <int G>
-__global__ void __launch_bounds__(kChunkThreads, 1)
-    attention_kernel_pair(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, AttnParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  constexpr int kShOff = PairKernelSmem<G>::SHARED_OFF;
-  const int warp = threadIdx.x >> 5;
-  if ((smem_u32(smem) & 1023u) != 0) {  // the same in both CTAs of the pair
-    griddep_wait();
-    if (threadIdx.x == 0) atomicOr(p.hdr + H_STATUS, MS_STATUS_INTERNAL);
-    return;
-  }
-  const uint32_t rank = cluster_rank();
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kShOff);
-  int* smid_slot = reinterpret_cast<int*>(smem + kShOff + 4);
-  // set-up that needs nothing from the kernels before: it overlaps their tail
-  if (warp == 1) {
-    tmem_alloc_pair(tmem_slot, 512);
-    tmem_relinquish_pair();
-  }
-  if (threadIdx.x == 0) {
-    uint32_t smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    *smid_slot = static_cast<int>(smid);
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // both CTAs run; the leader's SM id is readable
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int lead_smid = static_cast<int>(ld_cluster_u32(mapa_shared(smem_u32(smid_slot), 0)));
-  griddep_wait();  // the item tables (and, through the prologue, the append's q_rot and pages)
-  const int n_ch_items = p.hdr[H_NCH_ITEMS];
-  const int n_dec_items = p.hdr[H_NDEC_ITEMS];
-  // As in the single-CTA kernel, the starting queue goes by SM id (here the leader's): as a
-  // programmatic dependent, the blocks reach SMs in an order set by the kernels still draining.
-  const bool chunk_first = lead_smid < p.hdr[H_CHUNK_CTAS];
-  for (int ph = 0; ph < 2 && (n_ch_items > 0 || n_dec_items > 0); ++ph) {
-    const bool chunk = (ph == 0) == chunk_first;
-    if (chunk && n_ch_items > 0) {
-      chunk_phase_pair<G>(&tm_q, &tm_k, &tm_v, p, smem, tmem, rank);
-      tc_fence_before();
-      __syncthreads();
-      const bool aborted = reinterpret_cast<PairBars*>(smem + PairCfg::BAR_OFF)->abort != 0;  // set in both
-      invalidate_pair_barriers(smem);
-      __syncthreads();
-      if (aborted) break;
-    } else if (!chunk && n_dec_items > 0) {
-      decode_phase<128, G>(p, smem, &tm_k, &tm_v);
-      __syncwarp();
-      invalidate_decode_barriers<128, G>(smem);
-      __syncthreads();
-    }
-  }
-  tc_fence_before();
-  cluster_sync();  // neither CTA touches the other's memory any more
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem, 512);
-  }
-}
 
 }  // namespace
 
@@ -2295,62 +1648,6 @@ int launch_paths(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& 
   return cudaGetLastError() == cudaSuccess ? MS_OK : MS_ERR_CUDA;
 }
 
-// Clusters of two that fit on the device at once (1 CTA per SM), per device and
-// group size, looked up once; the pair kernel's grid is twice that.
-std::atomic<int> g_pair_clusters[kMaxDevices][4];
-
-template <int G>
-int pair_grid(cudaStream_t st) {
-  const int dev = current_device();
-  if (dev < 0) return -1;
-  constexpr int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  const int cached = g_pair_clusters[dev][gi].load(std::memory_order_relaxed);
-  if (cached > 0) return 2 * cached;
-  constexpr int smem = PairKernelSmem<G>::TOTAL;
-  if (ensure_smem_limit(attention_kernel_pair<G>, 9 + gi, smem) != MS_OK) return -1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * 1024);
-  cfg.blockDim = dim3(kChunkThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attention_kernel_pair<G>, &cfg) != cudaSuccess || n < 1) return -1;
-  g_pair_clusters[dev][gi].store(n, std::memory_order_relaxed);
-  return 2 * n;
-}
-
-template <int G>
-int launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int n_ctas,
-                cudaStream_t st) {
-  constexpr int smem = PairKernelSmem<G>::TOTAL;
-  static_assert(smem <= 232448, "pair attention kernel exceeds the per-CTA shared-memory limit");
-  constexpr int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  if (ensure_smem_limit(attention_kernel_pair<G>, 9 + gi, smem) != MS_OK) return MS_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_ctas);
-  cfg.blockDim = dim3(kChunkThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, attention_kernel_pair<G>, tq, tk, tv, p) != cudaSuccess) return MS_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? MS_OK : MS_ERR_CUDA;
-}
-
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -2401,20 +1698,6 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
   if (ws_bytes < w.total) return MS_ERR_ARG;
   const int sms = num_sms();
   if (sms <= 0) return MS_ERR_CUDA;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // D = 128 runs the chunk tiles on pairs of CTAs (clusters of two), D = 64 on single CTAs
-  const bool pair = D == 128;
-  int n_ctas = sms;  // one persistent CTA per SM
-  if (pair) {
-    switch (G) {
-      case 1: n_ctas = pair_grid<1>(st); break;
-      case 2: n_ctas = pair_grid<2>(st); break;
-      case 4: n_ctas = pair_grid<4>(st); break;
-      default: n_ctas = pair_grid<8>(st); break;
-    }
-    if (n_ctas <= 0) return MS_ERR_CUDA;
-    if (n_ctas > sms) n_ctas = sms & ~1;
-  }
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return MS_ERR_CUDA;
 
@@ -2477,31 +1760,31 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
   p.H_kv = H_kv;
   p.D = D;
   p.G = G;
-  p.dec_workers = n_ctas * dec_warps(D, G);
-  p.num_sms = n_ctas;
-  p.qt_per_item = pair ? 4 : 2;
-  p.ctas_per_item = pair ? 2 : 1;
+  p.dec_workers = sms * dec_warps(D, G);
+  p.num_sms = sms;
   p.clear_status = clear_status ? 1 : 0;
   p.test_stall = stall_limit_ns > 0 ? 1 : 0;
   p.wait_limit_ns = stall_limit_ns > 0 ? static_cast<uint64_t>(stall_limit_ns) : 2000000000ull;
   p.scale_log2 = scale * 1.4426950408889634f;
 
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (ensure_smem_limit(prologue_kernel, 8, static_cast<int>(sizeof(PrologueSmem))) != MS_OK) return MS_ERR_CUDA;
   *launched = true;  // from here on, kernels may be on the stream
   if (launch_dependent(prologue_kernel, dim3(1), dim3(kPrologueThreads), sizeof(PrologueSmem), st, p) !=
           cudaSuccess ||
       launch_dependent(items_kernel, dim3(sms < 64 ? sms : 64), dim3(kItemThreads), 0, st, p) != cudaSuccess)
     return MS_ERR_CUDA;
+  const int n_ctas = sms;  // one persistent CTA per SM
   int rc = MS_ERR_ARG;
   switch (D * 100 + G) {
     case 6401: rc = launch_paths<64, 1>(p, tq, tk, tv, tvp, n_ctas, st); break;
     case 6402: rc = launch_paths<64, 2>(p, tq, tk, tv, tvp, n_ctas, st); break;
     case 6404: rc = launch_paths<64, 4>(p, tq, tk, tv, tvp, n_ctas, st); break;
     case 6408: rc = launch_paths<64, 8>(p, tq, tk, tv, tvp, n_ctas, st); break;
-    case 12801: rc = launch_pair<1>(p, tq, tk, tv, n_ctas, st); break;
-    case 12802: rc = launch_pair<2>(p, tq, tk, tv, n_ctas, st); break;
-    case 12804: rc = launch_pair<4>(p, tq, tk, tv, n_ctas, st); break;
-    case 12808: rc = launch_pair<8>(p, tq, tk, tv, n_ctas, st); break;
+    case 12801: rc = launch_paths<128, 1>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 12802: rc = launch_paths<128, 2>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 12804: rc = launch_paths<128, 4>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 12808: rc = launch_paths<128, 8>(p, tq, tk, tv, tvp, n_ctas, st); break;
     default: break;
   }
   return rc;

@@ -322,162 +322,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
-// ------------------------------------------------------------------ CTA pairs (cluster of two)
-//
-// Two CTAs of a cluster work as a pair on one tile: the even CTA (rank 0,
-// the leader) issues every tensor-core MMA for both (cta_group::2: M = 256,
-// 128 rows in each CTA's tensor memory, the B operand split between the two
-// CTAs' shared memory), and the other CTA reaches the leader's mbarriers
-// through shared::cluster addresses.
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// shared::cluster address of the same shared-memory location in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
-// every thread of both CTAs: writes before it are visible to both CTAs after it
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-// Arrive on an mbarrier of either CTA.  Scope matters for cost: a release at
-// cluster scope waits for the thread's outstanding memory operations to be
-// visible to the whole cluster (about a microsecond with loads in flight), so
-// it is used only where the arrival publishes data written with plain stores
-// (mbar_arrive_cl_publish).  A hand-off of tensor-memory or tensor-core state
-// is ordered by the tcgen05 fences around it and takes the default
-// (release, CTA scope); a producer's arrival whose data comes by TMA needs no
-// ordering at all (relaxed).
-__device__ __forceinline__ void mbar_arrive_cl(uint32_t addr) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cl_publish(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx_cl(uint32_t addr, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes)
-               : "memory");
-}
-// raise the current phase's expected transaction bytes without arriving
-__device__ __forceinline__ void mbar_expect_tx_cl(uint32_t addr, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;" ::"r"(addr), "r"(bytes) : "memory");
-}
-
-// Wait on this CTA's mbarrier, bounded like mbar_wait, with n polls before the
-// clock starts.  cluster_acquire: acquire at cluster scope, for a phase whose
-// arrival published data stored by the other CTA (mbar_arrive_cl_publish).
-__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// non-blocking test of a phase (no suspension)
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, const volatile int* abort,
-                                             uint64_t limit_ns, bool cluster_acquire = false, int n_fast = 16) {
-  const uint32_t a = smem_u32(bar);
-  if (!cluster_acquire && mbar_test_wait(bar, parity)) return true;
-  auto poll = [&]() { return cluster_acquire ? mbar_try_wait_acq_cluster(a, parity) : mbar_try_wait(bar, parity); };
-  for (int i = 0; i < n_fast; ++i)
-    if (poll()) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (poll()) return true;
-    if ((it & 255u) == 0) {
-      if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-  }
-}
-
-// tensor copies whose completion is counted on an mbarrier of either CTA of the pair
-__device__ __forceinline__ void tma_load_2d_pair(void* dst_smem, const void* tmap, int32_t c0, int32_t c1,
-                                                 uint32_t bar_cl) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-      "[%4];" ::"r"(smem_u32(dst_smem)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(bar_cl)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_pair(void* dst_smem, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
-                                                 uint32_t bar_cl) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4}], [%5];" ::"r"(smem_u32(dst_smem)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cl)
-      : "memory");
-}
-
-// tensor memory of a pair: one warp of each CTA, same columns in both
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// D (+)= A B^T over the pair (M = 256: rows 0-127 in the leader, 128-255 in the peer)
-__device__ __forceinline__ void mma_pair_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// arrive once on the mbarrier at this offset in both CTAs of the pair when this thread's MMAs complete
-__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(static_cast<uint16_t>(3))
-      : "memory");
-}
-
 // Shared-memory matrix descriptor for tcgen05.mma (sm_100 family layout):
 // start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride
 // byte offset >> 4 in 32-45, version 1 in 46-47, swizzle mode in 61-63
