@@ -2,7 +2,7 @@
 """Mixed-step attention throughput on GB300: tokens/s and fraction of the step roofline.
 
 One timed step is one pass of the whole hot path -- ms_kv_append_rope then
-ms_mixed_step_attention -- over every batch of a workload.  By default all four
+ms_mixed_step_attention_ragged -- over every batch of a workload.  By default all four
 full-size workloads run one after another and print ONE JSON line: its top level
 is the largest single-GPU step, the long-context bimodal batch (the last
 4096-token chunk of a 32768-token prompt next to 512 decodes, 10 % of them at
@@ -243,13 +243,13 @@ def measure_config(name, args, ms, world, rank, device, dist) -> dict:
     for i, wl in enumerate(wls):
         states = [(r.cached_len, r.remaining) for r in wl.requests]
         tables = [r.block_table for r in wl.requests]
-        meta = ms.build_batch_metadata(states, tables, wl.token_budget, wl.max_chunk)
+        meta = ms.build_batch_metadata(states, tables, wl.token_budget, wl.max_chunk, ragged=True)
         batch = step.to_device(meta, device)
         T = meta["num_tokens"]
         q, k, v = workloads.step_tensors(wl, T, 50 + i + 1000 * rank, device)
         rows = [(int(meta["q_start_pos"][s]), int(meta["cu_seqlens_q"][s + 1] - meta["cu_seqlens_q"][s]))
                 for s in range(meta["num_rows"])]
-        counts = roofline.step_counts(rows, wl.H_q, wl.H_kv, wl.D, meta["bt_stride"])
+        counts = roofline.step_counts(rows, wl.H_q, wl.H_kv, wl.D)
         subs.append(dict(wl=wl, states=states, tables=tables, meta=meta, batch=batch, q=q, k=k, v=v,
                          q_rot=torch.empty_like(q), out=torch.empty_like(q), counts=counts))
     ws_bytes = max(ms.attention_workspace_size(max(s["meta"]["num_rows"], 1), max(s["meta"]["num_tokens"], 1),
@@ -268,8 +268,7 @@ def measure_config(name, args, ms, world, rank, device, dist) -> dict:
                 events[j][0].record(stream)
             ms.kv_append_rope(s["q"], s["k"], s["v"], b.positions, b.slot_mapping, cos, sin, k_cache, v_cache,
                               q_rot=s["q_rot"], dev_status=status, stream=stream)
-            ms.mixed_step_attention(s["q_rot"], k_cache, v_cache, b.cu_seqlens_q, b.q_start_pos, b.context_lens,
-                                    b.block_tables, b.context_total, s["out"], ws, stream=stream)
+            step.attend(s["q_rot"], k_cache, v_cache, b, s["out"], ws, stream=stream)
             if events is not None:
                 events[j][1].record(stream)
 
@@ -334,7 +333,7 @@ def measure_config(name, args, ms, world, rank, device, dist) -> dict:
         roof["traffic_source"] = (f"ncu capture of batch {b} (append + attention kernels)"
                                   + (", scaled by algorithmic bytes" if n_sub > 1 else ""))
         roof["traffic_vs_alg_bytes"] = round(roof["traffic"] / grp_bytes_avg, 4)
-    roof["kernel"] = ("one batch of the path: ms_kv_append_rope + ms_mixed_step_attention "
+    roof["kernel"] = ("one batch of the path: ms_kv_append_rope + ms_mixed_step_attention_ragged "
                       "(append, prologue, items and persistent attention_kernel launches)")
     roof["peak_source"] = (f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
                            + ("; sustained bf16 (kernel timed inside a step)" if roof["bound"] == "tensor" else ""))
@@ -368,67 +367,80 @@ def measure_config(name, args, ms, world, rank, device, dist) -> dict:
 
 
 def run_e2e(args, ms, step, subs, cos, sin, k_cache, v_cache, ws, status, device, stream, dist):
-    """Same metric through the public API from host buffers: per batch, the C++ scheduler
-    builds the metadata, which goes H2D (one packed copy) with q/k/v from pinned memory; the
-    output comes back D2H.  Uploads and downloads run on their own streams, ordered with events,
-    so they overlap the compute of neighbouring batches; every step ends with a full sync."""
+    """Same metric through the public API from host buffers, pipelined as a serving loop would be:
+    every step, per batch, the C++ scheduler builds the metadata on the host, which goes H2D in one
+    packed copy with q/k/v from pinned memory; the output comes back D2H.  Uploads, compute and
+    downloads run on three streams ordered by events, with two device slots per batch, so step s + 1
+    uploads while step s computes and step s - 1 downloads; the timed region ends with a full sync
+    after the last step's download."""
     import torch
     host = []
     for s in subs:
         host.append(dict(q=s["q"].cpu().pin_memory(), k=s["k"].cpu().pin_memory(), v=s["v"].cpu().pin_memory(),
                          out=torch.empty_like(s["out"], device="cpu").pin_memory()))
+    # two device slots per batch: its inputs, q_rot and output
+    slots = [[dict(q=s["q"], k=s["k"], v=s["v"], q_rot=s["q_rot"], out=s["out"]),
+              dict(q=torch.empty_like(s["q"]), k=torch.empty_like(s["k"]), v=torch.empty_like(s["v"]),
+                   q_rot=torch.empty_like(s["q_rot"]), out=torch.empty_like(s["out"]))] for s in subs]
     n = max(1, min(args.steps, args.e2e_steps))
-    h2d = d2h = 0
-    # uploads, compute and downloads on three streams: batch i + 1 uploads while batch i computes
     up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
     stagers = [step.MetaStager(s["meta"]["num_rows"], s["meta"]["num_tokens"],
-                               s["meta"]["num_rows"] * s["meta"]["bt_stride"], device) for s in subs]
-    done = [None] * len(subs)  # compute of the batch's previous step (its device buffers are free after it)
+                               s["meta"]["num_rows"] + 1 + int(s["meta"]["bt_offsets"][-1]), device) for s in subs]
+    computed = [[None, None] for _ in subs]  # compute of the slot's last step: its inputs are free after it
+    fetched = [[None, None] for _ in subs]   # download of the slot's last output: the slot's out is free after it
+    counter = {"step": 0, "h2d": 0, "d2h": 0}
 
     def e2e_step():
-        nonlocal h2d, d2h
         h2d = d2h = 0
+        par = counter["step"] & 1
         for i, (s, hb) in enumerate(zip(subs, host)):
             wl = s["wl"]
-            meta = ms.build_batch_metadata(s["states"], s["tables"], wl.token_budget, wl.max_chunk)
-            if done[i] is not None:
-                up.wait_event(done[i])
+            sl = slots[i][par]
+            meta = ms.build_batch_metadata(s["states"], s["tables"], wl.token_budget, wl.max_chunk, ragged=True)
+            if computed[i][par] is not None:
+                up.wait_event(computed[i][par])
             b = stagers[i].stage(meta, up)
-            q, k, v = s["q"], s["k"], s["v"]
             with torch.cuda.stream(up):
-                q.copy_(hb["q"], non_blocking=True)
-                k.copy_(hb["k"], non_blocking=True)
-                v.copy_(hb["v"], non_blocking=True)
+                sl["q"].copy_(hb["q"], non_blocking=True)
+                sl["k"].copy_(hb["k"], non_blocking=True)
+                sl["v"].copy_(hb["v"], non_blocking=True)
                 ready = torch.cuda.Event()
                 ready.record(up)
             stream.wait_event(ready)
-            q_rot = s["q_rot"]
-            ms.kv_append_rope(q, k, v, b.positions, b.slot_mapping, cos, sin, k_cache, v_cache, q_rot=q_rot,
-                              dev_status=status, stream=stream)
-            ms.mixed_step_attention(q_rot, k_cache, v_cache, b.cu_seqlens_q, b.q_start_pos, b.context_lens,
-                                    b.block_tables, b.context_total, s["out"], ws, stream=stream)
+            if fetched[i][par] is not None:
+                stream.wait_event(fetched[i][par])
+            ms.kv_append_rope(sl["q"], sl["k"], sl["v"], b.positions, b.slot_mapping, cos, sin, k_cache, v_cache,
+                              q_rot=sl["q_rot"], dev_status=status, stream=stream)
+            step.attend(sl["q_rot"], k_cache, v_cache, b, sl["out"], ws, stream=stream)
             fin = torch.cuda.Event()
             fin.record(stream)
-            done[i] = fin
+            computed[i][par] = fin
             down.wait_event(fin)
             with torch.cuda.stream(down):
-                hb["out"].copy_(s["out"], non_blocking=True)
-            h2d += b.h2d_bytes + (q.numel() + k.numel() + v.numel()) * 2
-            d2h += s["out"].numel() * 2
-        torch.cuda.synchronize()
+                hb["out"].copy_(sl["out"], non_blocking=True)
+                got = torch.cuda.Event()
+                got.record(down)
+            fetched[i][par] = got
+            h2d += b.h2d_bytes + (sl["q"].numel() + sl["k"].numel() + sl["v"].numel()) * 2
+            d2h += sl["out"].numel() * 2
+        counter["step"] += 1
+        counter["h2d"], counter["d2h"] = h2d, d2h
 
     for _ in range(2):
         e2e_step()
+    torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     t = time.perf_counter()
     for _ in range(n):
         e2e_step()
+    torch.cuda.synchronize()
     el = time.perf_counter() - t
     el = reduce_max(el, dist, device)
     tokens = reduce_sum(sum(s["meta"]["num_tokens"] for s in subs) * n, dist, device)
-    return {"value": round(tokens / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": n}
+    return {"value": round(tokens / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(counter["h2d"]),
+            "d2h_bytes_per_step": int(counter["d2h"]), "steps": n,
+            "pipeline": "3 streams, 2 device slots per batch; full sync after the last step"}
 
 
 # ---------------------------------------------------------------------------- oracle (CPU) timing
@@ -846,7 +858,7 @@ def run_split(args, local):
                 ws = step.workspace_for(b, wl.H_q, wl.H_kv, wl.D, device)
                 rows = [(int(meta["q_start_pos"][s_]), int(meta["cu_seqlens_q"][s_ + 1] - meta["cu_seqlens_q"][s_]))
                         for s_ in range(meta["num_rows"])]
-                cnt = roofline.step_counts(rows, wl.H_q, wl.H_kv, wl.D, meta["bt_stride"])
+                cnt = roofline.step_counts(rows, wl.H_q, wl.H_kv, wl.D)
 
                 def append():
                     ms.kv_append_rope(q, k, v, b.positions, b.slot_mapping, cos, sin, k_cache, v_cache,

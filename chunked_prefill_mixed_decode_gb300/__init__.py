@@ -105,6 +105,15 @@ def lib() -> ctypes.CDLL:
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _VP, _VP,
                                           ctypes.c_size_t, _VP]
+    h.ms_build_batch_metadata_ragged.restype = ctypes.c_int
+    h.ms_build_batch_metadata_ragged.argtypes = [
+        ctypes.POINTER(Request), ctypes.c_int32, ctypes.POINTER(SchedConfig), ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int64, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P, ctypes.POINTER(BatchInfo)]
+    h.ms_mixed_step_attention_ragged.restype = ctypes.c_int
+    h.ms_mixed_step_attention_ragged.argtypes = [_VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP, _VP, _VP,
+                                                 ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_float, _VP, _VP, ctypes.c_size_t, _VP]
     h.ms_mixed_step_attention_noalloc.restype = ctypes.c_int
     h.ms_mixed_step_attention_noalloc.argtypes = [_VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP, _VP,
                                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
@@ -168,12 +177,14 @@ def _stream(stream) -> int:
 def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndarray], token_budget: int,
                          max_chunk_per_request: int = 0, policy: int = POLICY_DECODE_FIRST,
                          min_chunk_per_request: int = 0, prefill_quota: int = 0,
-                         decode_share_permille: int = 500) -> dict:
+                         decode_share_permille: int = 500, ragged: bool = False) -> dict:
     """Token-budget packing + varlen metadata (ms_build_batch_metadata).
 
     ``states[i] = (cached_len, remaining_prompt)``; ``block_tables[i]`` is an
     int32 array of that request's physical pages.  Returns numpy int32 arrays
-    and the batch summary.
+    and the batch summary.  With ``ragged`` (ms_build_batch_metadata_ragged)
+    the block table comes as ``bt_offsets`` [rows + 1] and ``bt_pages`` (each
+    row's pages in use, back to back) instead of padded ``block_tables``.
     """
     n = len(states)
     reqs, keep = _request_array(states, block_tables)
@@ -183,11 +194,13 @@ def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndar
     cap_rows = max(n, 1)
     cap_tokens = max(int(token_budget), 1)
     max_pages = max(int(lens.max()) if n else 0, 1)
-    cap_bt = cap_rows * max_pages
+    # ragged: a row reads at most its request's pages
+    cap_bt = max(int(lens.sum()) if n else 0, 1) if ragged else cap_rows * max_pages
     # one output buffer; the returned arrays are views of it
+    bt_sizes = (("bt_offsets", cap_rows + 1), ("bt_pages", cap_bt)) if ragged else (("block_tables", cap_bt),)
     sizes = (("cu_seqlens_q", cap_rows + 1), ("q_start_pos", cap_rows), ("context_lens", cap_rows),
-             ("positions", cap_tokens), ("slot_mapping", cap_tokens), ("block_tables", cap_bt),
-             ("row_req", cap_rows), ("num_scheduled", max(n, 1)))
+             ("positions", cap_tokens), ("slot_mapping", cap_tokens)) + bt_sizes + \
+        (("row_req", cap_rows), ("num_scheduled", max(n, 1)))
     # every element a returned view covers is written by the call
     buf = np.empty(sum(sz for _, sz in sizes), dtype=np.int32)
     out, off = {}, 0
@@ -195,21 +208,35 @@ def build_batch_metadata(states: Sequence[tuple], block_tables: Sequence[np.ndar
         out[k] = buf[off:off + sz]
         off += sz
     info = BatchInfo()
-    rc = lib().ms_build_batch_metadata(reqs.ctypes.data_as(ctypes.POINTER(Request)), n, ctypes.byref(cfg), cap_rows,
-                                       cap_tokens, cap_bt, _i32(out["cu_seqlens_q"]), _i32(out["q_start_pos"]),
-                                       _i32(out["context_lens"]), _i32(out["positions"]),
-                                       _i32(out["slot_mapping"]), _i32(out["block_tables"]), _i32(out["row_req"]),
-                                       _i32(out["num_scheduled"]), ctypes.byref(info))
+    reqp = reqs.ctypes.data_as(ctypes.POINTER(Request))
+    if ragged:
+        rc = lib().ms_build_batch_metadata_ragged(reqp, n, ctypes.byref(cfg), cap_rows, cap_tokens, cap_bt,
+                                                  _i32(out["cu_seqlens_q"]), _i32(out["q_start_pos"]),
+                                                  _i32(out["context_lens"]), _i32(out["positions"]),
+                                                  _i32(out["slot_mapping"]), _i32(out["bt_offsets"]),
+                                                  _i32(out["bt_pages"]), _i32(out["row_req"]),
+                                                  _i32(out["num_scheduled"]), ctypes.byref(info))
+    else:
+        rc = lib().ms_build_batch_metadata(reqp, n, ctypes.byref(cfg), cap_rows, cap_tokens, cap_bt,
+                                           _i32(out["cu_seqlens_q"]), _i32(out["q_start_pos"]),
+                                           _i32(out["context_lens"]), _i32(out["positions"]),
+                                           _i32(out["slot_mapping"]), _i32(out["block_tables"]),
+                                           _i32(out["row_req"]), _i32(out["num_scheduled"]), ctypes.byref(info))
     del keep
-    _check(rc, "ms_build_batch_metadata")
+    _check(rc, "ms_build_batch_metadata_ragged" if ragged else "ms_build_batch_metadata")
     S, T, stride = info.num_rows, info.num_tokens, info.bt_stride
+    if ragged:
+        pages = int(out["bt_offsets"][S])
+        tables = {"bt_offsets": out["bt_offsets"][: S + 1], "bt_pages": out["bt_pages"][:pages]}
+    else:
+        tables = {"block_tables": out["block_tables"][: S * stride].reshape(S, stride)}
     return {
         "cu_seqlens_q": out["cu_seqlens_q"][: S + 1],
         "q_start_pos": out["q_start_pos"][:S],
         "context_lens": out["context_lens"][:S],
         "positions": out["positions"][:T],
         "slot_mapping": out["slot_mapping"][:T],
-        "block_tables": out["block_tables"][: S * stride].reshape(S, stride),
+        **tables,
         "bt_stride": stride,
         "row_req": out["row_req"][:S],
         "num_scheduled": out["num_scheduled"][:n],
@@ -554,6 +581,44 @@ def mixed_step_attention(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, con
                                        PAGE_SIZE, float(scale), _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "ms_mixed_step_attention")
+
+
+def mixed_step_attention_ragged(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, bt_offsets,
+                                bt_pages, context_total: int, out, workspace, scale: float = None,
+                                stream=None) -> None:
+    """Attention with the ragged block table (ms_mixed_step_attention_ragged): row s reads its pages
+    from ``bt_pages[bt_offsets[s]:bt_offsets[s + 1]]`` (device int32 tensors)."""
+    import torch
+    if q_rot.dim() != 3:
+        raise ValueError("q_rot must be [T, H_q, D]")
+    T, H_q, D = q_rot.shape
+    _dev(q_rot, "q_rot", torch.bfloat16)
+    if k_cache.dim() != 4:
+        raise ValueError(f"k_cache must be [pages, H_kv, {PAGE_SIZE}, D], got {tuple(k_cache.shape)}")
+    H_kv = k_cache.shape[1]
+    _pools(k_cache, v_cache, H_kv, D)
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape[0] < 1:
+        raise ValueError("cu_seqlens_q must be 1-D with rows + 1 entries")
+    S = cu_seqlens_q.shape[0] - 1
+    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _dev(q_start_pos, "q_start_pos", torch.int32, min_numel=S)
+    _dev(context_lens, "context_lens", torch.int32, min_numel=S)
+    _dev(bt_offsets, "bt_offsets", torch.int32, min_numel=S + 1)
+    _dev(bt_pages, "bt_pages", torch.int32, min_numel=1)
+    _dev(out, "out", torch.bfloat16, (T, H_q, D))
+    _dev(workspace, "workspace", None)
+    _on_one_gpu("q_rot k_cache v_cache cu_seqlens_q q_start_pos context_lens bt_offsets bt_pages out workspace",
+                q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, bt_offsets, bt_pages, out,
+                workspace)
+    if scale is None:
+        scale = float(D) ** -0.5
+    rc = lib().ms_mixed_step_attention_ragged(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                              _ptr(cu_seqlens_q), _ptr(q_start_pos), _ptr(context_lens),
+                                              _ptr(bt_offsets), _ptr(bt_pages), bt_pages.numel(), S, T,
+                                              int(context_total), H_q, H_kv, D, PAGE_SIZE, float(scale), _ptr(out),
+                                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                              _stream(stream))
+    _check(rc, "ms_mixed_step_attention_ragged")
 
 
 def mixed_step_attention_noalloc(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables,

@@ -89,7 +89,9 @@ struct AttnParams {
   const int32_t* cu;
   const int32_t* q_start;
   const int32_t* ctx_lens;
-  const int32_t* bt;
+  const int32_t* bt;      // padded rows of bt_stride entries, or (bt_off given) every row's pages back to back
+  const int32_t* bt_off;  // ragged block table: row s's pages at bt[bt_off[s] .. bt_off[s + 1]); else nullptr
+  int64_t bt_len;         // entries of bt
   bf16* out;
   int32_t* hdr;
   int32_t* dec_rows;
@@ -117,6 +119,12 @@ struct AttnParams {
 };
 
 __host__ __device__ inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// first block-table entry of row `row`: padded rows or ragged offsets
+__device__ __forceinline__ const int32_t* row_table(const AttnParams& p, int row) {
+  return p.bt + (p.bt_off != nullptr ? static_cast<int64_t>(__ldg(p.bt_off + row))
+                                     : static_cast<int64_t>(row) * p.bt_stride);
+}
 
 // ----------------------------------------------------------------------------
 // prologue: validate, classify, sort longest-first, lay out work lists
@@ -227,8 +235,13 @@ __global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParam
       const int32_t a = p.cu[s], b = p.cu[s + 1];
       const int32_t d = b - a, c = p.q_start[s], ctx = p.ctx_lens[s];
       // d == 0 is a pad row: valid, and neither a decode nor a chunk
-      const bool ok = a >= 0 && b <= p.num_tokens && d >= 0 && c >= 0 && ctx == c + d &&
-                      cdiv64(ctx, kPage) <= p.bt_stride;
+      bool ok = a >= 0 && b <= p.num_tokens && d >= 0 && c >= 0 && ctx == c + d;
+      if (p.bt_off != nullptr) {  // the row's pages must lie inside the table
+        const int64_t o0 = p.bt_off[s], o1 = p.bt_off[s + 1];
+        ok = ok && o0 >= 0 && o1 <= p.bt_len && cdiv64(ctx, kPage) <= o1 - o0;
+      } else {
+        ok = ok && cdiv64(ctx, kPage) <= p.bt_stride;
+      }
       if (ok) {
         rd[i] = d;
         rc[i] = c;
@@ -472,6 +485,7 @@ struct DecItem {
   int part;    // partial record of query head hk * G (+ g for the others)
   int ns;      // splits of the row
   int w0;      // lane j: page id of the item's page j (its first window of 32 pages)
+  const int32_t* btr;  // the row's block table
 };
 
 __device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, int split) {
@@ -491,7 +505,8 @@ __device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, i
   it.ns = __ldg(p.dec_nsplit + k);
   // the first window of page ids, loaded while the item waits its turn
   const int lane = threadIdx.x & 31;
-  it.w0 = lane < it.np ? __ldg(p.bt + static_cast<int64_t>(it.row) * p.bt_stride + it.p0 + lane) : 0;
+  it.btr = row_table(p, it.row);
+  it.w0 = lane < it.np ? __ldg(it.btr + it.p0 + lane) : 0;
   return it;
 }
 
@@ -606,7 +621,7 @@ __device__ __noinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem, c
     if ((pi & 31) == 0) {
       iss_bt = pi == 0 ? it.w0 : iss_bt_next;
       const int w = pi + 32 + lane;
-      if (pi + 32 < it.np) iss_bt_next = w < it.np ? __ldg(p.bt + static_cast<int64_t>(it.row) * p.bt_stride + it.p0 + w) : 0;
+      if (pi + 32 < it.np) iss_bt_next = w < it.np ? __ldg(it.btr + it.p0 + w) : 0;
     }
     int phys = __shfl_sync(0xffffffffu, iss_bt, pi & 31);
     if (lane == 0) {
@@ -1027,7 +1042,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
                     &bars->q_full);
       }
       const int kv_max = max(it.kv_end[0], it.kv_end[1]);
-      const int32_t* btrow = p.bt + static_cast<int64_t>(it.row) * p.bt_stride;
+      const int32_t* btrow = row_table(p, it.row);
       const int n_pages = (kv_max + kPage - 1) / kPage;
       // lane L < 4 holds the page id of page L of the current tile; the next tile's is in flight
       int pg_cur = lane < kTilePages && lane < n_pages ? __ldg(btrow + lane) : 0;
@@ -1676,19 +1691,21 @@ namespace {
 // every chunk-phase wait gives up after that many nanoseconds.
 int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, int32_t num_pages,
                    const int32_t* cu_seqlens_q, const int32_t* q_start_pos, const int32_t* context_lens,
-                   const int32_t* block_tables, int32_t bt_stride, int32_t num_rows, int32_t num_tokens,
+                   const int32_t* block_tables, const int32_t* bt_offsets, int64_t bt_len, int32_t bt_stride,
+                   int32_t num_rows, int32_t num_tokens,
                    int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
                    void* out, void* workspace, size_t ws_bytes, ms_stream_t stream, bool clear_status,
                    int64_t stall_limit_ns, bool* launched) {
   *launched = false;
   if (num_rows < 0 || num_tokens < 0 || context_total < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 ||
-      (D != 64 && D != 128) || page_size != kPage || bt_stride < 0 || num_pages < 0 || !(scale > 0.f))
+      (D != 64 && D != 128) || page_size != kPage || bt_stride < 0 || bt_len < 0 || num_pages < 0 ||
+      !(scale > 0.f))
     return MS_ERR_ARG;
   const int G = H_q / H_kv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return MS_ERR_ARG;
   if (num_rows == 0 || num_tokens == 0) return MS_OK;  // no tokens: every row is a pad row
   if (!q_rot || !k_cache || !v_cache || !cu_seqlens_q || !q_start_pos || !context_lens || !block_tables || !out ||
-      !workspace || num_pages < 1 || bt_stride < 1)
+      !workspace || num_pages < 1 || (bt_offsets == nullptr && bt_stride < 1) || (bt_offsets != nullptr && bt_len < 1))
     return MS_ERR_ARG;
   if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -1735,6 +1752,8 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
   p.q_start = q_start_pos;
   p.ctx_lens = context_lens;
   p.bt = block_tables;
+  p.bt_off = bt_offsets;
+  p.bt_len = bt_offsets != nullptr ? bt_len : static_cast<int64_t>(num_rows) * bt_stride;
   p.out = static_cast<bf16*>(out);
   p.hdr = reinterpret_cast<int32_t*>(ws + w.hdr);
   p.dec_rows = reinterpret_cast<int32_t*>(ws + w.dec_rows);
@@ -1801,8 +1820,23 @@ extern "C" MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_c
                                               size_t ws_bytes, ms_stream_t stream) {
   bool launched = false;
   return attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens, block_tables,
-                        bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D, page_size, scale, out,
+                        nullptr, 0, bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D, page_size, scale, out,
                         workspace, ws_bytes, stream, false, 0, &launched);
+}
+
+extern "C" MS_API int ms_mixed_step_attention_ragged(const void* q_rot, const void* k_cache, const void* v_cache,
+                                                     int32_t num_pages, const int32_t* cu_seqlens_q,
+                                                     const int32_t* q_start_pos, const int32_t* context_lens,
+                                                     const int32_t* bt_offsets, const int32_t* bt_pages,
+                                                     int64_t num_bt_pages, int32_t num_rows, int32_t num_tokens,
+                                                     int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D,
+                                                     int32_t page_size, float scale, void* out, void* workspace,
+                                                     size_t ws_bytes, ms_stream_t stream) {
+  if (bt_offsets == nullptr && num_rows > 0 && num_tokens > 0) return MS_ERR_ARG;
+  bool launched = false;
+  return attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens, bt_pages,
+                        bt_offsets, num_bt_pages, 0, num_rows, num_tokens, context_total, H_q, H_kv, D, page_size,
+                        scale, out, workspace, ws_bytes, stream, false, 0, &launched);
 }
 
 extern "C" MS_API int ms_test_attention_stall(const void* q_rot, const void* k_cache, const void* v_cache,
@@ -1815,7 +1849,7 @@ extern "C" MS_API int ms_test_attention_stall(const void* q_rot, const void* k_c
   if (wait_limit_ns < 100000 || wait_limit_ns > 2000000000ll) return MS_ERR_ARG;  // 0.1 ms .. 2 s
   bool launched = false;
   return attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens, block_tables,
-                        bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D, page_size, scale, out,
+                        nullptr, 0, bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D, page_size, scale, out,
                         workspace, ws_bytes, stream, false, wait_limit_ns, &launched);
 }
 
@@ -1893,7 +1927,7 @@ extern "C" MS_API int ms_mixed_step_attention_noalloc(const void* q_rot, const v
   // prologue, so the prologue still overlaps the append.
   bool launched = false;
   const int rc = attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens,
-                                block_tables, bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D,
+                                block_tables, nullptr, 0, bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D,
                                 page_size, scale, out, scratch, kNoAllocScratchBytes, stream, true, 0, &launched);
   if (rc != MS_OK) return rc;
   if (dev_status != nullptr) {

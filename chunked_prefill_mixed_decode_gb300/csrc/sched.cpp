@@ -32,14 +32,22 @@ struct Row {
   int32_t d;
 };
 
-}  // namespace
+// Block-table output of one packing: either rows of `stride` entries padded
+// with -1 (block_tables, cap entries) or each row's pages back to back after
+// its offset (bt_offsets [rows + 1], bt_pages, cap entries).
+struct TableOut {
+  int32_t* block_tables;
+  int32_t* bt_offsets;
+  int32_t* bt_pages;
+  int64_t cap;
+  bool ragged;
+};
 
-extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_req, const ms_sched_config* cfg,
-                                              int32_t cap_rows, int32_t cap_tokens, int64_t cap_bt,
-                                              int32_t* cu_seqlens_q, int32_t* q_start_pos,
-                                              int32_t* context_lens, int32_t* positions, int32_t* slot_mapping,
-                                              int32_t* block_tables, int32_t* row_req, int32_t* num_scheduled,
-                                              ms_batch_info* info) {
+int build_metadata(const ms_request* reqs, int32_t n_req, const ms_sched_config* cfg, int32_t cap_rows,
+                   int32_t cap_tokens, const TableOut& tab, int32_t* cu_seqlens_q, int32_t* q_start_pos,
+                   int32_t* context_lens, int32_t* positions, int32_t* slot_mapping, int32_t* row_req,
+                   int32_t* num_scheduled, ms_batch_info* info) {
+  int32_t* block_tables = tab.block_tables;
   if (n_req < 0 || cfg == nullptr || info == nullptr || cu_seqlens_q == nullptr || q_start_pos == nullptr ||
       context_lens == nullptr || row_req == nullptr || (n_req > 0 && (reqs == nullptr || num_scheduled == nullptr)))
     return MS_ERR_ARG;
@@ -135,15 +143,24 @@ extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_
     for (int32_t p = 0; p < need; ++p)
       if (bt[p] < 0 || bt[p] > INT32_MAX / kPage - 1) return MS_ERR_ARG;
   }
-  if (S > cap_rows || used > cap_tokens || static_cast<int64_t>(S) * stride > cap_bt) return MS_ERR_ARG;
+  int64_t table_entries = static_cast<int64_t>(S) * stride;  // padded rows
+  if (tab.ragged) {
+    table_entries = 0;  // the pages in use, back to back
+    for (const Row& r : rows) table_entries += ceil_div(static_cast<int64_t>(r.c) + r.d, kPage);
+    if (table_entries > INT32_MAX) return MS_ERR_ARG;
+  }
+  if (S > cap_rows || used > cap_tokens || table_entries > tab.cap) return MS_ERR_ARG;
   if (n_req > 0 && num_scheduled == nullptr) return MS_ERR_ARG;
   if (used > 0 && (positions == nullptr || slot_mapping == nullptr)) return MS_ERR_ARG;
-  if (static_cast<int64_t>(S) * stride > 0 && block_tables == nullptr) return MS_ERR_ARG;
+  if (tab.ragged ? (tab.bt_offsets == nullptr || (table_entries > 0 && tab.bt_pages == nullptr))
+                 : (table_entries > 0 && block_tables == nullptr))
+    return MS_ERR_ARG;
 
   // 4. metadata
   for (int32_t i = 0; i < n_req; ++i) num_scheduled[i] = 0;
   cu_seqlens_q[0] = 0;
   int32_t t = 0;
+  int32_t bt_next = 0;  // next free entry of bt_pages
   for (int32_t s = 0; s < S; ++s) {
     const Row& r = rows[s];
     const int32_t* bt = reqs[r.req].block_table;
@@ -158,10 +175,17 @@ extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_
       slot_mapping[t] = bt[pos / kPage] * kPage + pos % kPage;
     }
     const int32_t need = ceil_div(static_cast<int64_t>(r.c) + r.d, kPage);
-    int32_t* dst = block_tables + static_cast<int64_t>(s) * stride;
-    std::memcpy(dst, bt, static_cast<size_t>(need) * sizeof(int32_t));
-    std::fill(dst + need, dst + stride, -1);
+    if (tab.ragged) {
+      std::memcpy(tab.bt_pages + bt_next, bt, static_cast<size_t>(need) * sizeof(int32_t));
+      tab.bt_offsets[s] = bt_next;
+      bt_next += need;
+    } else {
+      int32_t* dst = block_tables + static_cast<int64_t>(s) * stride;
+      std::memcpy(dst, bt, static_cast<size_t>(need) * sizeof(int32_t));
+      std::fill(dst + need, dst + stride, -1);
+    }
   }
+  if (tab.ragged) tab.bt_offsets[S] = bt_next;
   info->num_rows = S;
   info->num_decodes = num_decodes;
   info->num_tokens = static_cast<int32_t>(used);
@@ -169,6 +193,30 @@ extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_
   info->unused_tokens = static_cast<int32_t>(budget - used);
   info->num_deferred = static_cast<int32_t>(n_decodes - n_dec);
   return MS_OK;
+}
+
+}  // namespace
+
+extern "C" MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_req, const ms_sched_config* cfg,
+                                              int32_t cap_rows, int32_t cap_tokens, int64_t cap_bt,
+                                              int32_t* cu_seqlens_q, int32_t* q_start_pos,
+                                              int32_t* context_lens, int32_t* positions, int32_t* slot_mapping,
+                                              int32_t* block_tables, int32_t* row_req, int32_t* num_scheduled,
+                                              ms_batch_info* info) {
+  const TableOut tab{block_tables, nullptr, nullptr, cap_bt, false};
+  return build_metadata(reqs, n_req, cfg, cap_rows, cap_tokens, tab, cu_seqlens_q, q_start_pos, context_lens,
+                        positions, slot_mapping, row_req, num_scheduled, info);
+}
+
+extern "C" MS_API int ms_build_batch_metadata_ragged(const ms_request* reqs, int32_t n_req,
+                                                     const ms_sched_config* cfg, int32_t cap_rows,
+                                                     int32_t cap_tokens, int64_t cap_pages, int32_t* cu_seqlens_q,
+                                                     int32_t* q_start_pos, int32_t* context_lens, int32_t* positions,
+                                                     int32_t* slot_mapping, int32_t* bt_offsets, int32_t* bt_pages,
+                                                     int32_t* row_req, int32_t* num_scheduled, ms_batch_info* info) {
+  const TableOut tab{nullptr, bt_offsets, bt_pages, cap_pages, true};
+  return build_metadata(reqs, n_req, cfg, cap_rows, cap_tokens, tab, cu_seqlens_q, q_start_pos, context_lens,
+                        positions, slot_mapping, row_req, num_scheduled, info);
 }
 
 extern "C" MS_API int ms_rope_table(int32_t max_pos, int32_t D, double base, float* cos_tab, float* sin_tab) {

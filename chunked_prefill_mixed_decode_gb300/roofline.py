@@ -12,7 +12,9 @@ Counts follow the pages' cost model:
   token reads against 4,096.
 
 Bytes count each row's K and V once per KV head (shared by its G query heads),
-Q in and O out, and the append's reads and writes; nothing padded or re-read.
+Q in and O out, the append's reads and writes, and the metadata: row offsets,
+positions and lengths, and each row's ceil((c + d) / 16) page ids (zwjcode
+section 06), the block table in its ragged form; nothing padded or re-read.
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ from typing import Iterable, Tuple
 BF16 = 2
 
 
-def step_counts(rows: Iterable[Tuple[int, int]], H_q: int, H_kv: int, D: int, bt_stride: int = 0) -> dict:
+def step_counts(rows: Iterable[Tuple[int, int]], H_q: int, H_kv: int, D: int) -> dict:
     """rows: (c, d) per packed row.  Returns FLOPs and bytes of append and attention."""
     rows = [(int(c), int(d)) for c, d in rows]
     T = sum(d for _, d in rows)
@@ -29,7 +31,8 @@ def step_counts(rows: Iterable[Tuple[int, int]], H_q: int, H_kv: int, D: int, bt
     pairs = sum(d * c + d * (d + 1) // 2 for c, d in rows)
     kv_tokens = sum(c + d for c, d in rows)
     flops = 4 * D * H_q * pairs
-    meta_bytes = 4 * ((S + 1) + 2 * S + S * bt_stride)
+    pages = sum((c + d + 15) // 16 for c, d in rows)
+    meta_bytes = 4 * ((S + 1) + 2 * S + (S + 1) + pages)
     attn_bytes = kv_tokens * H_kv * D * BF16 * 2 + 2 * T * H_q * D * BF16 + meta_bytes
     append_bytes = T * (2 * H_q * D * BF16 + 4 * H_kv * D * BF16 + 2 * (D // 2) * 4) + 8 * T
     dec = [(c, d) for c, d in rows if d == 1]

@@ -10,10 +10,15 @@ import dataclasses
 
 import numpy as np
 
-from . import (attention_workspace_size, build_batch_metadata, kv_append_rope, mixed_step_attention,
+from . import (attention_workspace_size, kv_append_rope, mixed_step_attention, mixed_step_attention_ragged,
                rope_table)
 
 META_KEYS = ("cu_seqlens_q", "q_start_pos", "context_lens", "positions", "slot_mapping", "block_tables")
+RAGGED_KEYS = ("cu_seqlens_q", "q_start_pos", "context_lens", "positions", "slot_mapping", "bt_offsets", "bt_pages")
+
+
+def _keys(meta: dict):
+    return RAGGED_KEYS if "bt_offsets" in meta else META_KEYS
 
 
 @dataclasses.dataclass
@@ -30,16 +35,21 @@ class DeviceBatch:
     num_decodes: int
     context_total: int
     host: dict
+    bt_offsets: object = None  # ragged block table (then block_tables holds the pages back to back)
+
+    @property
+    def ragged(self) -> bool:
+        return self.bt_offsets is not None
 
     @property
     def h2d_bytes(self) -> int:
-        return sum(int(self.host[k].nbytes) for k in META_KEYS)
+        return sum(int(np.asarray(self.host[k]).nbytes) for k in _keys(self.host))
 
 
 def to_device(meta: dict, device, non_blocking: bool = False) -> DeviceBatch:
     import torch
     t = {}
-    for k in META_KEYS:
+    for k in _keys(meta):
         a = np.ascontiguousarray(meta[k], dtype=np.int32)
         if a.size == 0:
             a = np.zeros(1, dtype=np.int32)  # keep a valid device pointer for empty arrays
@@ -47,13 +57,17 @@ def to_device(meta: dict, device, non_blocking: bool = False) -> DeviceBatch:
         if non_blocking:
             src = src.pin_memory()
         t[k] = src.to(device, non_blocking=non_blocking)
-    bt = t["block_tables"]
     S = int(meta["num_rows"])
+    ctx_total = int(np.asarray(meta["context_lens"], dtype=np.int64).sum())
+    if "bt_offsets" in meta:
+        return DeviceBatch(t["cu_seqlens_q"], t["q_start_pos"], t["context_lens"], t["positions"],
+                           t["slot_mapping"], t["bt_pages"], S, int(meta["num_tokens"]), int(meta["num_decodes"]),
+                           ctx_total, meta, bt_offsets=t["bt_offsets"])
+    bt = t["block_tables"]
     stride = int(meta["bt_stride"])
     t["block_tables"] = bt.view(max(S, 1), max(stride, 1)) if S > 0 and stride > 0 else bt.view(1, 1)
     return DeviceBatch(t["cu_seqlens_q"], t["q_start_pos"], t["context_lens"], t["positions"], t["slot_mapping"],
-                       t["block_tables"], S, int(meta["num_tokens"]), int(meta["num_decodes"]),
-                       int(np.asarray(meta["context_lens"], dtype=np.int64).sum()), meta)
+                       t["block_tables"], S, int(meta["num_tokens"]), int(meta["num_decodes"]), ctx_total, meta)
 
 
 class MetaStager:
@@ -87,7 +101,9 @@ class MetaStager:
     def stage(self, meta: dict, stream=None) -> DeviceBatch:
         import torch
         S, T, stride = int(meta["num_rows"]), int(meta["num_tokens"]), int(meta["bt_stride"])
-        need = 3 * S + 1 + 2 * T + S * stride + 6 * 4
+        ragged = "bt_offsets" in meta
+        n_bt = (S + 1 + int(meta["bt_offsets"][S])) if ragged else S * stride
+        need = 3 * S + 1 + 2 * T + n_bt + 7 * 4
         if need > self.cap:
             self._grow(max(need, 2 * self.cap))
         i = self.flip
@@ -96,8 +112,10 @@ class MetaStager:
             self.events[i].synchronize()
         hv = self.host[i].numpy()
         views, off = {}, 0
+        tabs = ((("bt_offsets", S + 1), ("bt_pages", int(meta["bt_offsets"][S]))) if ragged
+                else (("block_tables", S * stride),))
         for k, n in (("cu_seqlens_q", S + 1), ("q_start_pos", S), ("context_lens", S), ("positions", T),
-                     ("slot_mapping", T), ("block_tables", S * stride)):
+                     ("slot_mapping", T)) + tabs:
             n_alloc = max(n, 1)
             if off + n_alloc > self.cap:
                 raise ValueError("metadata larger than the stager's capacity")
@@ -111,14 +129,14 @@ class MetaStager:
             ev.record(st)
         self.events[i] = ev
         d = {k: self.dev[i][o:o + n] for k, (o, n) in views.items()}
+        ctx_total = int(np.asarray(meta["context_lens"], dtype=np.int64).sum())
+        if ragged:
+            return DeviceBatch(d["cu_seqlens_q"], d["q_start_pos"], d["context_lens"], d["positions"],
+                               d["slot_mapping"], d["bt_pages"], S, T, int(meta["num_decodes"]), ctx_total, meta,
+                               bt_offsets=d["bt_offsets"])
         bt = d["block_tables"].view(S, stride) if S > 0 and stride > 0 else d["block_tables"][:1].view(1, 1)
         return DeviceBatch(d["cu_seqlens_q"], d["q_start_pos"], d["context_lens"], d["positions"],
-                           d["slot_mapping"], bt, S, T, int(meta["num_decodes"]),
-                           int(np.asarray(meta["context_lens"], dtype=np.int64).sum()), meta)
-
-
-def schedule(states, block_tables, token_budget, max_chunk=0) -> dict:
-    return build_batch_metadata(states, block_tables, token_budget, max_chunk)
+                           d["slot_mapping"], bt, S, T, int(meta["num_decodes"]), ctx_total, meta)
 
 
 def rope_tables_device(max_pos: int, D: int, device, base: float = 10000.0):
@@ -142,6 +160,16 @@ def run_step(q, k, v, batch: DeviceBatch, cos, sin, k_cache, v_cache, out, works
     T = batch.num_tokens
     kv_append_rope(q[:T], k[:T], v[:T], batch.positions, batch.slot_mapping, cos, sin, k_cache, v_cache,
                    q_rot=q_rot[:T], dev_status=dev_status, stream=stream)
-    mixed_step_attention(q_rot[:T], k_cache, v_cache, batch.cu_seqlens_q, batch.q_start_pos, batch.context_lens,
-                         batch.block_tables, batch.context_total, out[:T], workspace, scale=scale, stream=stream)
+    attend(q_rot[:T], k_cache, v_cache, batch, out[:T], workspace, scale=scale, stream=stream)
     return q_rot
+
+
+def attend(q_rot, k_cache, v_cache, batch: DeviceBatch, out, workspace, scale=None, stream=None) -> None:
+    """The attention call of a staged batch, with its padded or ragged block table."""
+    if batch.ragged:
+        mixed_step_attention_ragged(q_rot, k_cache, v_cache, batch.cu_seqlens_q, batch.q_start_pos,
+                                    batch.context_lens, batch.bt_offsets, batch.block_tables, batch.context_total,
+                                    out, workspace, scale=scale, stream=stream)
+    else:
+        mixed_step_attention(q_rot, k_cache, v_cache, batch.cu_seqlens_q, batch.q_start_pos, batch.context_lens,
+                             batch.block_tables, batch.context_total, out, workspace, scale=scale, stream=stream)

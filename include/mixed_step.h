@@ -161,6 +161,26 @@ MS_API int ms_build_batch_metadata(const ms_request* reqs, int32_t n_req, const 
                                    int32_t* positions, int32_t* slot_mapping, int32_t* block_tables,
                                    int32_t* row_req, int32_t* num_scheduled, ms_batch_info* info);
 
+/* ms_build_batch_metadata_ragged -- the same packing and metadata as
+ * ms_build_batch_metadata, with the block table in its ragged form: row s
+ * holds exactly the ceil((c+d)/16) pages it reads ([zwj] section 06 gives a
+ * row ceil((c+d)/B) entries), at bt_pages[bt_offsets[s] .. bt_offsets[s+1]).
+ * The padded form costs rows x (longest row's pages) entries; in a step that
+ * mixes a few 64K-128K-token decodes with hundreds of short ones that is over
+ * ten times the pages in use, built on the host and copied to the device every
+ * step.
+ *   bt_offsets [cap_rows + 1]  host int32, bt_offsets[0] = 0, bt_offsets[S] = pages
+ *   bt_pages   [cap_pages]     host int32 page ids, row after row
+ * The other outputs, info (bt_stride is still the longest row's page count)
+ * and the errors are those of ms_build_batch_metadata; MS_ERR_ARG also when
+ * the pages exceed cap_pages. */
+MS_API int ms_build_batch_metadata_ragged(const ms_request* reqs, int32_t n_req, const ms_sched_config* cfg,
+                                          int32_t cap_rows, int32_t cap_tokens, int64_t cap_pages,
+                                          int32_t* cu_seqlens_q, int32_t* q_start_pos, int32_t* context_lens,
+                                          int32_t* positions, int32_t* slot_mapping, int32_t* bt_offsets,
+                                          int32_t* bt_pages, int32_t* row_req, int32_t* num_scheduled,
+                                          ms_batch_info* info);
+
 /* ms_rope_table -- host: cos/sin of p * base^(-2i/D) for p < max_pos, i < D/2,
  * computed in double precision and rounded to fp32.  Output layout
  * [max_pos][D/2] row-major, caller-allocated host buffers.  The rotary phase
@@ -240,6 +260,24 @@ MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_cache, const
                                    int64_t context_total,
                                    int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
                                    void* out, void* workspace, size_t ws_bytes, ms_stream_t stream);
+
+/* ms_mixed_step_attention_ragged -- ms_mixed_step_attention with the block
+ * table in the ragged form of ms_build_batch_metadata_ragged: row s reads its
+ * pages from bt_pages[bt_offsets[s] ..], and bt_offsets[s + 1] - bt_offsets[s]
+ * must be at least ceil(context_lens[s] / 16).
+ *   bt_offsets   device int32 [num_rows + 1]
+ *   bt_pages     device int32 [num_bt_pages]
+ * A row whose pages fall outside bt_pages, or has fewer than it needs, makes
+ * the step compute nothing and sets MS_STATUS_BAD_META.  Everything else
+ * (layouts, workspace, status, errors) is as ms_mixed_step_attention. */
+MS_API int ms_mixed_step_attention_ragged(const void* q_rot, const void* k_cache, const void* v_cache,
+                                          int32_t num_pages,
+                                          const int32_t* cu_seqlens_q, const int32_t* q_start_pos,
+                                          const int32_t* context_lens, const int32_t* bt_offsets,
+                                          const int32_t* bt_pages, int64_t num_bt_pages,
+                                          int32_t num_rows, int32_t num_tokens, int64_t context_total,
+                                          int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
+                                          void* out, void* workspace, size_t ws_bytes, ms_stream_t stream);
 
 /* ms_mixed_step_attention_noalloc -- the same attention step as
  * ms_mixed_step_attention, for callers that cannot give the library a

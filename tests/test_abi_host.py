@@ -375,3 +375,88 @@ def test_page_ids_a_row_reads_must_be_valid(ms):
     with pytest.raises(ms.MixedStepError) as e:  # a chunk row reads every page up to its last token
         ms.build_batch_metadata([(0, 40)], [np.asarray([0, -1, 2], dtype=np.int32)], 64)
     assert e.value.code == ms.MS_ERR_ARG
+
+
+# ------------------------------------------------------------------ ragged block tables
+
+def _expand_ragged(got):
+    """The ragged block table (bt_offsets, bt_pages) as the padded [rows, stride] table."""
+    S, stride = got["num_rows"], got["bt_stride"]
+    out = np.full((S, stride), -1, dtype=np.int32)
+    off = got["bt_offsets"]
+    assert off[0] == 0 and np.all(np.diff(off) >= 0) and off[S] == got["bt_pages"].size
+    for s in range(S):
+        out[s, : off[s + 1] - off[s]] = got["bt_pages"][off[s]: off[s + 1]]
+    return out
+
+
+def _assert_ragged_meta_equal(got, ref):
+    """zwjcode section 06: row s holds ceil((c+d)/16) pages -- exactly that many in the ragged form."""
+    need = -(-np.asarray(got["context_lens"], dtype=np.int64) // 16)
+    np.testing.assert_array_equal(np.diff(got["bt_offsets"]), need)
+    padded = dict(got)
+    padded["block_tables"] = _expand_ragged(got)
+    _assert_meta_equal(padded, ref)
+
+
+@pytest.mark.parametrize("name", ["worked_example_b8", "mha7b_b512", "mha13b_b2048", "gqa8b_b8192",
+                                  "long_bimodal_b4608"])
+def test_ragged_metadata_matches_oracle_expanded(ms, name):
+    wls = workloads.CONFIGS[name]()
+    wls = wls if isinstance(wls, list) else [wls]
+    for wl in wls[:3]:
+        tables = [r.block_table for r in wl.requests]
+        states = [(r.cached_len, r.remaining) for r in wl.requests]
+        got = ms.build_batch_metadata(states, tables, wl.token_budget, wl.max_chunk, ragged=True)
+        _assert_ragged_meta_equal(got, _oracle_meta(states, tables, wl.token_budget, wl.max_chunk))
+
+
+def test_ragged_scheduler_fuzz_and_errors(ms):
+    rng = np.random.default_rng(22)
+    for trial in range(300):
+        n = int(rng.integers(0, 12))
+        budget = int(rng.integers(0, 40))
+        cap = int(rng.integers(0, 3)) * int(rng.integers(1, 9))
+        states, tables = [], []
+        for _ in range(n):
+            c = int(rng.integers(0, 100))
+            rem = 0 if rng.random() < 0.5 else int(rng.integers(1, 60))
+            need = -(-(c + max(rem, 1)) // 16)
+            short = rng.random() < 0.08
+            n_pages = max(0, need - int(rng.integers(1, 3))) if short else need + int(rng.integers(0, 3))
+            tables.append(rng.integers(0, 1000, size=n_pages).astype(np.int32))
+            states.append((c, rem))
+        try:
+            ref = _oracle_meta(states, tables, budget, cap)
+            err = None
+        except oracle.BudgetError:
+            err = ms.MS_ERR_BUDGET
+        except oracle.NoPagesError:
+            err = ms.MS_ERR_NO_PAGES
+        if err is None:
+            _assert_ragged_meta_equal(ms.build_batch_metadata(states, tables, budget, cap, ragged=True), ref)
+        else:
+            with pytest.raises(ms.MixedStepError) as e:
+                ms.build_batch_metadata(states, tables, budget, cap, ragged=True)
+            assert e.value.code == err
+
+
+def test_ragged_scheduler_refuses_too_small_page_capacity(ms):
+    """Three decodes of 2, 1 and 3 pages need 6 entries: capacity 5 is MS_ERR_ARG, 6 is enough."""
+    lib = ms.lib()
+    states = [(20, 0), (3, 0), (40, 0)]
+    tables = [np.arange(4, dtype=np.int32), np.arange(4, 8, dtype=np.int32), np.arange(8, 12, dtype=np.int32)]
+    reqs = (ms.Request * 3)()
+    for i, ((c, r), t) in enumerate(zip(states, tables)):
+        reqs[i] = ms.Request(c, r, t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(t))
+    cfg = ms.SchedConfig(8, 0, 0, 0, 0, 500)
+    arr = {k: np.zeros(16, dtype=np.int32) for k in ("cu", "qs", "ctx", "pos", "slot", "off", "pages", "rr", "ns")}
+    info = ms.BatchInfo()
+    p = {k: v.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) for k, v in arr.items()}
+    for cap, want in ((5, ms.MS_ERR_ARG), (6, ms.MS_OK)):
+        rc = lib.ms_build_batch_metadata_ragged(reqs, 3, ctypes.byref(cfg), 3, 8, cap, p["cu"], p["qs"], p["ctx"],
+                                                p["pos"], p["slot"], p["off"], p["pages"], p["rr"], p["ns"],
+                                                ctypes.byref(info))
+        assert rc == want, (cap, rc)
+    assert arr["off"][:4].tolist() == [0, 2, 3, 6]
+    assert arr["pages"][:6].tolist() == [0, 1, 4, 8, 9, 10]

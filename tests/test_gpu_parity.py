@@ -358,6 +358,74 @@ def test_stalled_chunk_phase_times_out_and_the_workspace_recovers(env):
         _check_attention(workloads.bf16_bits(again[:T]), ref, f"call after stall {attempt}")
 
 
+def _ragged_batch(env, wl, states, dev="cuda"):
+    torch, ms, step = env
+    meta = ms.build_batch_metadata(states, _tables(wl), wl.token_budget, wl.max_chunk, ragged=True)
+    return meta, step.to_device(meta, dev)
+
+
+@pytest.mark.parametrize("H_q,H_kv,D", [(8, 2, 128), (8, 4, 64), (4, 4, 128)])
+def test_ragged_block_table_matches_padded_and_oracle(env, H_q, H_kv, D):
+    """zwjcode section 06 gives each row ceil((c+d)/B) block-table entries: the ragged form passes exactly
+    those.  Its attention output equals the padded call's bit for bit (the same pages are read) and the
+    oracle's within tolerance."""
+    torch, ms, step = env
+    wl = workloads.small_mixed(seed=H_q * 3 + H_kv + D, H_q=H_q, H_kv=H_kv, D=D)
+    case = Case(env, wl, _states(wl), seed=21).run(env)
+    T = case.meta["num_tokens"]
+    rmeta, rb = _ragged_batch(env, wl, _states(wl))
+    assert rb.ragged and rb.block_tables.numel() < case.batch.block_tables.numel()
+    out = torch.zeros_like(case.out)
+    ws = step.workspace_for(rb, wl.H_q, wl.H_kv, wl.D, "cuda")
+    step.attend(case.q_rot[:T], case.k_cache, case.v_cache, rb, out[:T], ws)
+    torch.cuda.synchronize()
+    assert ms.read_status(ws) == 0
+    np.testing.assert_array_equal(workloads.bf16_bits(out[:T]), workloads.bf16_bits(case.out[:T]))
+    ref_meta, (q_rot, kp, vp) = case.oracle_append()
+    ref = oracle.attention_all(q_rot, kp, vp, ref_meta, wl.H_kv)
+    _check_attention(workloads.bf16_bits(out[:T]), ref, "ragged")
+
+
+def test_ragged_row_short_of_pages_is_flagged(env):
+    """A row whose offsets give it fewer pages than ceil(context/16) makes the step compute nothing and
+    set BAD_META; so does an offset past the end of the page list."""
+    torch, ms, step = env
+    wl = workloads.small_mixed(seed=44, H_q=8, H_kv=2, D=128, dec_ctx=(20, 40), prompts=((0, 33),))
+    case = Case(env, wl, _states(wl), seed=4).run(env)
+    rmeta, rb = _ragged_batch(env, wl, _states(wl))
+    ws = step.workspace_for(rb, wl.H_q, wl.H_kv, wl.D, "cuda")
+    for bad in ("short", "past_end"):
+        off = rb.bt_offsets.clone()
+        if bad == "short":
+            off[1] -= 1  # row 0 loses a page (row 1 gains one)
+        else:
+            off[-1] += 5
+        b2 = step.DeviceBatch(rb.cu_seqlens_q, rb.q_start_pos, rb.context_lens, rb.positions, rb.slot_mapping,
+                              rb.block_tables, rb.num_rows, rb.num_tokens, rb.num_decodes, rb.context_total,
+                              rb.host, bt_offsets=off)
+        out = torch.zeros_like(case.out)
+        step.attend(case.q_rot, case.k_cache, case.v_cache, b2, out, ws)
+        torch.cuda.synchronize()
+        assert ms.read_status(ws) & ms.STATUS_BAD_META, bad
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["gqa8b_b8192", "long_bimodal_b4608"])
+def test_full_size_ragged_equals_padded(env, name):
+    """The full-size step with the ragged block table gives the padded call's output bit for bit."""
+    torch, ms, step = env
+    wl = workloads.CONFIGS[name]()
+    case = Case(env, wl, _states(wl), seed=23, host_pool=False).run(env)
+    T = case.meta["num_tokens"]
+    rmeta, rb = _ragged_batch(env, wl, _states(wl))
+    out = torch.zeros_like(case.out)
+    ws = step.workspace_for(rb, wl.H_q, wl.H_kv, wl.D, "cuda")
+    step.attend(case.q_rot[:T], case.k_cache, case.v_cache, rb, out[:T], ws)
+    torch.cuda.synchronize()
+    assert ms.read_status(ws) == 0
+    assert torch.equal(out[:T].view(torch.int16), case.out[:T].view(torch.int16))
+
+
 # ------------------------------------------------------------------ full-size configurations (sampled)
 
 def _sampled_parity(env, wl, seed, n_dec_rows=48, n_chunk_tokens=48, heads=None):
