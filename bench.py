@@ -1,8 +1,9 @@
 #!/usr/bin/env python
 """Mixed-step attention throughput on GB300: tokens/s and fraction of the step roofline.
 
-One timed step is one pass of the whole hot path -- ms_kv_append_rope then
-ms_mixed_step_attention_ragged -- over every batch of a workload.  By default all four
+One timed step is one pass of the whole hot path -- ms_mixed_step: the append
+(ms_kv_append_rope) then the attention (ms_mixed_step_attention_ragged) in one
+call -- over every batch of a workload.  By default all four
 full-size workloads run one after another and print ONE JSON line: its top level
 is the largest single-GPU step, the long-context bimodal batch (the last
 4096-token chunk of a 32768-token prompt next to 512 decodes, 10 % of them at
@@ -260,15 +261,14 @@ def measure_config(name, args, ms, world, rank, device, dist) -> dict:
     k_cache, v_cache = pool
 
     def one_step(events=None):
-        # a batch's events bracket its append and attention call, with nothing between
-        # the two: the attention call's kernels launch as programmatic dependents of the append
+        # a batch's events bracket its step call (append, then attention, whose kernels
+        # launch as programmatic dependents of the append's)
         for j, s in enumerate(subs):
             b = s["batch"]
             if events is not None:
                 events[j][0].record(stream)
-            ms.kv_append_rope(s["q"], s["k"], s["v"], b.positions, b.slot_mapping, cos, sin, k_cache, v_cache,
-                              q_rot=s["q_rot"], dev_status=status, stream=stream)
-            step.attend(s["q_rot"], k_cache, v_cache, b, s["out"], ws, stream=stream)
+            step.run_step(s["q"], s["k"], s["v"], b, cos, sin, k_cache, v_cache, s["out"], ws, q_rot=s["q_rot"],
+                          dev_status=status, stream=stream)
             if events is not None:
                 events[j][1].record(stream)
 
@@ -333,8 +333,8 @@ def measure_config(name, args, ms, world, rank, device, dist) -> dict:
         roof["traffic_source"] = (f"ncu capture of batch {b} (append + attention kernels)"
                                   + (", scaled by algorithmic bytes" if n_sub > 1 else ""))
         roof["traffic_vs_alg_bytes"] = round(roof["traffic"] / grp_bytes_avg, 4)
-    roof["kernel"] = ("one batch of the path: ms_kv_append_rope + ms_mixed_step_attention_ragged "
-                      "(append, prologue, items and persistent attention_kernel launches)")
+    roof["kernel"] = ("one batch of the path: ms_mixed_step (the append with the prologue in its launch, "
+                      "then the persistent attention_kernel)")
     roof["peak_source"] = (f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
                            + ("; sustained bf16 (kernel timed inside a step)" if roof["bound"] == "tensor" else ""))
     roof["per_launch"] = {"alg_bytes": int(grp_bytes_avg), "alg_flops": int(flops_avg),
@@ -358,7 +358,10 @@ def measure_config(name, args, ms, world, rank, device, dist) -> dict:
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16; KV pool larger than L2)",
         "config": config_block(name, wls, world),
         "roofline": roof, "step_roofline": step_roof, "e2e": e2e,
-        "gpu_launches": 4 * n_sub * args.steps, "clocks": clocks,
+        # per batch: the append with the prologue in its launch (one kernel on steps of at most
+        # FUSED_STEP_MAX_ROWS rows, else two), then the persistent attention kernel
+        "gpu_launches": sum(2 if s["meta"]["num_rows"] <= ms.FUSED_STEP_MAX_ROWS else 3 for s in subs) * args.steps,
+        "clocks": clocks,
     }
     del subs, ws, pool, k_cache, v_cache
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -409,9 +412,8 @@ def run_e2e(args, ms, step, subs, cos, sin, k_cache, v_cache, ws, status, device
             stream.wait_event(ready)
             if fetched[i][par] is not None:
                 stream.wait_event(fetched[i][par])
-            ms.kv_append_rope(sl["q"], sl["k"], sl["v"], b.positions, b.slot_mapping, cos, sin, k_cache, v_cache,
-                              q_rot=sl["q_rot"], dev_status=status, stream=stream)
-            step.attend(sl["q_rot"], k_cache, v_cache, b, sl["out"], ws, stream=stream)
+            step.run_step(sl["q"], sl["k"], sl["v"], b, cos, sin, k_cache, v_cache, sl["out"], ws, q_rot=sl["q_rot"],
+                          dev_status=status, stream=stream)
             fin = torch.cuda.Event()
             fin.record(stream)
             computed[i][par] = fin

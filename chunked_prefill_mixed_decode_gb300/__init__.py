@@ -75,6 +75,10 @@ class GraphBuffers(ctypes.Structure):
 
 
 _lib_handle = None
+# ms_mixed_step runs the attention's prologue inside the append's launch on steps of at most
+# this many rows (mixed_step.h)
+FUSED_STEP_MAX_ROWS = 1024
+
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _VP = ctypes.c_void_p
 
@@ -114,6 +118,11 @@ def lib() -> ctypes.CDLL:
                                                  ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                  ctypes.c_float, _VP, _VP, ctypes.c_size_t, _VP]
+    h.ms_mixed_step.restype = ctypes.c_int
+    h.ms_mixed_step.argtypes = [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP, ctypes.c_int32, _VP,
+                                _VP, _VP, _VP, _VP, _VP, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                ctypes.c_int32, ctypes.c_float, _VP, _VP, ctypes.c_size_t, _VP, _VP]
     h.ms_mixed_step_attention_noalloc.restype = ctypes.c_int
     h.ms_mixed_step_attention_noalloc.argtypes = [_VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP, _VP,
                                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
@@ -619,6 +628,63 @@ def mixed_step_attention_ragged(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_p
                                               _ptr(workspace), workspace.numel() * workspace.element_size(),
                                               _stream(stream))
     _check(rc, "ms_mixed_step_attention_ragged")
+
+
+def mixed_step(q, k, v, positions, slot_mapping, cos_tab, sin_tab, k_cache, v_cache, q_rot, cu_seqlens_q,
+               q_start_pos, context_lens, block_tables, context_total: int, out, workspace, bt_offsets=None,
+               dev_status=None, scale: float = None, stream=None) -> None:
+    """Append + attention of one step in one call (ms_mixed_step).  ``block_tables`` is the padded
+    [rows, stride] table, or, with ``bt_offsets`` given, the ragged page list; the other arguments are
+    those of kv_append_rope and mixed_step_attention(_ragged)."""
+    import torch
+    if q.dim() != 3:
+        raise ValueError(f"q must be [T, H_q, D], got {tuple(q.shape)}")
+    T, H_q, D = q.shape
+    if k_cache.dim() != 4:
+        raise ValueError(f"k_cache must be [pages, H_kv, {PAGE_SIZE}, D], got {tuple(k_cache.shape)}")
+    H_kv = k_cache.shape[1]
+    _dev(q, "q", torch.bfloat16)
+    _dev(k, "k", torch.bfloat16, (T, H_kv, D))
+    _dev(v, "v", torch.bfloat16, (T, H_kv, D))
+    _dev(q_rot, "q_rot", torch.bfloat16, (T, H_q, D))
+    _dev(positions, "positions", torch.int32, min_numel=T)
+    _dev(slot_mapping, "slot_mapping", torch.int32, min_numel=T)
+    if cos_tab.dim() != 2:
+        raise ValueError("cos_tab must be [max_pos, D/2]")
+    _dev(cos_tab, "cos_tab", torch.float32, (cos_tab.shape[0], D // 2))
+    _dev(sin_tab, "sin_tab", torch.float32, cos_tab.shape)
+    _pools(k_cache, v_cache, H_kv, D)
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape[0] < 1:
+        raise ValueError("cu_seqlens_q must be 1-D with rows + 1 entries")
+    S = cu_seqlens_q.shape[0] - 1
+    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _dev(q_start_pos, "q_start_pos", torch.int32, min_numel=S)
+    _dev(context_lens, "context_lens", torch.int32, min_numel=S)
+    if bt_offsets is None:
+        stride = block_tables.shape[1] if block_tables.dim() == 2 else block_tables.shape[0] // max(S, 1)
+        _dev(block_tables, "block_tables", torch.int32, min_numel=S * stride)
+        bt_len = 0
+    else:
+        _dev(bt_offsets, "bt_offsets", torch.int32, min_numel=S + 1)
+        _dev(block_tables, "block_tables", torch.int32, min_numel=1)
+        stride, bt_len = 0, block_tables.numel()
+    _dev(out, "out", torch.bfloat16, (T, H_q, D))
+    _dev(workspace, "workspace", None)
+    if dev_status is not None:
+        _dev(dev_status, "dev_status", torch.int32, min_numel=1)
+    _on_one_gpu("q k v q_rot positions slot_mapping cos_tab sin_tab k_cache v_cache cu_seqlens_q q_start_pos "
+                "context_lens block_tables bt_offsets out workspace dev_status", q, k, v, q_rot, positions,
+                slot_mapping, cos_tab, sin_tab, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens,
+                block_tables, bt_offsets, out, workspace, dev_status)
+    if scale is None:
+        scale = float(D) ** -0.5
+    rc = lib().ms_mixed_step(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(slot_mapping), _ptr(cos_tab),
+                             _ptr(sin_tab), cos_tab.shape[0], _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                             _ptr(q_rot), _ptr(cu_seqlens_q), _ptr(q_start_pos), _ptr(context_lens),
+                             _ptr(block_tables), _ptr(bt_offsets), bt_len, stride, S, T, int(context_total), H_q,
+                             H_kv, D, PAGE_SIZE, float(scale), _ptr(out), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
+    _check(rc, "ms_mixed_step")
 
 
 def mixed_step_attention_noalloc(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables,

@@ -28,12 +28,12 @@
 //     rescaled only when a row's maximum grows by more than a factor 2^8.
 //
 // A one-CTA prologue validates the metadata, chooses the split size, orders
-// rows longest-first and decides how many CTAs start on chunk tiles; a second
-// small kernel expands the per-row item counts into flat item tables.  One
-// persistent kernel (a CTA per SM) then runs both queues: CTAs on SMs below the
-// split start on chunk tiles, the rest on decode items, and each moves to the other
-// queue when its own runs dry.  Work comes from atomic counters; no CTA waits
-// on another.
+// rows longest-first, expands the per-row item counts into flat item tables
+// and decides how many CTAs start on chunk tiles.  One persistent kernel (a
+// CTA per SM) then runs both queues: CTAs on SMs below the split start on
+// chunk tiles, the rest on decode items, and each moves to the other queue
+// when its own runs dry.  Work comes from atomic counters; no CTA waits on
+// another.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,6 +44,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "append_rope.cuh"
 #include "mixed_step.h"
 #include "ptx.cuh"
 
@@ -57,7 +58,6 @@ constexpr int kMinSplitPages = 32;
 constexpr int kMaxSplitPages = 256;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kChunkThreads = 32 * (4 + kSoftmaxWarps);  // warp 0 TMA + queue, 2-9 softmax, 1/10/11 MMA
-constexpr int kPrologueThreads = 1024;
 constexpr int kSortLimit = 2048;    // rows sorted longest-first up to this count
 constexpr int kMaxRows = 8192;      // rows of one step
 // Cost model that splits the SMs between the two row kinds at the start of a
@@ -95,15 +95,13 @@ struct AttnParams {
   bf16* out;
   int32_t* hdr;
   int32_t* dec_rows;
-  int32_t* dec_item_prefix;
   int32_t* dec_part_base;
   int32_t* dec_nsplit;
   int32_t* ch_rows;
-  int32_t* ch_item_prefix;
-  int2* dec_items;  // per decode item: (decode row index, item within the row)
+  int2* dec_items;  // per decode split (items / H_kv entries): (decode row index, split within the row)
   int32_t* dec_cnt; // per (decode row, KV head): splits finished, for the last one to merge
-  int2* ch_items;   // per chunk item: (chunk row index, item within the row)
-  int64_t max_dec_items, max_ch_items;
+  int2* ch_items;   // per Q-tile pair of a chunk row (items / H_kv entries): (chunk row index, pair index)
+  int64_t max_dec_items, max_ch_items;  // capacities in items (entries x H_kv)
   float* part_ml;
   float* part_acc;
   int64_t max_partials;
@@ -115,6 +113,9 @@ struct AttnParams {
   int32_t clear_status;  // the prologue zeroes the status word first (scratch owned by the library)
   int32_t test_stall;    // test hook: chunk-phase producers publish no work item (0 in every real call)
   uint64_t wait_limit_ns;  // bound of every chunk-phase wait
+  float chunk_tile_ns;     // cost model of the SM split: ns per 128x128 chunk tile on one SM,
+  float decode_sm_gbs;     // decode GB/s of one SM at G = 1,
+  float hbm_gbs;           // and the HBM bandwidth that caps decode
   float scale_log2;
 };
 
@@ -127,62 +128,42 @@ __device__ __forceinline__ const int32_t* row_table(const AttnParams& p, int row
 }
 
 // ----------------------------------------------------------------------------
-// prologue: validate, classify, sort longest-first, lay out work lists
+// prologue: validate, classify, order longest-first, lay out the work lists
 // ----------------------------------------------------------------------------
 
-// exclusive scan of one int64 per thread over the block; returns the total
-__device__ int64_t block_exclusive_scan(int64_t v, int64_t* s_warp, int64_t& total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int64_t x = v;
+// Exclusive scan of one int per thread over the block (blockDim.x a multiple
+// of 32); returns the thread's prefix and sets `total`.  Each thread adds up
+// the warp totals ahead of its own warp, so a scan costs two barriers.
+__device__ __forceinline__ int block_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) s_warp[w] = x;
   __syncthreads();
-  if (w == 0) {
-    int64_t t = lane < (blockDim.x >> 5) ? s_warp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    s_warp[lane] = t;  // inclusive warp prefix
+  int before = 0, tot = 0;
+  for (int j = 0; j < nw; ++j) {
+    const int t = s_warp[j];
+    before += j < w ? t : 0;
+    tot += t;
   }
-  __syncthreads();
-  const int64_t before = (w > 0 ? s_warp[w - 1] : 0) + x - v;
-  total = s_warp[(blockDim.x >> 5) - 1];
-  __syncthreads();
-  return before;
+  __syncthreads();  // s_warp is free again
+  total = tot;
+  return before + x - v;
 }
 
-// Shared memory of the prologue: sort keys and per-row values of up to
-// kSortLimit rows, and the item prefix of up to kMaxRows rows.
-struct PrologueSmem {
-  int64_t key[kSortLimit];
-  int32_t id[kSortLimit];
-  int32_t d[kSortLimit];
-  int32_t c[kSortLimit];
-  int32_t pref[kMaxRows + 1];
-};
-
-// k with pref[k] <= item < pref[k + 1] (pref has n + 1 entries, in shared memory)
-__device__ __forceinline__ int find_in_prefix(const int32_t* pref, int n, int item) {
-  int lo = 0, hi = n;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (pref[mid] <= item)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  return lo;
+__device__ __forceinline__ int64_t warp_sum64(int64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
 }
 
 // Work items of one row: decode splits of `split` pages, or pairs of 128-row Q tiles.
-__device__ __forceinline__ int row_items(int kind, int c, int d, int tpt, unsigned split) {
-  if (kind == 0) return static_cast<int>((static_cast<unsigned>(c + kPage) / kPage + split - 1) / split);
+__device__ __forceinline__ int row_items(bool chunk, int c, int d, int tpt, unsigned split) {
+  if (!chunk) return static_cast<int>((static_cast<unsigned>(c + kPage) / kPage + split - 1) / split);
   const int n_qt = (d + tpt - 1) / tpt;
   return (n_qt + 1) >> 1;
 }
@@ -195,262 +176,410 @@ __device__ __forceinline__ unsigned chunk_tiles(int c, int d, int tpt) {
   return tiles;
 }
 
-// One CTA: validate the rows, split them into decode rows (d = 1) and chunk
-// rows (d > 1), order each list longest-first, size the decode splits, lay
-// out the per-item tables, zero the split counters and pick how many CTAs of
-// the main kernel start on chunk work.  Every row's values are read from
-// global memory once; the rest happens in registers and shared memory.
-//
-// Launched as a programmatic dependent of the kernel before it on the stream
-// (normally the append), it reads only the row metadata, which is complete
-// before that kernel starts, and runs alongside it; before it exits it waits
-// for that kernel, so the kernels after it see the append's writes.
-__global__ void __launch_bounds__(kPrologueThreads, 1) prologue_kernel(AttnParams p) {
-  extern __shared__ __align__(16) uint8_t psm_raw[];
-  PrologueSmem& sm = *reinterpret_cast<PrologueSmem*>(psm_raw);
-  __shared__ int64_t s_warp[32];
-  __shared__ int s_bad;
-  __shared__ unsigned long long s_ctx_sum, s_dec_pages, s_tiles;
-  constexpr int R = kMaxRows / kPrologueThreads;
-  const int tid = threadIdx.x;
-  const int S = p.num_rows;
-  int32_t* hdr = p.hdr;
-  griddep_launch_dependents();
-  if (tid == 0) {
-    s_tiles = 0;
-    // a library-owned scratch keeps the previous call's status: start this call at zero
-    // (before the first __syncthreads, so ahead of every status write of this call)
-    if (p.clear_status) hdr[H_STATUS] = 0;
+// Sort key of the row at position `pos` of its list: the top 19 bits of the
+// row's cost as a float (keys to read for a decode, query-key pairs for a
+// chunk), then the position reversed.  Keys are unique and nonzero (cost >= 1);
+// a larger key means more work or, at about equal cost, an earlier row.
+__device__ __forceinline__ uint32_t order_key(float cost, int pos) {
+  return ((__float_as_uint(cost) >> 13) << 13) | static_cast<uint32_t>(kMaxRows - 1 - pos);
+}
+
+// 32-bit words of the prologue's dynamic shared memory for S rows: sort keys
+// (both lists, each padded to 4), list order, each row's d and c, and the item
+// prefix in queue order.
+__host__ __device__ constexpr int prologue_words(int S) { return 5 * ((S + 3) & ~3) + 16; }
+
+// How many CTAs of the main kernel start on chunk tiles.  Chunk time falls as
+// 1/n with n chunk CTAs, in whole items; decode time is bytes over the
+// bandwidth of the other SMs, capped by HBM.  Take the best split near the
+// balance point, or, while decode stays HBM-bound, as many chunk CTAs as keep
+// it so.  Called by one whole warp; the candidate counts go one per lane.
+__device__ int chunk_cta_split(const AttnParams& p, float tiles, float dec_pages, int n_items, int lane) {
+  const float S = static_cast<float>(p.num_sms);
+  const float T = tiles * p.chunk_tile_ns;                                    // SM-ns of chunk work
+  const float B = dec_pages * p.H_kv * kPage * p.D * 4.f;                     // decode bytes
+  const float g = p.decode_sm_gbs / (1.f + 0.18f * (p.G - 1));                // GB/s per decode SM
+  const float n_hbm = fmaxf(0.f, floorf(S - p.hbm_gbs / g));  // most chunk CTAs with decode at HBM rate
+  if (T == 0.f) return static_cast<int>(B == 0.f ? S : n_hbm);
+  if (B == 0.f) return static_cast<int>(S);
+  if (T * p.hbm_gbs <= B * n_hbm) return static_cast<int>(n_hbm);  // chunk done within the HBM-bound decode time
+  // Balance point, then the nearby CTA count that minimizes the step: chunk work
+  // comes in whole items, so n chunk CTAs need ceil(items / n) rounds of about
+  // T / items each; decode runs on the other CTAs, capped by HBM.  Ties go to
+  // the smallest count.
+  const float n0 = fminf(S - 1.f, fmaxf(1.f, rintf(__fdividef(T * g * S, B + T * g))));
+  const int n_it = max(n_items, 1);
+  const float t_item = __fdividef(T, static_cast<float>(n_it));
+  const int k_lo = max(1, static_cast<int>(n0) - 16), k_hi = min(static_cast<int>(S) - 1, static_cast<int>(n0) + 16);
+  float best = 3.0e38f;
+  int bk = static_cast<int>(n0);
+  for (int k = k_lo + lane; k <= k_hi; k += 32) {
+    const float tc = static_cast<float>((n_it + k - 1) / k) * t_item;
+    const float td = __fdividef(B, fminf((S - k) * g, p.hbm_gbs));
+    const float tt = fmaxf(tc, td);
+    if (tt < best) {
+      best = tt;
+      bk = k;
+    }
   }
-  // 1. this thread's rows s = tid + i * 1024: load, validate, count (block sums, no atomics)
-  int rd[R], rc[R];
-  int64_t my_ctx = 0, my_pages = 0;
-  int my_bad = S > kMaxRows;
 #pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int s = tid + i * kPrologueThreads;
-    rd[i] = 0;
-    rc[i] = 0;
-    if (s < S && S <= kMaxRows) {
-      const int32_t a = p.cu[s], b = p.cu[s + 1];
-      const int32_t d = b - a, c = p.q_start[s], ctx = p.ctx_lens[s];
-      // d == 0 is a pad row: valid, and neither a decode nor a chunk
-      bool ok = a >= 0 && b <= p.num_tokens && d >= 0 && c >= 0 && ctx == c + d;
-      if (p.bt_off != nullptr) {  // the row's pages must lie inside the table
-        const int64_t o0 = p.bt_off[s], o1 = p.bt_off[s + 1];
-        ok = ok && o0 >= 0 && o1 <= p.bt_len && cdiv64(ctx, kPage) <= o1 - o0;
-      } else {
-        ok = ok && cdiv64(ctx, kPage) <= p.bt_stride;
-      }
-      if (ok) {
-        rd[i] = d;
-        rc[i] = c;
-        my_ctx += ctx;
-        if (d == 1) my_pages += (ctx + kPage - 1) / kPage;
-      } else {
-        my_bad = 1;
-      }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int ok = __shfl_xor_sync(0xffffffffu, bk, o);
+    if (ob < best || (ob == best && ok < bk)) {
+      best = ob;
+      bk = ok;
     }
   }
-  {
-    int64_t tot;
-    block_exclusive_scan(my_ctx, s_warp, tot);
-    if (tid == 0) s_ctx_sum = static_cast<unsigned long long>(tot);
-    block_exclusive_scan(my_pages, s_warp, tot);
-    if (tid == 0) s_dec_pages = static_cast<unsigned long long>(tot);
-    block_exclusive_scan(my_bad, s_warp, tot);
-    if (tid == 0) s_bad = tot != 0;
-    __syncthreads();
-  }
-  if (s_bad != 0 || static_cast<int64_t>(s_ctx_sum) > p.context_total) {
-    if (tid == 0) {
-      atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
-      hdr[H_DEC_CTR] = hdr[H_CH_CTR] = 0;
-      hdr[H_NDEC] = hdr[H_NDEC_ITEMS] = hdr[H_NCH] = hdr[H_NCH_ITEMS] = hdr[H_NPART] = 0;
-      hdr[H_SPLIT] = kMinSplitPages;
-      hdr[H_CHUNK_CTAS] = 0;
-      p.dec_item_prefix[0] = 0;
-      p.ch_item_prefix[0] = 0;
-    }
-    griddep_wait();
-    return;
-  }
-  // 2. decode split size: about 8 items per decode worker warp, clamped; at least
-  // 32 pages (64 when G >= 4, whose items carry G heads of partials to merge)
-  int64_t split = cdiv64(static_cast<int64_t>(s_dec_pages) * p.H_kv, static_cast<int64_t>(p.dec_workers) * 8);
+  return bk;
+}
+
+// Decode split size: about 8 items per decode worker warp, clamped; at least 32
+// pages (64 when G >= 4, whose items carry G heads of partials to merge).
+__device__ __forceinline__ int decode_split(const AttnParams& p, int64_t dec_pages) {
+  const int64_t num = dec_pages * p.H_kv, den = static_cast<int64_t>(p.dec_workers) * 8;
+  int64_t split = num + den <= 0xffffffffll
+                      ? static_cast<int64_t>(static_cast<uint32_t>(num + den - 1) / static_cast<uint32_t>(den))
+                      : cdiv64(num, den);
   const int64_t min_split = p.G >= 4 ? 2 * kMinSplitPages : kMinSplitPages;
   split = split < min_split ? min_split : (split > kMaxSplitPages ? kMaxSplitPages : split);
+  return static_cast<int>(split);
+}
+
+// Header of a call whose metadata failed validation: status set, no work.
+__device__ __forceinline__ void header_bad_meta(int32_t* hdr) {
+  atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
+  hdr[H_DEC_CTR] = hdr[H_CH_CTR] = 0;
+  hdr[H_NDEC] = hdr[H_NDEC_ITEMS] = hdr[H_NCH] = hdr[H_NCH_ITEMS] = hdr[H_NPART] = 0;
+  hdr[H_SPLIT] = kMinSplitPages;
+  hdr[H_CHUNK_CTAS] = 0;
+}
+
+// The prologue of a step of at most 32 rows: one warp, a row per lane, with
+// ballots and shuffles in place of shared memory and barriers.  Same outputs
+// as the block version below.
+__device__ __forceinline__ void prologue_warp(const AttnParams& p) {
+  const int lane = threadIdx.x, S = p.num_rows;
+  int32_t* hdr = p.hdr;
+  int d = 0, c = 0, ctx = 0;
+  bool ok = true;
+  if (lane < S) {
+    const int32_t a = p.cu[lane], b = p.cu[lane + 1];
+    d = b - a;
+    c = p.q_start[lane];
+    ctx = p.ctx_lens[lane];
+    ok = a >= 0 && b <= p.num_tokens && d >= 0 && c >= 0 && ctx == c + d;
+    if (p.bt_off != nullptr) {
+      const int64_t o0 = p.bt_off[lane], o1 = p.bt_off[lane + 1];
+      ok = ok && o0 >= 0 && o1 <= p.bt_len && cdiv64(ctx, kPage) <= o1 - o0;
+    } else {
+      ok = ok && cdiv64(ctx, kPage) <= p.bt_stride;
+    }
+    if (!ok) d = ctx = 0;
+  }
+  const bool bad = __any_sync(0xffffffffu, !ok);
+  const int64_t ctx_sum = warp_sum64(ctx);
+  if (bad || ctx_sum > p.context_total) {
+    if (lane == 0) header_bad_meta(hdr);
+    return;
+  }
+  const bool is_dec = d == 1, is_ch = d > 1;
+  const int64_t dec_pages = warp_sum64(is_dec ? (ctx + kPage - 1) / kPage : 0);
+  const int split = decode_split(p, dec_pages);
   const int tpt = 128 / p.G;
-  const unsigned split32 = static_cast<unsigned>(split);
-  // 3. the two row lists, each in input order first
-  int dpos[R], cpos[R];
-  int64_t n_dec = 0, n_ch = 0;
+  const unsigned bd = __ballot_sync(0xffffffffu, is_dec), bc = __ballot_sync(0xffffffffu, is_ch);
+  const int n_dec = __popc(bd), n_ch = __popc(bc);
+  // position in its list, then rank by key within the list (longest first):
+  // the keys sit in shared memory by list position, zero-padded, read 16 bytes at a time
+  __shared__ __align__(16) uint32_t s_key[2][32];
+  __shared__ int s_items[32], s_pref[32];
+  const bool listed = is_dec || is_ch;
+  const unsigned list = is_ch ? bc : bd;
+  const int pos = __popc(list & ((1u << lane) - 1u));
+  const uint32_t key = order_key(is_ch ? 0.5f * d * (2.f * c + d + 1.f) : c + 1.f, pos);
+  s_key[0][lane] = 0;
+  s_key[1][lane] = 0;
+  s_items[lane] = 0;
+  __syncwarp();
+  if (listed) s_key[is_ch][pos] = key;
+  __syncwarp();
+  int rank = 0;
+  const uint4* k4 = reinterpret_cast<const uint4*>(s_key[is_ch]);
 #pragma unroll
-  for (int i = 0; i < R; ++i) {
-    dpos[i] = -1;
-    cpos[i] = -1;
-    if (i * kPrologueThreads < S) {  // uniform
-      const int is_dec = rd[i] == 1, is_ch = rd[i] > 1;
-      int64_t tot_dec, tot_ch;
-      const int64_t o_dec = block_exclusive_scan(is_dec, s_warp, tot_dec);
-      const int64_t o_ch = block_exclusive_scan(is_ch, s_warp, tot_ch);
-      dpos[i] = is_dec ? static_cast<int>(n_dec + o_dec) : -1;
-      cpos[i] = is_ch ? static_cast<int>(n_ch + o_ch) : -1;
-      n_dec += tot_dec;
-      n_ch += tot_ch;
+  for (int m = 0; m < 8; ++m) {
+    const uint4 v = k4[m];
+    rank += (v.x > key) + (v.y > key) + (v.z > key) + (v.w > key);
+  }
+  const int items = listed ? row_items(is_ch, c, d, tpt, static_cast<unsigned>(split)) : 0;
+  const int q = (is_ch ? n_dec : 0) + rank;  // queue position
+  if (listed) s_items[q] = items;
+  __syncwarp();
+  {  // exclusive prefix over queue positions, one per lane
+    const int v = s_items[lane];
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    s_pref[lane] = x - v;
+  }
+  __syncwarp();
+  const int before = listed ? s_pref[q] : 0;  // items of the rows ahead in queue order
+  const int dec_tot = __reduce_add_sync(0xffffffffu, is_dec ? items : 0);
+  const int ch_tot = __reduce_add_sync(0xffffffffu, is_ch ? items : 0);
+  const int64_t n_dec_items = static_cast<int64_t>(dec_tot) * p.H_kv;
+  const int64_t n_ch_items = static_cast<int64_t>(ch_tot) * p.H_kv;
+  const bool dec_over = n_dec_items > p.max_dec_items || static_cast<int64_t>(dec_tot) * p.H_q > p.max_partials;
+  const bool ch_over = n_ch_items > p.max_ch_items;
+  const int64_t tiles = warp_sum64(is_ch ? static_cast<int64_t>(chunk_tiles(c, d, tpt)) * p.H_kv : 0);
+  if (is_dec) {
+    p.dec_rows[rank] = lane;
+    p.dec_part_base[rank] = static_cast<int32_t>(static_cast<int64_t>(before) * p.H_q);
+    p.dec_nsplit[rank] = items;
+    if (!dec_over) {
+      for (int i = 0; i < items; ++i) p.dec_items[before + i] = make_int2(rank, i);
+      for (int h = 0; h < p.H_kv; ++h) p.dec_cnt[rank * p.H_kv + h] = 0;
     }
   }
-  // 4. each list longest first (stable), then item counts in queue order
-  for (int kind = 0; kind < 2; ++kind) {
-    const int n = static_cast<int>(kind == 0 ? n_dec : n_ch);
-    int32_t* rows = kind == 0 ? p.dec_rows : p.ch_rows;
-    const bool sorted = n <= kSortLimit;
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const int s = tid + i * kPrologueThreads;
-      const int pos = kind == 0 ? dpos[i] : cpos[i];
-      if (s >= S || pos < 0) continue;
-      const int c = rc[i], d = rd[i];
-      if (sorted) {
-        const int64_t cost = kind == 0 ? c + 1 : static_cast<int64_t>(d) * (2ll * c + d + 1) / 2;
-        sm.key[pos] = (cost << 16) | (0xffff - (pos & 0xffff));  // ties keep input order
-        sm.id[pos] = s;
-        sm.d[pos] = static_cast<int32_t>(d);
-        sm.c[pos] = static_cast<int32_t>(c);
-      } else {
-        rows[pos] = s;
-        sm.pref[pos] = row_items(kind, c, d, tpt, split32);
-        if (kind == 1) atomicAdd(&s_tiles, static_cast<unsigned long long>(chunk_tiles(c, d, tpt)) * p.H_kv);
-      }
-    }
-    __syncthreads();
-    if (sorted) {
-      for (int j = tid; j < n; j += kPrologueThreads) {
-        const int64_t k = sm.key[j];
-        int rank = 0;
-        for (int m = 0; m < n; ++m) rank += sm.key[m] > k;
-        rows[rank] = sm.id[j];
-        const int c = sm.c[j], d = sm.d[j];
-        sm.pref[rank] = row_items(kind, c, d, tpt, split32);
-        if (kind == 1) atomicAdd(&s_tiles, static_cast<unsigned long long>(chunk_tiles(c, d, tpt)) * p.H_kv);
-      }
-      __syncthreads();
-    }
-    // 5. exclusive prefix of the per-row item counts (times H_kv) in queue order
-    int64_t run = 0;
-    for (int base = 0; base < n; base += kPrologueThreads) {
-      const int k = base + tid;
-      const int64_t v = k < n ? sm.pref[k] : 0;
-      int64_t tot;
-      const int64_t o = block_exclusive_scan(v, s_warp, tot);
-      if (k < n) {
-        const int64_t first = (run + o) * p.H_kv;
-        sm.pref[k] = static_cast<int32_t>(first);
-        if (kind == 0) {
-          p.dec_item_prefix[k] = static_cast<int32_t>(first);
-          p.dec_part_base[k] = static_cast<int32_t>((run + o) * p.H_q);
-          p.dec_nsplit[k] = static_cast<int32_t>(v);
-        } else {
-          p.ch_item_prefix[k] = static_cast<int32_t>(first);
-        }
-      }
-      run += tot;
-    }
-    const int64_t n_items = run * p.H_kv;
-    const int64_t cap = kind == 0 ? p.max_dec_items : p.max_ch_items;
-    const bool overflow = n_items > cap || (kind == 0 && run * p.H_q > p.max_partials);
-    if (tid == 0) {
-      sm.pref[n] = static_cast<int32_t>(n_items);
-      if (kind == 0) {
-        p.dec_item_prefix[n] = static_cast<int32_t>(n_items);
-        hdr[H_NDEC] = overflow ? 0 : static_cast<int32_t>(n_dec);
-        hdr[H_NDEC_ITEMS] = overflow ? 0 : static_cast<int32_t>(n_items);
-        hdr[H_NPART] = static_cast<int32_t>(run * p.H_q);
-      } else {
-        p.ch_item_prefix[n] = static_cast<int32_t>(n_items);
-        hdr[H_NCH] = overflow ? 0 : static_cast<int32_t>(n_ch);
-        hdr[H_NCH_ITEMS] = overflow ? 0 : static_cast<int32_t>(n_items);
-      }
-      if (overflow) atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
-    }
-    __syncthreads();
-    __syncthreads();
+  if (is_ch) {
+    p.ch_rows[rank] = lane;
+    if (!ch_over)
+      for (int i = 0; i < items; ++i) p.ch_items[before - dec_tot + i] = make_int2(rank, i);
   }
-  if (tid == 0) {
+  const int n_first = chunk_cta_split(p, static_cast<float>(tiles), static_cast<float>(dec_pages),
+                                      ch_over ? 0 : static_cast<int>(n_ch_items), lane);
+  if (lane == 0) {
+    hdr[H_NDEC] = dec_over ? 0 : n_dec;
+    hdr[H_NDEC_ITEMS] = dec_over ? 0 : static_cast<int32_t>(n_dec_items);
+    hdr[H_NPART] = static_cast<int32_t>(static_cast<int64_t>(dec_tot) * p.H_q);
+    hdr[H_NCH] = ch_over ? 0 : n_ch;
+    hdr[H_NCH_ITEMS] = ch_over ? 0 : static_cast<int32_t>(n_ch_items);
+    if (dec_over || ch_over) atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
     hdr[H_DEC_CTR] = 0;
     hdr[H_CH_CTR] = 0;
-    hdr[H_SPLIT] = static_cast<int32_t>(split);
+    hdr[H_SPLIT] = split;
+    hdr[H_CHUNK_CTAS] = n_first;
   }
-  // 7. starting split of the SMs between chunk tiles and decode pages.  Chunk
-  // time falls as 1/n with n chunk CTAs, in whole items; decode time is bytes
-  // over the bandwidth of the other SMs, capped by HBM.  Take the best split
-  // near the balance point, or, while decode stays HBM-bound, as many chunk
-  // CTAs as keep it so.
-  if (tid == 0) {
-    const float S = static_cast<float>(p.num_sms);
-    const float T = static_cast<float>(s_tiles) * kChunkTileNs;                     // SM-ns of chunk work
-    const float B = static_cast<float>(s_dec_pages) * p.H_kv * kPage * p.D * 4.f;  // decode bytes
-    const float g = kDecodeSmGBs / (1.f + 0.18f * (p.G - 1));                      // GB/s per decode SM
-    const float n_hbm = fmaxf(0.f, floorf(S - kHbmGBs / g));  // most chunk CTAs with decode at HBM rate
-    float n;
-    if (T == 0.f)
-      n = B == 0.f ? S : n_hbm;
-    else if (B == 0.f)
-      n = S;
-    else if (T * kHbmGBs <= B * n_hbm)  // chunk done within the HBM-bound decode time
-      n = n_hbm;
-    else {
-      // Balance point, then the nearby CTA count that minimizes the step: chunk work
-      // comes in whole items, so n chunk CTAs need ceil(items / n) rounds of about
-      // T / items each; decode runs on the other CTAs, capped by HBM.
-      const float n0 = fminf(S - 1.f, fmaxf(1.f, rintf(__fdividef(T * g * S, B + T * g))));
-      const float n_it = fmaxf(static_cast<float>(hdr[H_NCH_ITEMS]), 1.f);
-      const float t_item = T / n_it;
-      float best = 3.0e38f;
-      n = n0;
-      const int k_lo = max(1, static_cast<int>(n0) - 16), k_hi = min(static_cast<int>(S) - 1, static_cast<int>(n0) + 16);
-      for (int k = k_lo; k <= k_hi; ++k) {
-        const float tc = ceilf(n_it / k) * t_item;
-        const float td = B / fminf((S - k) * g, kHbmGBs);
-        const float tt = fmaxf(tc, td);
-        if (tt < best) {
-          best = tt;
-          n = static_cast<float>(k);
-        }
+}
+
+// The prologue on one CTA of blockDim.x threads (a multiple of 32, at most
+// 1024; warp 0 alone up to 32 rows): validate the rows, split them into decode rows (d = 1)
+// and chunk rows (d > 1), order each list longest-first, size the decode
+// splits, write the flat item tables (item -> row in queue order, item within
+// the row), zero the split counters and pick how many CTAs of the main kernel
+// start on chunk work.  Every row's values are read from global memory once;
+// the rest happens in shared memory (prologue_words(S) words of dynamic shared
+// memory).  It runs once per step from a cold instruction cache, so its loops
+// stay rolled and its code short.  It reads only the row metadata, never the
+// appended K/V, so it may run alongside the append.
+__device__ __forceinline__ void prologue_body(const AttnParams& p) {
+  extern __shared__ __align__(16) int32_t psm[];
+  __shared__ int s_warp[32];
+  __shared__ long long s_sum[2][32];
+  __shared__ unsigned s_cnt[2][32];
+  __shared__ unsigned long long s_tiles;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  const int S = p.num_rows;  // at most kMaxRows (checked by the host, which sizes psm by it)
+  int32_t* hdr = p.hdr;
+  const int Sp = (S + 3) & ~3;
+  uint32_t* key = reinterpret_cast<uint32_t*>(psm);  // Sp + 8 words
+  int32_t* lst = psm + Sp + 8;                       // list order: decode rows, then chunk rows
+  int32_t* rd = lst + Sp;                            // per row (input order): d (0 for pad rows), c
+  int32_t* rc = rd + Sp;
+  int32_t* pref = rc + Sp;                           // per queue position: items, then their prefix
+  // a library-owned scratch keeps the previous call's status: start this call at zero
+  // (ahead of every status write of this call, all of which come after a barrier or from this thread)
+  if (tid == 0 && p.clear_status) hdr[H_STATUS] = 0;
+  if (S <= 32) {
+    if (warp == 0) prologue_warp(p);
+    return;
+  }
+  if (tid == 0) s_tiles = 0;
+  // 1. load and validate the rows; count decodes, chunks, context and decode pages
+  int64_t my_ctx = 0, my_pages = 0;
+  unsigned my_dec = 0, my_ch = 0;
+  int my_bad = 0;
+  for (int s = tid; s < S; s += nt) {
+    const int32_t a = p.cu[s], b = p.cu[s + 1];
+    const int32_t d = b - a, c = p.q_start[s], ctx = p.ctx_lens[s];
+    // d == 0 is a pad row: valid, and neither a decode nor a chunk
+    bool ok = a >= 0 && b <= p.num_tokens && d >= 0 && c >= 0 && ctx == c + d;
+    if (p.bt_off != nullptr) {  // the row's pages must lie inside the table
+      const int64_t o0 = p.bt_off[s], o1 = p.bt_off[s + 1];
+      ok = ok && o0 >= 0 && o1 <= p.bt_len && cdiv64(ctx, kPage) <= o1 - o0;
+    } else {
+      ok = ok && cdiv64(ctx, kPage) <= p.bt_stride;
+    }
+    my_bad |= !ok;
+    rd[s] = ok ? d : 0;
+    rc[s] = c;
+    if (ok) {
+      my_ctx += ctx;
+      my_dec += d == 1;
+      my_ch += d > 1;
+      if (d == 1) my_pages += (ctx + kPage - 1) / kPage;
+    }
+  }
+  my_ctx = warp_sum64(my_ctx);
+  my_pages = warp_sum64(my_pages);
+  my_dec = __reduce_add_sync(0xffffffffu, my_dec);
+  my_ch = __reduce_add_sync(0xffffffffu, my_ch);
+  if (lane == 0) {
+    s_sum[0][warp] = my_ctx;
+    s_sum[1][warp] = my_pages;
+    s_cnt[0][warp] = my_dec;
+    s_cnt[1][warp] = my_ch;
+  }
+  const int bad = __syncthreads_or(my_bad);
+  int64_t ctx_sum = 0, dec_pages = 0;
+  int n_dec = 0, n_ch = 0;
+  for (int j = 0; j < nw; ++j) {
+    ctx_sum += s_sum[0][j];
+    dec_pages += s_sum[1][j];
+    n_dec += static_cast<int>(s_cnt[0][j]);
+    n_ch += static_cast<int>(s_cnt[1][j]);
+  }
+  if (bad || ctx_sum > p.context_total) {
+    if (tid == 0) header_bad_meta(hdr);
+    return;
+  }
+  // 2. decode split size
+  const int split = decode_split(p, dec_pages);
+  const int tpt = 128 / p.G;
+  const unsigned split32 = static_cast<unsigned>(split);
+  // 3. the two lists in input order: decode rows at lst[0, n_dec), chunk rows after them
+  const int n_tot = n_dec + n_ch;
+  {
+    int o_dec = 0, o_ch = 0;
+    for (int base = 0; base < S; base += nt) {  // uniform
+      const int s = base + tid;  // the row this thread loaded
+      const int d = s < S ? rd[s] : 0;
+      int tot;
+      const int o = block_scan((d == 1) | ((d > 1) << 16), s_warp, tot);  // both counts, 16 bits each
+      if (d == 1) lst[o_dec + (o & 0xffff)] = s;
+      if (d > 1) lst[n_dec + o_ch + (o >> 16)] = s;
+      o_dec += tot & 0xffff;
+      o_ch += tot >> 16;
+    }
+  }
+  // 4. sort keys, each list from a 16-byte boundary, padded with zero keys
+  const int ch_base = (n_dec + 3) & ~3;
+  if (tid < 4) {
+    if (n_dec + tid < ch_base) key[n_dec + tid] = 0;
+    if (n_ch + tid < ((n_ch + 3) & ~3)) key[ch_base + n_ch + tid] = 0;
+  }
+  __syncthreads();
+  for (int j = tid; j < n_tot; j += nt) {
+    const bool ch = j >= n_dec;
+    const int pos = ch ? j - n_dec : j, row = lst[j];
+    const float d = static_cast<float>(rd[row]), c = static_cast<float>(rc[row]);
+    key[(ch ? ch_base : 0) + pos] = order_key(ch ? 0.5f * d * (2.f * c + d + 1.f) : c + 1.f, pos);
+  }
+  __syncthreads();
+  // 5. each list longest first: a row's rank is the number of larger keys in its
+  // list (lists longer than kSortLimit keep input order); rows in queue order,
+  // and each row's item count at its queue position
+  for (int j = tid; j < n_tot; j += nt) {
+    const bool ch = j >= n_dec;
+    const int pos = ch ? j - n_dec : j, n = ch ? n_ch : n_dec;
+    int rank = pos;
+    if (n <= kSortLimit) {
+      const uint32_t* kl = key + (ch ? ch_base : 0);
+      const uint32_t mine = kl[pos];
+      const uint4* k4 = reinterpret_cast<const uint4*>(kl);
+      rank = 0;
+      for (int m = 0; m < (n + 3) >> 2; ++m) {
+        const uint4 v = k4[m];
+        rank += (v.x > mine) + (v.y > mine) + (v.z > mine) + (v.w > mine);
       }
     }
-    hdr[H_CHUNK_CTAS] = static_cast<int>(n);
+    const int row = lst[j], c = rc[row], d = rd[row];
+    (ch ? p.ch_rows : p.dec_rows)[rank] = row;
+    pref[(ch ? n_dec : 0) + rank] = row_items(ch, c, d, tpt, split32);
+    if (ch) atomicAdd(&s_tiles, static_cast<unsigned long long>(chunk_tiles(c, d, tpt)) * p.H_kv);
   }
+  __syncthreads();
+  // 6. exclusive prefix of the item counts in queue order (decode rows, then chunk rows)
+  int run = 0;
+  for (int base = 0; base < n_tot; base += nt) {  // uniform
+    const int q = base + tid;
+    const int v = q < n_tot ? pref[q] : 0;
+    int tot;
+    const int o = block_scan(v, s_warp, tot);
+    if (q < n_tot) {
+      pref[q] = run + o;
+      if (q < n_dec) {
+        p.dec_part_base[q] = static_cast<int32_t>(static_cast<int64_t>(run + o) * p.H_q);
+        p.dec_nsplit[q] = v;
+      }
+    }
+    run += tot;
+  }
+  if (tid == 0) pref[n_tot] = run;
+  __syncthreads();
+  const int dec_tot = pref[n_dec], ch_tot = run - dec_tot;
+  const int64_t n_dec_items = static_cast<int64_t>(dec_tot) * p.H_kv;
+  const int64_t n_ch_items = static_cast<int64_t>(ch_tot) * p.H_kv;
+  const bool dec_over = n_dec_items > p.max_dec_items || static_cast<int64_t>(dec_tot) * p.H_q > p.max_partials;
+  const bool ch_over = n_ch_items > p.max_ch_items;
+  // 7. item tables, a thread per row: entry pref[q] + i -> (row k, its item i),
+  // one entry per row item (a work item is an entry and a KV head); and the
+  // split counters of every (decode row, KV head), zeroed 16 bytes at a time
+  for (int q = tid; q < n_tot; q += nt) {
+    const bool ch = q >= n_dec;
+    if (ch ? ch_over : dec_over) continue;
+    const int k = ch ? q - n_dec : q;
+    const int cnt = pref[q + 1] - pref[q];
+    int2* out = (ch ? p.ch_items : p.dec_items) + (pref[q] - (ch ? dec_tot : 0));
+    for (int i = 0; i < cnt; ++i) out[i] = make_int2(k, i);
+  }
+  if (!dec_over) {
+    const int n_cnt = n_dec * p.H_kv;  // the counters start 16-byte aligned in the workspace
+    for (int i = tid; i < (n_cnt >> 2); i += nt) reinterpret_cast<int4*>(p.dec_cnt)[i] = make_int4(0, 0, 0, 0);
+    for (int i = (n_cnt & ~3) + tid; i < n_cnt; i += nt) p.dec_cnt[i] = 0;
+  }
+  // 8. the header the main kernel starts from
+  if (warp == 0) {
+    const int n_first = chunk_cta_split(p, static_cast<float>(s_tiles), static_cast<float>(dec_pages),
+                                        ch_over ? 0 : static_cast<int>(n_ch_items), lane);
+    if (lane == 0) {
+      hdr[H_NDEC] = dec_over ? 0 : n_dec;
+      hdr[H_NDEC_ITEMS] = dec_over ? 0 : static_cast<int32_t>(n_dec_items);
+      hdr[H_NPART] = static_cast<int32_t>(static_cast<int64_t>(dec_tot) * p.H_q);
+      hdr[H_NCH] = ch_over ? 0 : n_ch;
+      hdr[H_NCH_ITEMS] = ch_over ? 0 : static_cast<int32_t>(n_ch_items);
+      if (dec_over || ch_over) atomicOr(hdr + H_STATUS, MS_STATUS_BAD_META);
+      hdr[H_DEC_CTR] = 0;
+      hdr[H_CH_CTR] = 0;
+      hdr[H_SPLIT] = static_cast<int32_t>(split);
+      hdr[H_CHUNK_CTAS] = n_first;
+    }
+  }
+}
+
+// The prologue as its own kernel, launched as a programmatic dependent of the
+// kernel before it on the stream (normally the append): it runs alongside that
+// kernel and waits for it before it exits, so the kernel after it sees the
+// append's writes.
+__global__ void __launch_bounds__(1024, 1) prologue_kernel(AttnParams p) {
+  griddep_launch_dependents();
+  prologue_body(p);
   griddep_wait();
 }
 
-// Item tables: item i of a list -> (row index in queue order, item within the
-// row), found by binary search over the list's item prefix staged in shared
-// memory; also zeroes the per-(decode row, KV head) split counters.  Runs on
-// many CTAs right after the prologue.
-constexpr int kItemThreads = 512;
-__global__ void __launch_bounds__(kItemThreads) items_kernel(AttnParams p) {
-  __shared__ int32_t pref[kMaxRows + 1];
-  griddep_launch_dependents();
-  griddep_wait();  // the prologue's lists and prefixes
-  for (int kind = 0; kind < 2; ++kind) {
-    const int n = kind == 0 ? p.hdr[H_NDEC] : p.hdr[H_NCH];
-    const int n_items = kind == 0 ? p.hdr[H_NDEC_ITEMS] : p.hdr[H_NCH_ITEMS];
-    const int32_t* gp = kind == 0 ? p.dec_item_prefix : p.ch_item_prefix;
-    if (n_items == 0) continue;  // uniform
-    for (int k = threadIdx.x; k <= n; k += kItemThreads) pref[k] = __ldg(gp + k);
-    __syncthreads();
-    int2* out = kind == 0 ? p.dec_items : p.ch_items;
-    for (int it = blockIdx.x * kItemThreads + threadIdx.x; it < n_items; it += gridDim.x * kItemThreads) {
-      const int k = find_in_prefix(pref, n, it);
-      out[it] = make_int2(k, it - pref[k]);
-    }
-    __syncthreads();
+// The append and the prologue as one kernel (the step call on small steps):
+// CTA 0 runs the prologue, the others the append's work units.  Launched in
+// plain stream order, so nothing of the step before is still running.
+template <typename Idx>
+__global__ void __launch_bounds__(kAppendThreads) append_prologue_kernel(AppendArgs a, AttnParams p) {
+  griddep_launch_dependents();  // the attention kernel may start its set-up
+  if (blockIdx.x == 0) {
+    prologue_body(p);
+    return;
   }
-  const int64_t n_cnt = static_cast<int64_t>(p.hdr[H_NDEC]) * p.H_kv;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kItemThreads + threadIdx.x; i < n_cnt;
-       i += static_cast<int64_t>(gridDim.x) * kItemThreads)
-    p.dec_cnt[i] = 0;
+  append_rope_units<Idx>(a, static_cast<Idx>(blockIdx.x - 1) * kAppendThreads + threadIdx.x,
+                         static_cast<Idx>(gridDim.x - 1) * kAppendThreads);
 }
 
 // ----------------------------------------------------------------------------
@@ -490,10 +619,11 @@ struct DecItem {
 
 __device__ __forceinline__ DecItem describe_dec(const AttnParams& p, int item, int split) {
   DecItem it;
-  const int2 kl = __ldg(p.dec_items + item);  // (decode row index, item within the row)
-  const int k = kl.x, local = kl.y;
-  const int sp = local / p.H_kv;
-  it.hk = local - sp * p.H_kv;
+  // items run (split, KV head) with the head fastest; the table has one entry per split
+  const int e = item / p.H_kv;
+  const int2 kl = __ldg(p.dec_items + e);  // (decode row index, split within the row)
+  const int k = kl.x, sp = kl.y;
+  it.hk = item - e * p.H_kv;
   it.k = k;
   it.row = __ldg(p.dec_rows + k);
   it.ctx = __ldg(p.ctx_lens + it.row);
@@ -998,16 +1128,18 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
       ChItem it;
       it.row = -1;
       if (item < n_items) {
-        const int2 kl = __ldg(p.ch_items + item);  // (chunk row index, item within the row)
-        const int k = kl.x, local = kl.y;
+        // items run (row item, KV head) with the head fastest; the table has one entry per row item
+        const int e = item / p.H_kv;
+        const int2 kl = __ldg(p.ch_items + e);  // (chunk row index, Q-tile pair counted from the last)
+        const int k = kl.x;
         it.row = __ldg(p.ch_rows + k);
         it.tb = __ldg(p.cu + it.row);
         const int d = __ldg(p.cu + it.row + 1) - it.tb;
         it.c = __ldg(p.q_start + it.row);
         const int n_qt = (d + TPT - 1) / TPT;
         const int n_pair = (n_qt + 1) >> 1;
-        const int pair = n_pair - 1 - local / p.H_kv;  // later tiles see more keys: run them first
-        it.hk = local % p.H_kv;
+        const int pair = n_pair - 1 - kl.y;  // later tiles see more keys: run them first
+        it.hk = item - e * p.H_kv;
         it.n_kt = 0;
         for (int t = 0; t < 2; ++t) {
           const int qt = 2 * pair + t;
@@ -1458,7 +1590,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  griddep_wait();  // the item tables (and, through the prologue, the append's q_rot and pages)
+  griddep_wait();  // the prologue's item tables (and, through it, the append's q_rot and pages)
   const int n_ch_items = p.hdr[H_NCH_ITEMS];
   const int n_dec_items = p.hdr[H_NDEC_ITEMS];
   __syncthreads();  // every thread holds the address before the phases reuse the memory
@@ -1508,7 +1640,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 namespace {
 
 struct WsLayout {
-  size_t hdr, dec_rows, dec_item_prefix, dec_part_base, dec_nsplit, ch_rows, ch_item_prefix, dec_cnt, dec_items,
+  size_t hdr, dec_rows, dec_part_base, dec_nsplit, ch_rows, dec_cnt, dec_items,
       ch_items, part_ml, part_acc, total;
   int64_t max_partials, max_dec_items, max_ch_items;
 };
@@ -1523,16 +1655,12 @@ WsLayout ws_layout(int64_t max_rows, int64_t max_tokens, int64_t max_context_tot
   off += H_WORDS * 4;
   w.dec_rows = off;
   off = align_up(off + max_rows * 4, 16);
-  w.dec_item_prefix = off;
-  off = align_up(off + (max_rows + 1) * 4, 16);
   w.dec_part_base = off;
   off = align_up(off + max_rows * 4, 16);
   w.dec_nsplit = off;
   off = align_up(off + max_rows * 4, 16);
   w.ch_rows = off;
   off = align_up(off + max_rows * 4, 16);
-  w.ch_item_prefix = off;
-  off = align_up(off + (max_rows + 1) * 4, 16);
   w.dec_cnt = off;
   off = align_up(off + max_rows * H_kv * 4, 256);
   // every decode split covers >= kMinSplitPages pages: splits <= ctx / (16 * kMinSplitPages) + rows
@@ -1540,10 +1668,10 @@ WsLayout ws_layout(int64_t max_rows, int64_t max_tokens, int64_t max_context_tot
   const int64_t G = H_q / (H_kv > 0 ? H_kv : 1);
   w.max_dec_items = H_kv * max_splits;
   w.max_ch_items = H_kv * (cdiv64(max_tokens * G, 128) + max_rows);
-  w.dec_items = off;
-  off = align_up(off + w.max_dec_items * 8, 256);
+  w.dec_items = off;  // one entry per split, per Q-tile pair: the KV head is not in the tables
+  off = align_up(off + (w.max_dec_items / H_kv) * 8, 256);
   w.ch_items = off;
-  off = align_up(off + w.max_ch_items * 8, 256);
+  off = align_up(off + (w.max_ch_items / H_kv) * 8, 256);
   w.max_partials = H_q * max_splits;
   w.part_ml = off;
   off = align_up(off + w.max_partials * 2 * 4, 256);
@@ -1682,21 +1810,26 @@ extern "C" MS_API int ms_num_sms(void) {
 
 namespace {
 
-// The attention call behind both entry points.  Every argument check comes
-// before the first enqueue, so a call that returns an error has put nothing on
-// the stream.  *launched tells whether kernels were enqueued (a step with no
-// tokens enqueues none); clear_status makes the prologue zero the status word
-// before anything of this call can set it.  stall_limit_ns > 0 is the test
-// hook of ms_test_attention_stall: chunk-phase producers publish nothing and
-// every chunk-phase wait gives up after that many nanoseconds.
-int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, int32_t num_pages,
-                   const int32_t* cu_seqlens_q, const int32_t* q_start_pos, const int32_t* context_lens,
-                   const int32_t* block_tables, const int32_t* bt_offsets, int64_t bt_len, int32_t bt_stride,
-                   int32_t num_rows, int32_t num_tokens,
-                   int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
-                   void* out, void* workspace, size_t ws_bytes, ms_stream_t stream, bool clear_status,
-                   int64_t stall_limit_ns, bool* launched) {
-  *launched = false;
+// An attention call's launch parameters: the kernels' arguments and the four
+// tensor maps.
+struct AttnPlan {
+  AttnParams p;
+  CUtensorMap tq, tk, tv, tvp;
+};
+
+// Checks every argument of an attention call and fills *L; enqueues nothing.
+// *empty: the step has no tokens, so there is nothing to launch.
+// clear_status makes the prologue zero the status word before anything of
+// this call can set it.  stall_limit_ns > 0 is the test hook of
+// ms_test_attention_stall: chunk-phase producers publish nothing and every
+// chunk-phase wait gives up after that many nanoseconds.
+int attention_setup(const void* q_rot, const void* k_cache, const void* v_cache, int32_t num_pages,
+                    const int32_t* cu_seqlens_q, const int32_t* q_start_pos, const int32_t* context_lens,
+                    const int32_t* block_tables, const int32_t* bt_offsets, int64_t bt_len, int32_t bt_stride,
+                    int32_t num_rows, int32_t num_tokens, int64_t context_total, int32_t H_q, int32_t H_kv,
+                    int32_t D, int32_t page_size, float scale, void* out, void* workspace, size_t ws_bytes,
+                    bool clear_status, int64_t stall_limit_ns, AttnPlan* L, bool* empty) {
+  *empty = true;
   if (num_rows < 0 || num_tokens < 0 || context_total < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 ||
       (D != 64 && D != 128) || page_size != kPage || bt_stride < 0 || bt_len < 0 || num_pages < 0 ||
       !(scale > 0.f))
@@ -1704,6 +1837,7 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
   const int G = H_q / H_kv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return MS_ERR_ARG;
   if (num_rows == 0 || num_tokens == 0) return MS_OK;  // no tokens: every row is a pad row
+  *empty = false;
   if (!q_rot || !k_cache || !v_cache || !cu_seqlens_q || !q_start_pos || !context_lens || !block_tables || !out ||
       !workspace || num_pages < 1 || (bt_offsets == nullptr && bt_stride < 1) || (bt_offsets != nullptr && bt_len < 1))
     return MS_ERR_ARG;
@@ -1718,7 +1852,10 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return MS_ERR_CUDA;
 
-  CUtensorMap tq, tk, tv, tvp;
+  CUtensorMap& tq = L->tq;
+  CUtensorMap& tk = L->tk;
+  CUtensorMap& tv = L->tv;
+  CUtensorMap& tvp = L->tvp;
   {
     const cuuint64_t dq[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_q),
                               static_cast<cuuint64_t>(num_tokens)};
@@ -1744,7 +1881,7 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
   }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  AttnParams p;
+  AttnParams& p = L->p;
   p.q_rot = static_cast<const bf16*>(q_rot);
   p.k_cache = static_cast<const bf16*>(k_cache);
   p.v_cache = static_cast<const bf16*>(v_cache);
@@ -1757,11 +1894,9 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
   p.out = static_cast<bf16*>(out);
   p.hdr = reinterpret_cast<int32_t*>(ws + w.hdr);
   p.dec_rows = reinterpret_cast<int32_t*>(ws + w.dec_rows);
-  p.dec_item_prefix = reinterpret_cast<int32_t*>(ws + w.dec_item_prefix);
   p.dec_part_base = reinterpret_cast<int32_t*>(ws + w.dec_part_base);
   p.dec_nsplit = reinterpret_cast<int32_t*>(ws + w.dec_nsplit);
   p.ch_rows = reinterpret_cast<int32_t*>(ws + w.ch_rows);
-  p.ch_item_prefix = reinterpret_cast<int32_t*>(ws + w.ch_item_prefix);
   p.dec_items = reinterpret_cast<int2*>(ws + w.dec_items);
   p.dec_cnt = reinterpret_cast<int32_t*>(ws + w.dec_cnt);
   p.ch_items = reinterpret_cast<int2*>(ws + w.ch_items);
@@ -1786,16 +1921,31 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
   p.wait_limit_ns = stall_limit_ns > 0 ? static_cast<uint64_t>(stall_limit_ns) : 2000000000ull;
   p.scale_log2 = scale * 1.4426950408889634f;
 
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (ensure_smem_limit(prologue_kernel, 8, static_cast<int>(sizeof(PrologueSmem))) != MS_OK) return MS_ERR_CUDA;
-  *launched = true;  // from here on, kernels may be on the stream
-  if (launch_dependent(prologue_kernel, dim3(1), dim3(kPrologueThreads), sizeof(PrologueSmem), st, p) !=
-          cudaSuccess ||
-      launch_dependent(items_kernel, dim3(sms < 64 ? sms : 64), dim3(kItemThreads), 0, st, p) != cudaSuccess)
-    return MS_ERR_CUDA;
-  const int n_ctas = sms;  // one persistent CTA per SM
+  p.chunk_tile_ns = kChunkTileNs;
+  p.decode_sm_gbs = kDecodeSmGBs;
+  p.hbm_gbs = kHbmGBs;
+  return MS_OK;
+}
+
+// The prologue as its own kernel, a programmatic dependent of the kernel
+// before it: about a thread per row (one warp up to 32 rows, else at least a
+// warp per scheduler).
+int launch_prologue(const AttnParams& p, cudaStream_t st) {
+  if (ensure_smem_limit(prologue_kernel, 8, prologue_words(kMaxRows) * 4) != MS_OK) return MS_ERR_CUDA;
+  const int S = p.num_rows;
+  const int threads = S <= 32 ? 32 : S >= 1024 ? 1024 : S <= 128 ? 128 : (S + 31) / 32 * 32;
+  return launch_dependent(prologue_kernel, dim3(1), dim3(threads), prologue_words(S) * 4, st, p) == cudaSuccess
+             ? MS_OK
+             : MS_ERR_CUDA;
+}
+
+// The persistent attention kernel for the call's head dim and group size.
+int launch_attention(const AttnPlan& L, cudaStream_t st) {
+  const AttnParams& p = L.p;
+  const CUtensorMap &tq = L.tq, &tk = L.tk, &tv = L.tv, &tvp = L.tvp;
+  const int n_ctas = p.num_sms;  // one persistent CTA per SM
   int rc = MS_ERR_ARG;
-  switch (D * 100 + G) {
+  switch (p.D * 100 + p.G) {
     case 6401: rc = launch_paths<64, 1>(p, tq, tk, tv, tvp, n_ctas, st); break;
     case 6402: rc = launch_paths<64, 2>(p, tq, tk, tv, tvp, n_ctas, st); break;
     case 6404: rc = launch_paths<64, 4>(p, tq, tk, tv, tvp, n_ctas, st); break;
@@ -1808,6 +1958,36 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
   }
   return rc;
 }
+
+// The attention call behind the attention entry points: prologue, then the
+// persistent kernel.  Every argument check comes before the first enqueue, so
+// a call that returns an error has put nothing on the stream.  *launched tells
+// whether kernels were enqueued (a step with no tokens enqueues none).
+int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, int32_t num_pages,
+                   const int32_t* cu_seqlens_q, const int32_t* q_start_pos, const int32_t* context_lens,
+                   const int32_t* block_tables, const int32_t* bt_offsets, int64_t bt_len, int32_t bt_stride,
+                   int32_t num_rows, int32_t num_tokens,
+                   int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
+                   void* out, void* workspace, size_t ws_bytes, ms_stream_t stream, bool clear_status,
+                   int64_t stall_limit_ns, bool* launched) {
+  *launched = false;
+  AttnPlan L;
+  bool empty = true;
+  const int rc = attention_setup(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens,
+                                 block_tables, bt_offsets, bt_len, bt_stride, num_rows, num_tokens, context_total, H_q,
+                                 H_kv, D, page_size, scale, out, workspace, ws_bytes, clear_status, stall_limit_ns, &L,
+                                 &empty);
+  if (rc != MS_OK || empty) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  *launched = true;  // from here on, kernels may be on the stream
+  const int rp = launch_prologue(L.p, st);
+  return rp != MS_OK ? rp : launch_attention(L, st);
+}
+
+// Steps of at most this many rows run the prologue inside the append's launch
+// (its shared memory, prologue_words(rows), then sits on every append CTA:
+// 20 KB at this bound, under an eighth of the SM's for 8 resident CTAs).
+constexpr int kFuseRows = 1024;
 
 }  // namespace
 
@@ -1837,6 +2017,53 @@ extern "C" MS_API int ms_mixed_step_attention_ragged(const void* q_rot, const vo
   return attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens, bt_pages,
                         bt_offsets, num_bt_pages, 0, num_rows, num_tokens, context_total, H_q, H_kv, D, page_size,
                         scale, out, workspace, ws_bytes, stream, false, 0, &launched);
+}
+
+extern "C" MS_API int ms_mixed_step(const void* q, const void* k, const void* v, const int32_t* positions,
+                                   const int32_t* slot_mapping, const float* cos_tab, const float* sin_tab,
+                                   int32_t max_pos, void* k_cache, void* v_cache, int32_t num_pages, void* q_rot,
+                                   const int32_t* cu_seqlens_q, const int32_t* q_start_pos,
+                                   const int32_t* context_lens, const int32_t* block_tables,
+                                   const int32_t* bt_offsets, int64_t bt_len, int32_t bt_stride, int32_t num_rows,
+                                   int32_t num_tokens, int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D,
+                                   int32_t page_size, float scale, void* out, void* workspace, size_t ws_bytes,
+                                   int32_t* dev_status, ms_stream_t stream) {
+  AppendArgs a;
+  int64_t units = 0;
+  int rc = append_setup(q, k, v, positions, slot_mapping, num_tokens, cos_tab, sin_tab, max_pos, k_cache, v_cache,
+                        num_pages, q_rot, H_q, H_kv, D, page_size, dev_status, &a, &units);
+  if (rc != MS_OK) return rc;
+  AttnPlan L;
+  bool empty = true;
+  rc = attention_setup(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens, block_tables,
+                       bt_offsets, bt_offsets != nullptr ? bt_len : 0, bt_offsets != nullptr ? 0 : bt_stride, num_rows,
+                       num_tokens, context_total, H_q, H_kv, D, page_size, scale, out, workspace, ws_bytes, false, 0,
+                       &L, &empty);
+  if (rc != MS_OK) return rc;
+  if (units == 0) return MS_OK;  // no tokens: nothing to append or attend
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (empty || num_rows > kFuseRows) {
+    rc = ms_kv_append_rope(q, k, v, positions, slot_mapping, num_tokens, cos_tab, sin_tab, max_pos, k_cache, v_cache,
+                           num_pages, q_rot, H_q, H_kv, D, page_size, dev_status, stream);
+    if (rc != MS_OK || empty) return rc;
+    rc = launch_prologue(L.p, st);
+    return rc != MS_OK ? rc : launch_attention(L, st);
+  }
+  // CTA 0 runs the prologue beside the append's CTAs; plain stream order, so the
+  // step before has finished with the workspace
+  const int64_t blocks = 1 + append_blocks(units, L.p.num_sms);
+  const int smem = prologue_words(num_rows) * 4;
+  if (units + blocks * kAppendThreads < (int64_t{1} << 31)) {
+    if (ensure_smem_limit(append_prologue_kernel<uint32_t>, 9, prologue_words(kFuseRows) * 4) != MS_OK)
+      return MS_ERR_CUDA;
+    append_prologue_kernel<uint32_t><<<static_cast<unsigned>(blocks), kAppendThreads, smem, st>>>(a, L.p);
+  } else {
+    if (ensure_smem_limit(append_prologue_kernel<int64_t>, 10, prologue_words(kFuseRows) * 4) != MS_OK)
+      return MS_ERR_CUDA;
+    append_prologue_kernel<int64_t><<<static_cast<unsigned>(blocks), kAppendThreads, smem, st>>>(a, L.p);
+  }
+  if (cudaGetLastError() != cudaSuccess) return MS_ERR_CUDA;
+  return launch_attention(L, st);
 }
 
 extern "C" MS_API int ms_test_attention_stall(const void* q_rot, const void* k_cache, const void* v_cache,

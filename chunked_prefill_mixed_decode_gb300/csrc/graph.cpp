@@ -6,7 +6,7 @@
 // next bucket; the pad tokens are wasted work and the scheduler's budget and
 // the executed token count differ by that padding.
 //
-// Here one graph per bucket records ms_kv_append_rope + ms_mixed_step_attention
+// Here one graph per bucket records ms_mixed_step (append + attention)
 // at fixed sizes: bucket tokens, max_rows rows, a block-table stride of
 // max_row_pages and a context bound of num_pages * 16.  A replay copies the
 // step's metadata into fixed device buffers, padded: tokens past the real
@@ -90,16 +90,13 @@ int enqueue_step(const ms_step_graph* g, int32_t bucket, cudaStream_t st) {
   uint8_t* ws = ws_base(g);
   const int32_t* positions = reinterpret_cast<const int32_t*>(ws + g->lay.positions);
   const int32_t* slots = reinterpret_cast<const int32_t*>(ws + g->lay.slots);
-  int rc = ms_kv_append_rope(b.q, b.k, b.v, positions, slots, bucket, b.cos_tab, b.sin_tab, c.max_pos, b.k_cache,
-                             b.v_cache, c.num_pages, b.q_rot, c.H_q, c.H_kv, c.D, kPage, b.dev_status,
-                             reinterpret_cast<ms_stream_t>(st));
-  if (rc != MS_OK) return rc;
-  return ms_mixed_step_attention(
-      b.q_rot, b.k_cache, b.v_cache, c.num_pages, reinterpret_cast<const int32_t*>(ws + g->lay.cu),
-      reinterpret_cast<const int32_t*>(ws + g->lay.q_start), reinterpret_cast<const int32_t*>(ws + g->lay.ctx),
-      reinterpret_cast<const int32_t*>(ws + g->lay.bt), c.max_row_pages, c.max_rows, bucket,
-      static_cast<int64_t>(c.num_pages) * kPage, c.H_q, c.H_kv, c.D, kPage, c.scale, b.out, ws + g->lay.attn,
-      g->lay.total - g->lay.attn, reinterpret_cast<ms_stream_t>(st));
+  return ms_mixed_step(b.q, b.k, b.v, positions, slots, b.cos_tab, b.sin_tab, c.max_pos, b.k_cache, b.v_cache,
+                       c.num_pages, b.q_rot, reinterpret_cast<const int32_t*>(ws + g->lay.cu),
+                       reinterpret_cast<const int32_t*>(ws + g->lay.q_start),
+                       reinterpret_cast<const int32_t*>(ws + g->lay.ctx),
+                       reinterpret_cast<const int32_t*>(ws + g->lay.bt), nullptr, 0, c.max_row_pages, c.max_rows,
+                       bucket, static_cast<int64_t>(c.num_pages) * kPage, c.H_q, c.H_kv, c.D, kPage, c.scale, b.out,
+                       ws + g->lay.attn, g->lay.total - g->lay.attn, b.dev_status, reinterpret_cast<ms_stream_t>(st));
 }
 
 void release(ms_step_graph* g) {

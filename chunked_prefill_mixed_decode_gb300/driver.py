@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import time
 
-from . import Engine, StepGraph, attention_workspace_size, kv_append_rope, mixed_step_attention, read_status
+from . import Engine, StepGraph, attention_workspace_size, mixed_step, read_status
 from .step import MetaStager
 
 
@@ -91,12 +91,10 @@ class RoundDriver:
             batch = self.stager.stage(meta, self.stream)
             t_plan = time.perf_counter()
             self.ev0.record(self.stream)
-            kv_append_rope(q[:T], k[:T], v[:T], batch.positions, batch.slot_mapping, self.cos, self.sin,
-                           self.k_cache, self.v_cache, q_rot=self.q_rot[:T], dev_status=self.status,
-                           stream=self.stream)
-            mixed_step_attention(self.q_rot[:T], self.k_cache, self.v_cache, batch.cu_seqlens_q, batch.q_start_pos,
-                                 batch.context_lens, batch.block_tables, batch.context_total, self.out[:T],
-                                 self.workspace, scale=self.scale, stream=self.stream)
+            mixed_step(q[:T], k[:T], v[:T], batch.positions, batch.slot_mapping, self.cos, self.sin, self.k_cache,
+                       self.v_cache, self.q_rot[:T], batch.cu_seqlens_q, batch.q_start_pos, batch.context_lens,
+                       batch.block_tables, batch.context_total, self.out[:T], self.workspace,
+                       dev_status=self.status, scale=self.scale, stream=self.stream)
             self.ev1.record(self.stream)
             self.stream.synchronize()
             st = read_status(self.status, self.stream) | read_status(self.workspace, self.stream)

@@ -10,7 +10,7 @@ import dataclasses
 
 import numpy as np
 
-from . import (attention_workspace_size, kv_append_rope, mixed_step_attention, mixed_step_attention_ragged,
+from . import (attention_workspace_size, mixed_step, mixed_step_attention, mixed_step_attention_ragged,
                rope_table)
 
 META_KEYS = ("cu_seqlens_q", "q_start_pos", "context_lens", "positions", "slot_mapping", "block_tables")
@@ -154,13 +154,15 @@ def workspace_for(batch: DeviceBatch, H_q: int, H_kv: int, D: int, device):
 
 def run_step(q, k, v, batch: DeviceBatch, cos, sin, k_cache, v_cache, out, workspace, q_rot=None,
              dev_status=None, scale=None, stream=None):
-    """kv_append_rope then mixed_step_attention on one stream; returns q_rot."""
+    """One step of one layer through ms_mixed_step (the append, then the attention, with the
+    prologue inside the append's launch on small steps); returns q_rot."""
     if q_rot is None:
         q_rot = q
     T = batch.num_tokens
-    kv_append_rope(q[:T], k[:T], v[:T], batch.positions, batch.slot_mapping, cos, sin, k_cache, v_cache,
-                   q_rot=q_rot[:T], dev_status=dev_status, stream=stream)
-    attend(q_rot[:T], k_cache, v_cache, batch, out[:T], workspace, scale=scale, stream=stream)
+    mixed_step(q[:T], k[:T], v[:T], batch.positions, batch.slot_mapping, cos, sin, k_cache, v_cache, q_rot[:T],
+               batch.cu_seqlens_q, batch.q_start_pos, batch.context_lens, batch.block_tables, batch.context_total,
+               out[:T], workspace, bt_offsets=batch.bt_offsets if batch.ragged else None, dev_status=dev_status,
+               scale=scale, stream=stream)
     return q_rot
 
 

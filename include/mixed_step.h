@@ -279,6 +279,28 @@ MS_API int ms_mixed_step_attention_ragged(const void* q_rot, const void* k_cache
                                           int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
                                           void* out, void* workspace, size_t ws_bytes, ms_stream_t stream);
 
+/* ms_mixed_step -- one step of one attention layer: ms_kv_append_rope of the
+ * step's num_tokens new tokens, then the attention of ms_mixed_step_attention
+ * (block_tables padded with bt_stride, bt_offsets == NULL) or of
+ * ms_mixed_step_attention_ragged (block_tables = bt_pages with bt_len entries,
+ * bt_offsets given), in that order on `stream`, with the same arguments,
+ * layouts, status words and errors as those calls.  Decodes and prompt
+ * chunks share one forward pass ([sar] sections 02-04), so a step calls this
+ * once per attention layer over the whole packed batch.  T of the
+ * append is num_tokens.  On steps of at most 1024 rows the append and the
+ * attention's prologue share one launch (two kernels per step instead of
+ * three); results are bit-identical to the two separate calls.  Every
+ * argument of both parts is checked before the first enqueue.
+ * Errors: MS_ERR_ARG, MS_ERR_CUDA. */
+MS_API int ms_mixed_step(const void* q, const void* k, const void* v, const int32_t* positions,
+                         const int32_t* slot_mapping, const float* cos_tab, const float* sin_tab, int32_t max_pos,
+                         void* k_cache, void* v_cache, int32_t num_pages, void* q_rot,
+                         const int32_t* cu_seqlens_q, const int32_t* q_start_pos, const int32_t* context_lens,
+                         const int32_t* block_tables, const int32_t* bt_offsets, int64_t bt_len, int32_t bt_stride,
+                         int32_t num_rows, int32_t num_tokens, int64_t context_total,
+                         int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
+                         void* out, void* workspace, size_t ws_bytes, int32_t* dev_status, ms_stream_t stream);
+
 /* ms_mixed_step_attention_noalloc -- the same attention step as
  * ms_mixed_step_attention, for callers that cannot give the library a
  * workspace.  A serving process that reserves nearly all device memory for

@@ -168,6 +168,57 @@ def test_many_rows(env, n_dec):
     _full_parity(env, wl, _states(wl), seed=10)
 
 
+@pytest.mark.parametrize("n_dec", [30, 31, 32, 33])
+def test_prologue_row_count_edges(env, n_dec):
+    """Up to 32 rows the prologue is one warp (a row per lane); from 33 rows a block of warps.
+    n_dec decodes plus one chunk straddle that edge."""
+    rng = np.random.default_rng(70 + n_dec)
+    ctx = tuple(int(c) for c in rng.integers(0, 700, size=n_dec))
+    wl = workloads.small_mixed(seed=70 + n_dec, H_q=8, H_kv=2, D=128, dec_ctx=ctx, prompts=((40, 37),))
+    _full_parity(env, wl, _states(wl), seed=11)
+
+
+@pytest.mark.parametrize("n_dec,ragged", [(3, False), (3, True), (60, False), (60, True), (1100, True)])
+def test_step_call_equals_separate_calls(env, n_dec, ragged):
+    """ms_mixed_step against ms_kv_append_rope followed by the attention call, same inputs: q_rot, both
+    pools and the output bit-identical, and the output within tolerance of the oracle.  Up to 32 rows the
+    prologue inside the append's launch is one warp, up to 1024 rows a block of warps; past 1024 rows the
+    step call launches the three kernels of the separate calls."""
+    torch, ms, step = env
+    rng = np.random.default_rng(90 + n_dec)
+    ctx = tuple(int(c) for c in rng.integers(0, 300, size=n_dec))
+    wl = workloads.small_mixed(seed=90 + n_dec, H_q=8, H_kv=2, D=64, dec_ctx=ctx, prompts=((40, 37), (0, 130)))
+    states = _states(wl)
+    meta = ms.build_batch_metadata(states, _tables(wl), wl.token_budget, wl.max_chunk, ragged=ragged)
+    b = step.to_device(meta, "cuda")
+    T = meta["num_tokens"]
+    q, k, v = workloads.step_tensors(wl, T, 7, "cuda")
+    cos, sin = step.rope_tables_device(wl.max_pos + 1, wl.D, "cuda")
+    runs = []
+    for fused in (False, True):
+        kc, vc = workloads.kv_pool(wl, 7, "cuda")
+        q_rot, out = torch.empty_like(q), torch.zeros_like(q)
+        ws = step.workspace_for(b, wl.H_q, wl.H_kv, wl.D, "cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            step.run_step(q, k, v, b, cos, sin, kc, vc, out, ws, q_rot=q_rot, dev_status=status)
+        else:
+            ms.kv_append_rope(q, k, v, b.positions, b.slot_mapping, cos, sin, kc, vc, q_rot=q_rot,
+                              dev_status=status)
+            step.attend(q_rot, kc, vc, b, out, ws)
+        torch.cuda.synchronize()
+        assert ms.read_status(status) == 0 and ms.read_status(ws) == 0
+        runs.append([workloads.bf16_bits(t) for t in (q_rot, kc, vc, out)])
+    for name, sep, fus in zip(("q_rot", "k_cache", "v_cache", "out"), *runs):
+        np.testing.assert_array_equal(fus, sep, err_msg=name)
+    pmeta = ms.build_batch_metadata(states, _tables(wl), wl.token_budget, wl.max_chunk)
+    k_in, v_in = (workloads.bf16_bits(t) for t in workloads.kv_pool(wl, 7, "cuda"))
+    q_ref, kp, vp = oracle.kv_append(workloads.bf16_bits(q), workloads.bf16_bits(k), workloads.bf16_bits(v),
+                                     pmeta["positions"], pmeta["slot_mapping"], k_in, v_in)
+    np.testing.assert_array_equal(runs[1][0], q_ref)
+    _check_attention(runs[1][3], oracle.attention_all(q_ref, kp, vp, pmeta, wl.H_kv), "step call")
+
+
 def test_more_rows_than_a_step_holds_is_refused(env):
     """8193 rows: the call returns MS_ERR_ARG before any launch."""
     torch, ms, step = env
@@ -241,16 +292,24 @@ def test_status_reports_bad_slot_and_page(env):
     assert ms.read_status(case.ws) == 0  # cleared by the read
 
 
-def test_inconsistent_metadata_is_flagged(env):
+@pytest.mark.parametrize("dec_ctx", [(20, 30), tuple(range(20, 60))])
+def test_inconsistent_metadata_is_flagged(env, dec_ctx):
+    """Both prologue shapes (one warp up to 32 rows, a block beyond) reject a row with ctx != c + d."""
     torch, ms, step = env
-    wl = workloads.small_mixed(seed=42, H_q=4, H_kv=2, D=64, dec_ctx=(20, 30), prompts=((0, 9),))
+    wl = workloads.small_mixed(seed=42, H_q=4, H_kv=2, D=64, dec_ctx=dec_ctx, prompts=((0, 9),))
     case = Case(env, wl, _states(wl), seed=3)
-    case.batch.context_lens[0] += 1  # no longer c + d
+    case.batch.context_lens[len(dec_ctx) // 2] += 1  # no longer c + d
     ms.mixed_step_attention(case.q, case.k_cache, case.v_cache, case.batch.cu_seqlens_q, case.batch.q_start_pos,
                             case.batch.context_lens, case.batch.block_tables, case.batch.context_total,
                             case.out, case.ws)
     torch.cuda.synchronize()
     assert ms.read_status(case.ws) & ms.STATUS_BAD_META
+    # the same through the step call, whose prologue runs inside the append's launch
+    step.run_step(case.q, case.k, case.v, case.batch, case.cos, case.sin, case.k_cache, case.v_cache, case.out,
+                  case.ws, q_rot=case.q_rot, dev_status=case.status)
+    torch.cuda.synchronize()
+    assert ms.read_status(case.ws) & ms.STATUS_BAD_META
+    assert ms.read_status(case.status) == 0  # the append itself was fine
 
 
 def test_append_bad_position_and_negative_slot(env):
