@@ -133,6 +133,13 @@ def lib() -> ctypes.CDLL:
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _VP, _VP,
                                           ctypes.c_size_t, ctypes.c_int64, _VP]
+    h.ms_test_attention_split.restype = ctypes.c_int
+    h.ms_test_attention_split.argtypes = [_VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int64,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_float, _VP, _VP, ctypes.c_size_t, ctypes.c_int32, _VP]
+    h.ms_cost_model_rates.restype = ctypes.c_int
+    h.ms_cost_model_rates.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
     h.ms_read_status.restype = ctypes.c_int
     h.ms_read_status.argtypes = [_VP, _VP, _I32P]
     h.ms_num_sms.restype = ctypes.c_int
@@ -732,6 +739,50 @@ def test_attention_stall(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, con
                                        workspace.numel() * workspace.element_size(), int(wait_limit_ns),
                                        _stream(stream))
     _check(rc, "ms_test_attention_stall")
+
+
+def test_attention_split(q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables,
+                         context_total: int, out, workspace, chunk_ctas: int, bt_offsets=None, scale: float = None,
+                         stream=None) -> None:
+    """Test hook of the SM-split cost model (ms_test_attention_split): the attention call with
+    ``chunk_ctas`` CTAs starting on chunk work.  ``block_tables`` is the padded table, or with
+    ``bt_offsets`` the ragged page list.  Outputs equal the ordinary call's."""
+    import torch
+    if q_rot.dim() != 3:
+        raise ValueError("q_rot must be [T, H_q, D]")
+    T, H_q, D = q_rot.shape
+    H_kv = k_cache.shape[1]
+    _pools(k_cache, v_cache, H_kv, D)
+    S = cu_seqlens_q.shape[0] - 1
+    if bt_offsets is None:
+        stride = block_tables.shape[1] if block_tables.dim() == 2 else block_tables.shape[0] // max(S, 1)
+        bt_len = 0
+    else:
+        _dev(bt_offsets, "bt_offsets", torch.int32, min_numel=S + 1)
+        stride, bt_len = 0, block_tables.numel()
+    _dev(block_tables, "block_tables", torch.int32, min_numel=1)
+    _dev(out, "out", torch.bfloat16, (T, H_q, D))
+    _dev(workspace, "workspace", None)
+    _on_one_gpu("q_rot k_cache v_cache cu_seqlens_q q_start_pos context_lens block_tables bt_offsets out workspace",
+                q_rot, k_cache, v_cache, cu_seqlens_q, q_start_pos, context_lens, block_tables, bt_offsets, out,
+                workspace)
+    if scale is None:
+        scale = float(D) ** -0.5
+    rc = lib().ms_test_attention_split(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                       _ptr(cu_seqlens_q), _ptr(q_start_pos), _ptr(context_lens),
+                                       _ptr(block_tables), _ptr(bt_offsets), bt_len, stride, S, T,
+                                       int(context_total), H_q, H_kv, D, PAGE_SIZE, float(scale), _ptr(out),
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       int(chunk_ctas), _stream(stream))
+    _check(rc, "ms_test_attention_split")
+
+
+def cost_model_rates() -> tuple:
+    """(rated SM clock in MHz, HBM GB/s) behind the SM split before a call has measured the clock
+    (ms_cost_model_rates)."""
+    mhz, gbs = ctypes.c_float(0), ctypes.c_float(0)
+    _check(lib().ms_cost_model_rates(ctypes.byref(mhz), ctypes.byref(gbs)), "ms_cost_model_rates")
+    return float(mhz.value), float(gbs.value)
 
 
 def read_status(dev_status, stream=None) -> int:

@@ -61,11 +61,19 @@ constexpr int kChunkThreads = 32 * (4 + kSoftmaxWarps);  // warp 0 TMA + queue, 
 constexpr int kSortLimit = 2048;    // rows sorted longest-first up to this count
 constexpr int kMaxRows = 8192;      // rows of one step
 // Cost model that splits the SMs between the two row kinds at the start of a
-// step (CTAs then move to whichever queue still has work): one 128x128 chunk
-// tile per SM, and the decode bandwidth one SM sustains, capped by HBM.
-constexpr float kChunkTileNs = 3000.f;   // per 128x128 tile and SM, alongside decode traffic
-constexpr float kDecodeSmGBs = 62.f;    // G = 1; fewer bytes per SM-cycle as G grows
-constexpr float kHbmGBs = 6500.f;
+// step (CTAs then move to whichever queue still has work): the SM time of one
+// 128x128 chunk tile, and the decode bandwidth one SM sustains, capped by HBM.
+// Both SM-side rates are properties of the kernels' instruction streams, so
+// they are kept per SM clock cycle and scaled by the clock the previous call
+// ran at (measured on the GPU, see H_CLOCK_MHZ); HBM bandwidth comes from the
+// device's memory clock and bus width.  The per-cycle figures come from
+// sweeps of the split on the 8B GQA and long bimodal steps, where the kernel
+// measured its clock at about 1.94 GHz (3.0 us per tile, 62 GB/s per decode
+// SM); a test sweeps the split again and checks the model's choice against
+// the best.
+constexpr float kChunkTileCycles = 5820.f;    // SM cycles per 128x128 tile, alongside decode traffic
+constexpr float kDecodeBytesPerCycle = 32.f;  // decode bytes per SM cycle at G = 1; fewer as G grows
+constexpr float kHbmCopyEfficiency = 0.80f;   // sustained share of the nominal HBM rate
 
 // workspace header (int32 words)
 enum {
@@ -79,6 +87,7 @@ enum {
   H_SPLIT = 7,
   H_NPART = 8,
   H_CHUNK_CTAS = 9,  // CTAs that start on chunk work (the rest start on decodes)
+  H_CLOCK_MHZ = 10,  // SM clock the last call ran at (kept across calls; 0 in a fresh workspace)
   H_WORDS = 64
 };
 
@@ -113,9 +122,9 @@ struct AttnParams {
   int32_t clear_status;  // the prologue zeroes the status word first (scratch owned by the library)
   int32_t test_stall;    // test hook: chunk-phase producers publish no work item (0 in every real call)
   uint64_t wait_limit_ns;  // bound of every chunk-phase wait
-  float chunk_tile_ns;     // cost model of the SM split: ns per 128x128 chunk tile on one SM,
-  float decode_sm_gbs;     // decode GB/s of one SM at G = 1,
-  float hbm_gbs;           // and the HBM bandwidth that caps decode
+  int32_t force_chunk_ctas;  // test hook: CTAs that start on chunk work (-1: the cost model decides)
+  float sm_mhz;              // cost model: the SM clock when no call has measured it yet,
+  float hbm_gbs;             // and the HBM bandwidth that caps decode
   float scale_log2;
 };
 
@@ -195,10 +204,14 @@ __host__ __device__ constexpr int prologue_words(int S) { return 5 * ((S + 3) & 
 // balance point, or, while decode stays HBM-bound, as many chunk CTAs as keep
 // it so.  Called by one whole warp; the candidate counts go one per lane.
 __device__ int chunk_cta_split(const AttnParams& p, float tiles, float dec_pages, int n_items, int lane) {
+  if (p.force_chunk_ctas >= 0) return min(p.force_chunk_ctas, p.num_sms);
+  // the SM clock of the previous call on this workspace, else the device's rated clock
+  const int measured = p.hdr[H_CLOCK_MHZ];
+  const float mhz = measured >= 200 && measured <= 5000 ? static_cast<float>(measured) : p.sm_mhz;
   const float S = static_cast<float>(p.num_sms);
-  const float T = tiles * p.chunk_tile_ns;                                    // SM-ns of chunk work
+  const float T = tiles * __fdividef(kChunkTileCycles * 1000.f, mhz);         // SM-ns of chunk work
   const float B = dec_pages * p.H_kv * kPage * p.D * 4.f;                     // decode bytes
-  const float g = p.decode_sm_gbs / (1.f + 0.18f * (p.G - 1));                // GB/s per decode SM
+  const float g = kDecodeBytesPerCycle * mhz * 1e-3f / (1.f + 0.18f * (p.G - 1));  // GB/s per decode SM
   const float n_hbm = fmaxf(0.f, floorf(S - p.hbm_gbs / g));  // most chunk CTAs with decode at HBM rate
   if (T == 0.f) return static_cast<int>(B == 0.f ? S : n_hbm);
   if (B == 0.f) return static_cast<int>(S);
@@ -1591,6 +1604,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   griddep_wait();  // the prologue's item tables (and, through it, the append's q_rot and pages)
+  // CTA 0 times its own run in SM cycles and in ns: the SM clock, for the next call's cost model
+  const long long clk0 = clock64();
+  const uint64_t ns0 = globaltimer_ns();
   const int n_ch_items = p.hdr[H_NCH_ITEMS];
   const int n_dec_items = p.hdr[H_NDEC_ITEMS];
   __syncthreads();  // every thread holds the address before the phases reuse the memory
@@ -1627,6 +1643,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, ChCfg<D>::TMEM_COLS);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const uint64_t ns = globaltimer_ns() - ns0;
+    if (ns >= 20000)  // long enough for the timer's resolution
+      p.hdr[H_CLOCK_MHZ] = static_cast<int>(static_cast<double>(clock64() - clk0) * 1e3 / static_cast<double>(ns));
   }
 }
 
@@ -1732,6 +1753,32 @@ int num_sms() {
   return n;
 }
 
+// The cost model's device rates, looked up once per device: the rated SM
+// clock (MHz) and the HBM bandwidth (GB/s), nominal (memory clock x bus width,
+// double data rate) times the sustained copy share.
+std::atomic<float> g_sm_mhz[kMaxDevices], g_hbm_gbs[kMaxDevices];
+
+int device_rates(float* sm_mhz, float* hbm_gbs) {
+  const int dev = current_device();
+  if (dev < 0) return MS_ERR_CUDA;
+  float mhz = g_sm_mhz[dev].load(std::memory_order_relaxed);
+  float gbs = g_hbm_gbs[dev].load(std::memory_order_relaxed);
+  if (!(mhz > 0.f) || !(gbs > 0.f)) {
+    int clk_khz = 0, mem_khz = 0, bus_bits = 0;
+    if (cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&mem_khz, cudaDevAttrMemoryClockRate, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&bus_bits, cudaDevAttrGlobalMemoryBusWidth, dev) != cudaSuccess)
+      return MS_ERR_CUDA;
+    mhz = clk_khz > 0 ? clk_khz * 1e-3f : 2000.f;
+    gbs = mem_khz > 0 && bus_bits > 0 ? 2.f * mem_khz * 1e3f * (bus_bits / 8.f) * 1e-9f * kHbmCopyEfficiency : 6500.f;
+    g_sm_mhz[dev].store(mhz, std::memory_order_relaxed);
+    g_hbm_gbs[dev].store(gbs, std::memory_order_relaxed);
+  }
+  *sm_mhz = mhz;
+  *hbm_gbs = gbs;
+  return MS_OK;
+}
+
 // Raise `kernel`'s dynamic shared-memory limit on the current device once
 // (bit `slot` of the device's mask).
 template <typename Kernel>
@@ -1801,6 +1848,11 @@ extern "C" MS_API size_t ms_attention_workspace_size(int32_t max_rows, int32_t m
       (D != 64 && D != 128))
     return 0;
   return ws_layout(max_rows, max_tokens, max_context_total, H_q, H_kv, D).total;
+}
+
+extern "C" MS_API int ms_cost_model_rates(float* sm_mhz, float* hbm_gbs) {
+  if (sm_mhz == nullptr || hbm_gbs == nullptr) return MS_ERR_ARG;
+  return device_rates(sm_mhz, hbm_gbs);
 }
 
 extern "C" MS_API int ms_num_sms(void) {
@@ -1921,9 +1973,8 @@ int attention_setup(const void* q_rot, const void* k_cache, const void* v_cache,
   p.wait_limit_ns = stall_limit_ns > 0 ? static_cast<uint64_t>(stall_limit_ns) : 2000000000ull;
   p.scale_log2 = scale * 1.4426950408889634f;
 
-  p.chunk_tile_ns = kChunkTileNs;
-  p.decode_sm_gbs = kDecodeSmGBs;
-  p.hbm_gbs = kHbmGBs;
+  p.force_chunk_ctas = -1;
+  if (device_rates(&p.sm_mhz, &p.hbm_gbs) != MS_OK) return MS_ERR_CUDA;
   return MS_OK;
 }
 
@@ -1969,7 +2020,7 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
                    int32_t num_rows, int32_t num_tokens,
                    int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
                    void* out, void* workspace, size_t ws_bytes, ms_stream_t stream, bool clear_status,
-                   int64_t stall_limit_ns, bool* launched) {
+                   int64_t stall_limit_ns, bool* launched, int32_t force_chunk_ctas = -1) {
   *launched = false;
   AttnPlan L;
   bool empty = true;
@@ -1978,6 +2029,7 @@ int attention_call(const void* q_rot, const void* k_cache, const void* v_cache, 
                                  H_kv, D, page_size, scale, out, workspace, ws_bytes, clear_status, stall_limit_ns, &L,
                                  &empty);
   if (rc != MS_OK || empty) return rc;
+  L.p.force_chunk_ctas = force_chunk_ctas;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   *launched = true;  // from here on, kernels may be on the stream
   const int rp = launch_prologue(L.p, st);
@@ -2078,6 +2130,22 @@ extern "C" MS_API int ms_test_attention_stall(const void* q_rot, const void* k_c
   return attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens, block_tables,
                         nullptr, 0, bt_stride, num_rows, num_tokens, context_total, H_q, H_kv, D, page_size, scale, out,
                         workspace, ws_bytes, stream, false, wait_limit_ns, &launched);
+}
+
+extern "C" MS_API int ms_test_attention_split(const void* q_rot, const void* k_cache, const void* v_cache,
+                                              int32_t num_pages, const int32_t* cu_seqlens_q,
+                                              const int32_t* q_start_pos, const int32_t* context_lens,
+                                              const int32_t* block_tables, const int32_t* bt_offsets, int64_t bt_len,
+                                              int32_t bt_stride, int32_t num_rows, int32_t num_tokens,
+                                              int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D,
+                                              int32_t page_size, float scale, void* out, void* workspace,
+                                              size_t ws_bytes, int32_t chunk_ctas, ms_stream_t stream) {
+  if (chunk_ctas < 0) return MS_ERR_ARG;
+  bool launched = false;
+  return attention_call(q_rot, k_cache, v_cache, num_pages, cu_seqlens_q, q_start_pos, context_lens, block_tables,
+                        bt_offsets, bt_offsets != nullptr ? bt_len : 0, bt_offsets != nullptr ? 0 : bt_stride,
+                        num_rows, num_tokens, context_total, H_q, H_kv, D, page_size, scale, out, workspace, ws_bytes,
+                        stream, false, 0, &launched, chunk_ctas);
 }
 
 extern "C" MS_API int ms_read_status(int32_t* dev_status, ms_stream_t stream, int32_t* host_status) {

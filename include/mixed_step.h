@@ -221,8 +221,11 @@ MS_API int ms_kv_append_rope(const void* q, const void* k, const void* v,
 /* ms_attention_workspace_size -- bytes of device workspace that
  * ms_mixed_step_attention needs for steps of at most max_rows rows,
  * max_tokens new tokens and max_context_total = sum over rows of context_lens.
- * The first 256 bytes of a workspace hold its status word and queue counters:
- * zero the whole workspace once before its first use. */
+ * The first 256 bytes of a workspace hold its header, 64 int32 words: word 0
+ * the status word, then queue counters and the step's plan (word 9: how many
+ * CTAs started on chunk work) and, kept across calls, word 10: the SM clock
+ * in MHz the last call measured, which the next call's SM-split cost model
+ * uses.  Zero the whole workspace once before its first use. */
 MS_API size_t ms_attention_workspace_size(int32_t max_rows, int32_t max_tokens, int64_t max_context_total,
                                           int32_t H_q, int32_t H_kv, int32_t D);
 
@@ -362,6 +365,23 @@ MS_API int ms_test_attention_stall(const void* q_rot, const void* k_cache, const
                                    int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, float scale,
                                    void* out, void* workspace, size_t ws_bytes, int64_t wait_limit_ns,
                                    ms_stream_t stream);
+
+/* ms_test_attention_split -- test hook: ms_mixed_step_attention (bt_offsets ==
+ * NULL, block_tables padded with bt_stride) or ms_mixed_step_attention_ragged
+ * (bt_offsets given, block_tables = bt_pages with bt_len entries) with the
+ * starting split of the SMs forced: chunk_ctas CTAs (clamped to the SM count)
+ * start on chunk work, the others on decode items.  CTAs still move to the
+ * other queue when their own runs dry, so the outputs equal the ordinary
+ * call's; only the timing changes.  The pages have no counterpart: the hook
+ * lets a test sweep the split against the cost model's choice (workspace
+ * header word 9).  Errors: MS_ERR_ARG (also for chunk_ctas < 0), MS_ERR_CUDA. */
+MS_API int ms_test_attention_split(const void* q_rot, const void* k_cache, const void* v_cache, int32_t num_pages,
+                                   const int32_t* cu_seqlens_q, const int32_t* q_start_pos,
+                                   const int32_t* context_lens, const int32_t* block_tables,
+                                   const int32_t* bt_offsets, int64_t bt_len, int32_t bt_stride, int32_t num_rows,
+                                   int32_t num_tokens, int64_t context_total, int32_t H_q, int32_t H_kv, int32_t D,
+                                   int32_t page_size, float scale, void* out, void* workspace, size_t ws_bytes,
+                                   int32_t chunk_ctas, ms_stream_t stream);
 
 /* ---- Multi-round engine (host) ------------------------------------------
  * A page pool with full-input admission and a plan/commit round driver over
@@ -534,6 +554,14 @@ MS_API int ms_graph_read_status(ms_step_graph* g, ms_stream_t stream, int32_t* h
  * clears it.  Returns MS_OK, MS_ERR_DEVICE when the word was non-zero, or
  * MS_ERR_ARG / MS_ERR_CUDA. */
 MS_API int ms_read_status(int32_t* dev_status, ms_stream_t stream, int32_t* host_status);
+
+/* ms_cost_model_rates -- host: the current device's rates behind the SM
+ * split of the attention call, before any call has measured the SM clock:
+ * the rated SM clock in MHz, and the HBM bandwidth in GB/s taken as the
+ * nominal rate (memory clock x bus width, double data rate) times 0.80, the
+ * sustained share a device-to-device copy reaches.
+ * Errors: MS_ERR_ARG (NULL output), MS_ERR_CUDA. */
+MS_API int ms_cost_model_rates(float* sm_mhz, float* hbm_gbs);
 
 /* ms_num_sms -- SM count of the current device (the persistent grid size), or
  * a negative MS_ERR_* code. */
