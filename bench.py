@@ -99,18 +99,19 @@ def describe(name: str, wls) -> str:
 
 
 def captured_traffic(config: str):
-    """DRAM bytes of one captured attention launch, if the kernel source still matches the capture."""
+    """DRAM bytes of one captured batch (the append launch and the attention kernel), if every
+    kernel source the capture lists still matches it."""
     import hashlib
     path = os.path.join(ROOT, "profiles", f"attention_kernel_{config}.traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            cur = hashlib.sha256(f.read()).hexdigest()
-    except (OSError, KeyError, ValueError):
+        for src, sha in rec["sources"].items():
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != sha:
+                    return None  # a kernel changed since the counters were taken
+    except (OSError, KeyError, ValueError, AttributeError):
         return None
-    if cur != rec.get("source_sha256"):
-        return None  # the kernel changed since the counters were taken
     return rec
 
 

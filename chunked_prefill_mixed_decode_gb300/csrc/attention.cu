@@ -60,6 +60,7 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kChunkThreads = 32 * (4 + kSoftmaxWarps);  // warp 0 TMA + queue, 2-9 softmax, 1/10/11 MMA
 constexpr int kSortLimit = 2048;    // rows sorted longest-first up to this count
 constexpr int kMaxRows = 8192;      // rows of one step
+constexpr int kMaxTokens = 1 << 21;  // tokens of one step (a chunk row's Q-tile pairs fit in 16 bits)
 // Cost model that splits the SMs between the two row kinds at the start of a
 // step (CTAs then move to whichever queue still has work): the SM time of one
 // 128x128 chunk tile, and the decode bandwidth one SM sustains, capped by HBM.
@@ -109,7 +110,7 @@ struct AttnParams {
   int32_t* ch_rows;
   int2* dec_items;  // per decode split (items / H_kv entries): (decode row index, split within the row)
   int32_t* dec_cnt; // per (decode row, KV head): splits finished, for the last one to merge
-  int2* ch_items;   // per Q-tile pair of a chunk row (items / H_kv entries): (chunk row index, pair index)
+  int2* ch_items;   // per chunk item: (chunk row index, KV head << 16 | Q-tile pair counted from the last)
   int64_t max_dec_items, max_ch_items;  // capacities in items (entries x H_kv)
   float* part_ml;
   float* part_acc;
@@ -125,6 +126,7 @@ struct AttnParams {
   int32_t force_chunk_ctas;  // test hook: CTAs that start on chunk work (-1: the cost model decides)
   float sm_mhz;              // cost model: the SM clock when no call has measured it yet,
   float hbm_gbs;             // and the HBM bandwidth that caps decode
+  float l2_bytes;            // L2 capacity (orders the chunk items)
   float scale_log2;
 };
 
@@ -198,13 +200,28 @@ __device__ __forceinline__ uint32_t order_key(float cost, int pos) {
 // prefix in queue order.
 __host__ __device__ constexpr int prologue_words(int S) { return 5 * ((S + 3) & ~3) + 16; }
 
-// How many CTAs of the main kernel start on chunk tiles.  Chunk time falls as
-// 1/n with n chunk CTAs, in whole items; decode time is bytes over the
-// bandwidth of the other SMs, capped by HBM.  Take the best split near the
-// balance point, or, while decode stays HBM-bound, as many chunk CTAs as keep
-// it so.  Called by one whole warp; the candidate counts go one per lane.
-__device__ int chunk_cta_split(const AttnParams& p, float tiles, float dec_pages, int n_items, int lane) {
-  if (p.force_chunk_ctas >= 0) return min(p.force_chunk_ctas, p.num_sms);
+// How many CTAs of the main kernel start on chunk tiles, and which side bounds
+// the step.  Chunk time falls as 1/n with n chunk CTAs, in whole items; decode
+// time is bytes over the bandwidth of the other SMs, capped by HBM.  Take the
+// best split near the balance point, or, while decode stays HBM-bound, as many
+// chunk CTAs as keep it so.  Called by one whole warp; the candidate counts go
+// one per lane.
+//
+// It also orders the chunk items.  Longest first by default.  But when decode
+// rows stream through L2 beside chunk rows whose K/V (all KV heads) would fill
+// more than half of it, the items run KV head by KV head instead: the CTAs on
+// chunk work at any time then share one head's K/V tiles in L2, where with
+// every head in flight each head's prefix would be pulled from DRAM again and
+// again (measured: 7 % more DRAM traffic than the algorithmic bytes on a
+// 32K-key chunk next to 512 decodes, 6 % on 40 heads of 4K keys; on 8 heads
+// of 10K keys, where the chunk rows bound the step, longest-first is faster).
+struct SmSplit {
+  int chunk_ctas;
+  bool head_major;
+};
+
+__device__ SmSplit chunk_cta_split(const AttnParams& p, float tiles, float dec_pages, int n_items,
+                                   float chunk_keys, int lane) {
   // the SM clock of the previous call on this workspace, else the device's rated clock
   const int measured = p.hdr[H_CLOCK_MHZ];
   const float mhz = measured >= 200 && measured <= 5000 ? static_cast<float>(measured) : p.sm_mhz;
@@ -213,38 +230,55 @@ __device__ int chunk_cta_split(const AttnParams& p, float tiles, float dec_pages
   const float B = dec_pages * p.H_kv * kPage * p.D * 4.f;                     // decode bytes
   const float g = kDecodeBytesPerCycle * mhz * 1e-3f / (1.f + 0.18f * (p.G - 1));  // GB/s per decode SM
   const float n_hbm = fmaxf(0.f, floorf(S - p.hbm_gbs / g));  // most chunk CTAs with decode at HBM rate
-  if (T == 0.f) return static_cast<int>(B == 0.f ? S : n_hbm);
-  if (B == 0.f) return static_cast<int>(S);
-  if (T * p.hbm_gbs <= B * n_hbm) return static_cast<int>(n_hbm);  // chunk done within the HBM-bound decode time
-  // Balance point, then the nearby CTA count that minimizes the step: chunk work
-  // comes in whole items, so n chunk CTAs need ceil(items / n) rounds of about
-  // T / items each; decode runs on the other CTAs, capped by HBM.  Ties go to
-  // the smallest count.
-  const float n0 = fminf(S - 1.f, fmaxf(1.f, rintf(__fdividef(T * g * S, B + T * g))));
-  const int n_it = max(n_items, 1);
-  const float t_item = __fdividef(T, static_cast<float>(n_it));
-  const int k_lo = max(1, static_cast<int>(n0) - 16), k_hi = min(static_cast<int>(S) - 1, static_cast<int>(n0) + 16);
-  float best = 3.0e38f;
-  int bk = static_cast<int>(n0);
-  for (int k = k_lo + lane; k <= k_hi; k += 32) {
-    const float tc = static_cast<float>((n_it + k - 1) / k) * t_item;
-    const float td = __fdividef(B, fminf((S - k) * g, p.hbm_gbs));
-    const float tt = fmaxf(tc, td);
-    if (tt < best) {
-      best = tt;
-      bk = k;
+  SmSplit r;
+  r.head_major = B > 0.f && chunk_keys * p.H_kv * p.D * 4.f > 0.5f * p.l2_bytes;
+  if (T == 0.f) {
+    r.chunk_ctas = static_cast<int>(B == 0.f ? S : n_hbm);
+  } else if (B == 0.f) {
+    r.chunk_ctas = static_cast<int>(S);
+  } else if (T * p.hbm_gbs <= B * n_hbm) {  // chunk done within the HBM-bound decode time
+    r.chunk_ctas = static_cast<int>(n_hbm);
+  } else {
+    // Balance point, then the nearby CTA count that minimizes the step: chunk work
+    // comes in whole items, so n chunk CTAs need ceil(items / n) rounds of about
+    // T / items each; decode runs on the other CTAs, capped by HBM.  Ties go to
+    // the smallest count.
+    const float n0 = fminf(S - 1.f, fmaxf(1.f, rintf(__fdividef(T * g * S, B + T * g))));
+    const int n_it = max(n_items, 1);
+    const float t_item = __fdividef(T, static_cast<float>(n_it));
+    const int k_lo = max(1, static_cast<int>(n0) - 16), k_hi = min(static_cast<int>(S) - 1, static_cast<int>(n0) + 16);
+    float best = 3.0e38f;
+    int bk = static_cast<int>(n0);
+    for (int k = k_lo + lane; k <= k_hi; k += 32) {
+      const float tc = static_cast<float>((n_it + k - 1) / k) * t_item;
+      const float td = __fdividef(B, fminf((S - k) * g, p.hbm_gbs));
+      const float tt = fmaxf(tc, td);
+      if (tt < best) {
+        best = tt;
+        bk = k;
+      }
     }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-    const int ok = __shfl_xor_sync(0xffffffffu, bk, o);
-    if (ob < best || (ob == best && ok < bk)) {
-      best = ob;
-      bk = ok;
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      if (ob < best || (ob == best && ok < bk)) {
+        best = ob;
+        bk = ok;
+      }
     }
+    r.chunk_ctas = bk;
   }
-  return bk;
+  if (p.force_chunk_ctas >= 0) r.chunk_ctas = min(p.force_chunk_ctas, p.num_sms);
+  return r;
+}
+
+// Table entry of item i of a chunk row with np Q-tile pairs: (KV head) << 16 |
+// (pair counted from the last), KV head by KV head or longest pair first.
+__device__ __forceinline__ int chunk_entry(int i, int np, int H_kv, bool head_major) {
+  const int hk = head_major ? i / np : i % H_kv;
+  const int e = head_major ? i - hk * np : i / H_kv;
+  return (hk << 16) | e;
 }
 
 // Decode split size: about 8 items per decode worker warp, clamped; at least 32
@@ -346,6 +380,7 @@ __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
   const bool dec_over = n_dec_items > p.max_dec_items || static_cast<int64_t>(dec_tot) * p.H_q > p.max_partials;
   const bool ch_over = n_ch_items > p.max_ch_items;
   const int64_t tiles = warp_sum64(is_ch ? static_cast<int64_t>(chunk_tiles(c, d, tpt)) * p.H_kv : 0);
+  const int64_t chunk_keys = warp_sum64(is_ch ? ctx : 0);
   if (is_dec) {
     p.dec_rows[rank] = lane;
     p.dec_part_base[rank] = static_cast<int32_t>(static_cast<int64_t>(before) * p.H_q);
@@ -355,13 +390,15 @@ __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
       for (int h = 0; h < p.H_kv; ++h) p.dec_cnt[rank * p.H_kv + h] = 0;
     }
   }
+  const SmSplit sp = chunk_cta_split(p, static_cast<float>(tiles), static_cast<float>(dec_pages),
+                                     ch_over ? 0 : static_cast<int>(n_ch_items), static_cast<float>(chunk_keys), lane);
   if (is_ch) {
     p.ch_rows[rank] = lane;
     if (!ch_over)
-      for (int i = 0; i < items; ++i) p.ch_items[before - dec_tot + i] = make_int2(rank, i);
+      for (int i = 0; i < items * p.H_kv; ++i)
+        p.ch_items[static_cast<int64_t>(before - dec_tot) * p.H_kv + i] =
+            make_int2(rank, chunk_entry(i, items, p.H_kv, sp.head_major));
   }
-  const int n_first = chunk_cta_split(p, static_cast<float>(tiles), static_cast<float>(dec_pages),
-                                      ch_over ? 0 : static_cast<int>(n_ch_items), lane);
   if (lane == 0) {
     hdr[H_NDEC] = dec_over ? 0 : n_dec;
     hdr[H_NDEC_ITEMS] = dec_over ? 0 : static_cast<int32_t>(n_dec_items);
@@ -372,7 +409,7 @@ __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
     hdr[H_DEC_CTR] = 0;
     hdr[H_CH_CTR] = 0;
     hdr[H_SPLIT] = split;
-    hdr[H_CHUNK_CTAS] = n_first;
+    hdr[H_CHUNK_CTAS] = sp.chunk_ctas;
   }
 }
 
@@ -389,9 +426,10 @@ __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
 __device__ __forceinline__ void prologue_body(const AttnParams& p) {
   extern __shared__ __align__(16) int32_t psm[];
   __shared__ int s_warp[32];
-  __shared__ long long s_sum[2][32];
+  __shared__ long long s_sum[3][32];
   __shared__ unsigned s_cnt[2][32];
   __shared__ unsigned long long s_tiles;
+  __shared__ SmSplit s_split;
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
   const int S = p.num_rows;  // at most kMaxRows (checked by the host, which sizes psm by it)
   int32_t* hdr = p.hdr;
@@ -410,7 +448,7 @@ __device__ __forceinline__ void prologue_body(const AttnParams& p) {
   }
   if (tid == 0) s_tiles = 0;
   // 1. load and validate the rows; count decodes, chunks, context and decode pages
-  int64_t my_ctx = 0, my_pages = 0;
+  int64_t my_ctx = 0, my_pages = 0, my_ch_keys = 0;
   unsigned my_dec = 0, my_ch = 0;
   int my_bad = 0;
   for (int s = tid; s < S; s += nt) {
@@ -432,24 +470,28 @@ __device__ __forceinline__ void prologue_body(const AttnParams& p) {
       my_dec += d == 1;
       my_ch += d > 1;
       if (d == 1) my_pages += (ctx + kPage - 1) / kPage;
+      if (d > 1) my_ch_keys += ctx;
     }
   }
   my_ctx = warp_sum64(my_ctx);
   my_pages = warp_sum64(my_pages);
+  my_ch_keys = warp_sum64(my_ch_keys);
   my_dec = __reduce_add_sync(0xffffffffu, my_dec);
   my_ch = __reduce_add_sync(0xffffffffu, my_ch);
   if (lane == 0) {
     s_sum[0][warp] = my_ctx;
     s_sum[1][warp] = my_pages;
+    s_sum[2][warp] = my_ch_keys;
     s_cnt[0][warp] = my_dec;
     s_cnt[1][warp] = my_ch;
   }
   const int bad = __syncthreads_or(my_bad);
-  int64_t ctx_sum = 0, dec_pages = 0;
+  int64_t ctx_sum = 0, dec_pages = 0, chunk_keys = 0;
   int n_dec = 0, n_ch = 0;
   for (int j = 0; j < nw; ++j) {
     ctx_sum += s_sum[0][j];
     dec_pages += s_sum[1][j];
+    chunk_keys += s_sum[2][j];
     n_dec += static_cast<int>(s_cnt[0][j]);
     n_ch += static_cast<int>(s_cnt[1][j]);
   }
@@ -536,16 +578,28 @@ __device__ __forceinline__ void prologue_body(const AttnParams& p) {
   const int64_t n_ch_items = static_cast<int64_t>(ch_tot) * p.H_kv;
   const bool dec_over = n_dec_items > p.max_dec_items || static_cast<int64_t>(dec_tot) * p.H_q > p.max_partials;
   const bool ch_over = n_ch_items > p.max_ch_items;
-  // 7. item tables, a thread per row: entry pref[q] + i -> (row k, its item i),
-  // one entry per row item (a work item is an entry and a KV head); and the
-  // split counters of every (decode row, KV head), zeroed 16 bytes at a time
-  for (int q = tid; q < n_tot; q += nt) {
-    const bool ch = q >= n_dec;
-    if (ch ? ch_over : dec_over) continue;
-    const int k = ch ? q - n_dec : q;
+  // 7. item tables.  Decode rows, a thread per row: entry pref[q] + i -> (row
+  // k, split i), one entry per split (a work item is an entry and a KV head).
+  // Then the SM split, which also orders the chunk items; chunk rows, a warp
+  // per row: one entry per item, (row k, KV head and Q-tile pair).  Then the
+  // split counters of every (decode row, KV head), zeroed 16 bytes at a time.
+  for (int q = tid; q < n_dec && !dec_over; q += nt) {
     const int cnt = pref[q + 1] - pref[q];
-    int2* out = (ch ? p.ch_items : p.dec_items) + (pref[q] - (ch ? dec_tot : 0));
-    for (int i = 0; i < cnt; ++i) out[i] = make_int2(k, i);
+    int2* out = p.dec_items + pref[q];
+    for (int i = 0; i < cnt; ++i) out[i] = make_int2(q, i);
+  }
+  if (warp == 0) {
+    const SmSplit sp = chunk_cta_split(p, static_cast<float>(s_tiles), static_cast<float>(dec_pages),
+                                       ch_over ? 0 : static_cast<int>(n_ch_items), static_cast<float>(chunk_keys),
+                                       lane);
+    if (lane == 0) s_split = sp;
+  }
+  __syncthreads();
+  for (int q = n_dec + warp; q < n_tot && !ch_over; q += nw) {
+    const int np = pref[q + 1] - pref[q];
+    int2* out = p.ch_items + static_cast<int64_t>(pref[q] - dec_tot) * p.H_kv;
+    for (int i = lane; i < np * p.H_kv; i += 32)
+      out[i] = make_int2(q - n_dec, chunk_entry(i, np, p.H_kv, s_split.head_major));
   }
   if (!dec_over) {
     const int n_cnt = n_dec * p.H_kv;  // the counters start 16-byte aligned in the workspace
@@ -554,8 +608,6 @@ __device__ __forceinline__ void prologue_body(const AttnParams& p) {
   }
   // 8. the header the main kernel starts from
   if (warp == 0) {
-    const int n_first = chunk_cta_split(p, static_cast<float>(s_tiles), static_cast<float>(dec_pages),
-                                        ch_over ? 0 : static_cast<int>(n_ch_items), lane);
     if (lane == 0) {
       hdr[H_NDEC] = dec_over ? 0 : n_dec;
       hdr[H_NDEC_ITEMS] = dec_over ? 0 : static_cast<int32_t>(n_dec_items);
@@ -566,7 +618,7 @@ __device__ __forceinline__ void prologue_body(const AttnParams& p) {
       hdr[H_DEC_CTR] = 0;
       hdr[H_CH_CTR] = 0;
       hdr[H_SPLIT] = static_cast<int32_t>(split);
-      hdr[H_CHUNK_CTAS] = n_first;
+      hdr[H_CHUNK_CTAS] = s_split.chunk_ctas;
     }
   }
 }
@@ -1141,9 +1193,7 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
       ChItem it;
       it.row = -1;
       if (item < n_items) {
-        // items run (row item, KV head) with the head fastest; the table has one entry per row item
-        const int e = item / p.H_kv;
-        const int2 kl = __ldg(p.ch_items + e);  // (chunk row index, Q-tile pair counted from the last)
+        const int2 kl = __ldg(p.ch_items + item);  // (chunk row index, KV head << 16 | pair from the last)
         const int k = kl.x;
         it.row = __ldg(p.ch_rows + k);
         it.tb = __ldg(p.cu + it.row);
@@ -1151,8 +1201,10 @@ __device__ __noinline__ void chunk_phase(const CUtensorMap* tm_q_p, const CUtens
         it.c = __ldg(p.q_start + it.row);
         const int n_qt = (d + TPT - 1) / TPT;
         const int n_pair = (n_qt + 1) >> 1;
-        const int pair = n_pair - 1 - kl.y;  // later tiles see more keys: run them first
-        it.hk = item - e * p.H_kv;
+        // the prologue ordered the row's items (KV head by KV head, or longest pair
+        // first); later Q-tile pairs see more keys
+        it.hk = kl.y >> 16;
+        const int pair = n_pair - 1 - (kl.y & 0xffff);
         it.n_kt = 0;
         for (int t = 0; t < 2; ++t) {
           const int qt = 2 * pair + t;
@@ -1689,10 +1741,10 @@ WsLayout ws_layout(int64_t max_rows, int64_t max_tokens, int64_t max_context_tot
   const int64_t G = H_q / (H_kv > 0 ? H_kv : 1);
   w.max_dec_items = H_kv * max_splits;
   w.max_ch_items = H_kv * (cdiv64(max_tokens * G, 128) + max_rows);
-  w.dec_items = off;  // one entry per split, per Q-tile pair: the KV head is not in the tables
+  w.dec_items = off;  // one entry per split: the KV head is not in the table
   off = align_up(off + (w.max_dec_items / H_kv) * 8, 256);
-  w.ch_items = off;
-  off = align_up(off + (w.max_ch_items / H_kv) * 8, 256);
+  w.ch_items = off;  // one entry per chunk item
+  off = align_up(off + w.max_ch_items * 8, 256);
   w.max_partials = H_q * max_splits;
   w.part_ml = off;
   off = align_up(off + w.max_partials * 2 * 4, 256);
@@ -1756,26 +1808,31 @@ int num_sms() {
 // The cost model's device rates, looked up once per device: the rated SM
 // clock (MHz) and the HBM bandwidth (GB/s), nominal (memory clock x bus width,
 // double data rate) times the sustained copy share.
-std::atomic<float> g_sm_mhz[kMaxDevices], g_hbm_gbs[kMaxDevices];
+std::atomic<float> g_sm_mhz[kMaxDevices], g_hbm_gbs[kMaxDevices], g_l2_bytes[kMaxDevices];
 
-int device_rates(float* sm_mhz, float* hbm_gbs) {
+int device_rates(float* sm_mhz, float* hbm_gbs, float* l2_bytes) {
   const int dev = current_device();
   if (dev < 0) return MS_ERR_CUDA;
   float mhz = g_sm_mhz[dev].load(std::memory_order_relaxed);
   float gbs = g_hbm_gbs[dev].load(std::memory_order_relaxed);
-  if (!(mhz > 0.f) || !(gbs > 0.f)) {
-    int clk_khz = 0, mem_khz = 0, bus_bits = 0;
+  float l2 = g_l2_bytes[dev].load(std::memory_order_relaxed);
+  if (!(mhz > 0.f) || !(gbs > 0.f) || !(l2 > 0.f)) {
+    int clk_khz = 0, mem_khz = 0, bus_bits = 0, l2_b = 0;
     if (cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&mem_khz, cudaDevAttrMemoryClockRate, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&bus_bits, cudaDevAttrGlobalMemoryBusWidth, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&bus_bits, cudaDevAttrGlobalMemoryBusWidth, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2_b, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
       return MS_ERR_CUDA;
     mhz = clk_khz > 0 ? clk_khz * 1e-3f : 2000.f;
     gbs = mem_khz > 0 && bus_bits > 0 ? 2.f * mem_khz * 1e3f * (bus_bits / 8.f) * 1e-9f * kHbmCopyEfficiency : 6500.f;
+    l2 = l2_b > 0 ? static_cast<float>(l2_b) : 64.f * (1 << 20);
     g_sm_mhz[dev].store(mhz, std::memory_order_relaxed);
     g_hbm_gbs[dev].store(gbs, std::memory_order_relaxed);
+    g_l2_bytes[dev].store(l2, std::memory_order_relaxed);
   }
   *sm_mhz = mhz;
   *hbm_gbs = gbs;
+  *l2_bytes = l2;
   return MS_OK;
 }
 
@@ -1852,7 +1909,8 @@ extern "C" MS_API size_t ms_attention_workspace_size(int32_t max_rows, int32_t m
 
 extern "C" MS_API int ms_cost_model_rates(float* sm_mhz, float* hbm_gbs) {
   if (sm_mhz == nullptr || hbm_gbs == nullptr) return MS_ERR_ARG;
-  return device_rates(sm_mhz, hbm_gbs);
+  float l2 = 0.f;
+  return device_rates(sm_mhz, hbm_gbs, &l2);
 }
 
 extern "C" MS_API int ms_num_sms(void) {
@@ -1896,7 +1954,7 @@ int attention_setup(const void* q_rot, const void* k_cache, const void* v_cache,
   if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return MS_ERR_ARG;
-  if (num_rows > kMaxRows) return MS_ERR_ARG;
+  if (num_rows > kMaxRows || num_tokens > kMaxTokens) return MS_ERR_ARG;
   const WsLayout w = ws_layout(num_rows, num_tokens, context_total, H_q, H_kv, D);
   if (ws_bytes < w.total) return MS_ERR_ARG;
   const int sms = num_sms();
@@ -1974,7 +2032,7 @@ int attention_setup(const void* q_rot, const void* k_cache, const void* v_cache,
   p.scale_log2 = scale * 1.4426950408889634f;
 
   p.force_chunk_ctas = -1;
-  if (device_rates(&p.sm_mhz, &p.hbm_gbs) != MS_OK) return MS_ERR_CUDA;
+  if (device_rates(&p.sm_mhz, &p.hbm_gbs, &p.l2_bytes) != MS_OK) return MS_ERR_CUDA;
   return MS_OK;
 }
 

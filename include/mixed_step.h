@@ -253,7 +253,8 @@ MS_API size_t ms_attention_workspace_size(int32_t max_rows, int32_t max_tokens, 
  *                this step's sizes, zeroed before first use; its first int32 is
  *                the status word (read it with ms_read_status)
  * Out-of-range page ids are not read (MS_STATUS_BAD_PAGE).  A step holds at
- * most 8192 rows.  Steps that share a workspace must not overlap on the GPU.
+ * most 8192 rows and 2^21 tokens.  Steps that share a workspace must not
+ * overlap on the GPU.
  * Errors: MS_ERR_ARG, MS_ERR_CUDA. */
 MS_API int ms_mixed_step_attention(const void* q_rot, const void* k_cache, const void* v_cache,
                                    int32_t num_pages,

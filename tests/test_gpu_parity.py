@@ -237,6 +237,24 @@ def test_more_rows_than_a_step_holds_is_refused(env):
     assert e.value.code == ms.MS_ERR_ARG
 
 
+def test_more_tokens_than_a_step_holds_is_refused(env):
+    """2^21 + 1 tokens in one chunk row: the call returns MS_ERR_ARG before any launch."""
+    torch, ms, step = env
+    T = (1 << 21) + 1
+    meta = {"cu_seqlens_q": np.array([0, T], np.int32), "q_start_pos": np.zeros(1, np.int32),
+            "context_lens": np.array([T], np.int32), "positions": np.zeros(1, np.int32),
+            "slot_mapping": np.zeros(1, np.int32), "block_tables": np.zeros((1, 1), np.int32),
+            "num_rows": 1, "num_tokens": T, "num_decodes": 0, "bt_stride": 1}
+    b = step.to_device(meta, "cuda")
+    q = torch.zeros((T, 1, 64), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((1, 1, 16, 64), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ms.MixedStepError) as e:
+        ms.mixed_step_attention(q, kc, kc, b.cu_seqlens_q, b.q_start_pos, b.context_lens, b.block_tables, T,
+                                torch.empty_like(q), ws)
+    assert e.value.code == ms.MS_ERR_ARG
+
+
 def test_chunked_prefill_matches_full_prefill_on_gpu(env):
     """zwjcode section 07: chunks [2, 3, 1] of a 6-token prompt -- and a 300-token prompt as
     [100, 37, 163] -- give the same outputs as one full prefill (same pool, same inputs)."""
