@@ -93,17 +93,27 @@ enum {
 };
 
 struct AttnParams {
-  const bf16* q_rot;
-  const bf16* k_cache;
-  const bf16* v_cache;
+  // Read by the prologue, which runs once per step from cold caches: kept
+  // together at the front so that they span the fewest constant-cache lines.
   const int32_t* cu;
   const int32_t* q_start;
   const int32_t* ctx_lens;
-  const int32_t* bt;      // padded rows of bt_stride entries, or (bt_off given) every row's pages back to back
   const int32_t* bt_off;  // ragged block table: row s's pages at bt[bt_off[s] .. bt_off[s + 1]); else nullptr
-  int64_t bt_len;         // entries of bt
-  bf16* out;
   int32_t* hdr;
+  int64_t bt_len;         // entries of bt
+  int64_t context_total;
+  int64_t max_dec_items, max_ch_items;  // capacities in items (entries x H_kv)
+  int64_t max_partials;
+  int32_t bt_stride, num_rows, num_tokens, num_pages;
+  int32_t H_q, H_kv, D, G;
+  int32_t dec_workers;       // decode worker warps in the grid
+  int32_t num_sms;
+  int32_t clear_status;      // the prologue zeroes the status word first (scratch owned by the library)
+  int32_t force_chunk_ctas;  // test hook: CTAs that start on chunk work (-1: the cost model decides)
+  float sm_mhz;              // cost model: the SM clock when no call has measured it yet,
+  float hbm_gbs;             // and the HBM bandwidth that caps decode
+  float l2_bytes;            // L2 capacity (orders the chunk items)
+  float scale_log2;
   int32_t* dec_rows;
   int32_t* dec_part_base;
   int32_t* dec_nsplit;
@@ -111,23 +121,16 @@ struct AttnParams {
   int2* dec_items;  // per decode split (items / H_kv entries): (decode row index, split within the row)
   int32_t* dec_cnt; // per (decode row, KV head): splits finished, for the last one to merge
   int2* ch_items;   // per chunk item: (chunk row index, KV head << 16 | Q-tile pair counted from the last)
-  int64_t max_dec_items, max_ch_items;  // capacities in items (entries x H_kv)
+  // the attention kernel's alone
+  const bf16* q_rot;
+  const bf16* k_cache;
+  const bf16* v_cache;
+  const int32_t* bt;      // padded rows of bt_stride entries, or (bt_off given) every row's pages back to back
+  bf16* out;
   float* part_ml;
   float* part_acc;
-  int64_t max_partials;
-  int64_t context_total;
-  int32_t bt_stride, num_rows, num_tokens, num_pages;
-  int32_t H_q, H_kv, D, G;
-  int32_t dec_workers;  // decode worker warps in the grid
-  int32_t num_sms;
-  int32_t clear_status;  // the prologue zeroes the status word first (scratch owned by the library)
-  int32_t test_stall;    // test hook: chunk-phase producers publish no work item (0 in every real call)
   uint64_t wait_limit_ns;  // bound of every chunk-phase wait
-  int32_t force_chunk_ctas;  // test hook: CTAs that start on chunk work (-1: the cost model decides)
-  float sm_mhz;              // cost model: the SM clock when no call has measured it yet,
-  float hbm_gbs;             // and the HBM bandwidth that caps decode
-  float l2_bytes;            // L2 capacity (orders the chunk items)
-  float scale_log2;
+  int32_t test_stall;      // test hook: chunk-phase producers publish no work item (0 in every real call)
 };
 
 __host__ __device__ inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -164,6 +167,13 @@ __device__ __forceinline__ int block_scan(int v, int* s_warp, int& total) {
   __syncthreads();  // s_warp is free again
   total = tot;
   return before + x - v;
+}
+
+// warp sum of values in [0, 2^31): two 32-bit reductions of the 16-bit halves
+__device__ __forceinline__ int64_t warp_sum31(int v) {
+  const unsigned lo = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(v) & 0xffffu);
+  const unsigned hi = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(v) >> 16);
+  return (static_cast<int64_t>(hi) << 16) + lo;
 }
 
 __device__ __forceinline__ int64_t warp_sum64(int64_t v) {
@@ -221,9 +231,9 @@ struct SmSplit {
 };
 
 __device__ SmSplit chunk_cta_split(const AttnParams& p, float tiles, float dec_pages, int n_items,
-                                   float chunk_keys, int lane) {
-  // the SM clock of the previous call on this workspace, else the device's rated clock
-  const int measured = p.hdr[H_CLOCK_MHZ];
+                                   int n_dec_items, float chunk_keys, int measured, int lane) {
+  // the SM clock of the previous call on this workspace (header word H_CLOCK_MHZ, read
+  // by the caller early), else the device's rated clock
   const float mhz = measured >= 200 && measured <= 5000 ? static_cast<float>(measured) : p.sm_mhz;
   const float S = static_cast<float>(p.num_sms);
   const float T = tiles * __fdividef(kChunkTileCycles * 1000.f, mhz);         // SM-ns of chunk work
@@ -232,7 +242,12 @@ __device__ SmSplit chunk_cta_split(const AttnParams& p, float tiles, float dec_p
   const float n_hbm = fmaxf(0.f, floorf(S - p.hbm_gbs / g));  // most chunk CTAs with decode at HBM rate
   SmSplit r;
   r.head_major = B > 0.f && chunk_keys * p.H_kv * p.D * 4.f > 0.5f * p.l2_bytes;
-  if (T == 0.f) {
+  // a step whose chunk items and decode items all start at once: a CTA per chunk item
+  const int dec_ctas = static_cast<int>((static_cast<int64_t>(n_dec_items) * p.num_sms + p.dec_workers - 1) /
+                                        p.dec_workers);
+  if (n_items + dec_ctas <= p.num_sms) {
+    r.chunk_ctas = n_items;
+  } else if (T == 0.f) {
     r.chunk_ctas = static_cast<int>(B == 0.f ? S : n_hbm);
   } else if (B == 0.f) {
     r.chunk_ctas = static_cast<int>(S);
@@ -308,14 +323,15 @@ __device__ __forceinline__ void header_bad_meta(int32_t* hdr) {
 __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
   const int lane = threadIdx.x, S = p.num_rows;
   int32_t* hdr = p.hdr;
+  const int measured_mhz = hdr[H_CLOCK_MHZ];  // loaded beside the row metadata
   int d = 0, c = 0, ctx = 0;
   bool ok = true;
   if (lane < S) {
     const int32_t a = p.cu[lane], b = p.cu[lane + 1];
-    d = b - a;
+    d = static_cast<int32_t>(static_cast<uint32_t>(b) - static_cast<uint32_t>(a));  // checked below
     c = p.q_start[lane];
     ctx = p.ctx_lens[lane];
-    ok = a >= 0 && b <= p.num_tokens && d >= 0 && c >= 0 && ctx == c + d;
+    ok = a >= 0 && b >= a && b <= p.num_tokens && c >= 0 && static_cast<int64_t>(ctx) == static_cast<int64_t>(c) + d;
     if (p.bt_off != nullptr) {
       const int64_t o0 = p.bt_off[lane], o1 = p.bt_off[lane + 1];
       ok = ok && o0 >= 0 && o1 <= p.bt_len && cdiv64(ctx, kPage) <= o1 - o0;
@@ -325,13 +341,13 @@ __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
     if (!ok) d = ctx = 0;
   }
   const bool bad = __any_sync(0xffffffffu, !ok);
-  const int64_t ctx_sum = warp_sum64(ctx);
+  const int64_t ctx_sum = warp_sum31(ctx);  // ctx >= 0 here (valid rows, or 0)
   if (bad || ctx_sum > p.context_total) {
     if (lane == 0) header_bad_meta(hdr);
     return;
   }
   const bool is_dec = d == 1, is_ch = d > 1;
-  const int64_t dec_pages = warp_sum64(is_dec ? (ctx + kPage - 1) / kPage : 0);
+  const int64_t dec_pages = warp_sum31(is_dec ? (ctx + kPage - 1) / kPage : 0);
   const int split = decode_split(p, dec_pages);
   const int tpt = 128 / p.G;
   const unsigned bd = __ballot_sync(0xffffffffu, is_dec), bc = __ballot_sync(0xffffffffu, is_ch);
@@ -379,8 +395,11 @@ __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
   const int64_t n_ch_items = static_cast<int64_t>(ch_tot) * p.H_kv;
   const bool dec_over = n_dec_items > p.max_dec_items || static_cast<int64_t>(dec_tot) * p.H_q > p.max_partials;
   const bool ch_over = n_ch_items > p.max_ch_items;
-  const int64_t tiles = warp_sum64(is_ch ? static_cast<int64_t>(chunk_tiles(c, d, tpt)) * p.H_kv : 0);
-  const int64_t chunk_keys = warp_sum64(is_ch ? ctx : 0);
+  const int64_t tiles =
+      warp_sum31(is_ch ? static_cast<int>(min(static_cast<int64_t>(chunk_tiles(c, d, tpt)) * p.H_kv,
+                                                int64_t{0x7fffffff}))
+                       : 0);
+  const int64_t chunk_keys = warp_sum31(is_ch ? ctx : 0);
   if (is_dec) {
     p.dec_rows[rank] = lane;
     p.dec_part_base[rank] = static_cast<int32_t>(static_cast<int64_t>(before) * p.H_q);
@@ -391,7 +410,9 @@ __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
     }
   }
   const SmSplit sp = chunk_cta_split(p, static_cast<float>(tiles), static_cast<float>(dec_pages),
-                                     ch_over ? 0 : static_cast<int>(n_ch_items), static_cast<float>(chunk_keys), lane);
+                                     ch_over ? 0 : static_cast<int>(n_ch_items),
+                                     dec_over ? 0 : static_cast<int>(n_dec_items), static_cast<float>(chunk_keys),
+                                     measured_mhz, lane);
   if (is_ch) {
     p.ch_rows[rank] = lane;
     if (!ch_over)
@@ -447,15 +468,17 @@ __device__ __forceinline__ void prologue_body(const AttnParams& p) {
     return;
   }
   if (tid == 0) s_tiles = 0;
+  const int measured_mhz = warp == 0 ? hdr[H_CLOCK_MHZ] : 0;  // for the SM split, loaded early
   // 1. load and validate the rows; count decodes, chunks, context and decode pages
   int64_t my_ctx = 0, my_pages = 0, my_ch_keys = 0;
   unsigned my_dec = 0, my_ch = 0;
   int my_bad = 0;
   for (int s = tid; s < S; s += nt) {
     const int32_t a = p.cu[s], b = p.cu[s + 1];
-    const int32_t d = b - a, c = p.q_start[s], ctx = p.ctx_lens[s];
+    const int32_t d = static_cast<int32_t>(static_cast<uint32_t>(b) - static_cast<uint32_t>(a));  // checked below
+    const int32_t c = p.q_start[s], ctx = p.ctx_lens[s];
     // d == 0 is a pad row: valid, and neither a decode nor a chunk
-    bool ok = a >= 0 && b <= p.num_tokens && d >= 0 && c >= 0 && ctx == c + d;
+    bool ok = a >= 0 && b >= a && b <= p.num_tokens && c >= 0 && static_cast<int64_t>(ctx) == static_cast<int64_t>(c) + d;
     if (p.bt_off != nullptr) {  // the row's pages must lie inside the table
       const int64_t o0 = p.bt_off[s], o1 = p.bt_off[s + 1];
       ok = ok && o0 >= 0 && o1 <= p.bt_len && cdiv64(ctx, kPage) <= o1 - o0;
@@ -590,8 +613,9 @@ __device__ __forceinline__ void prologue_body(const AttnParams& p) {
   }
   if (warp == 0) {
     const SmSplit sp = chunk_cta_split(p, static_cast<float>(s_tiles), static_cast<float>(dec_pages),
-                                       ch_over ? 0 : static_cast<int>(n_ch_items), static_cast<float>(chunk_keys),
-                                       lane);
+                                       ch_over ? 0 : static_cast<int>(n_ch_items),
+                                       dec_over ? 0 : static_cast<int>(n_dec_items), static_cast<float>(chunk_keys),
+                                       measured_mhz, lane);
     if (lane == 0) s_split = sp;
   }
   __syncthreads();

@@ -328,6 +328,15 @@ def test_inconsistent_metadata_is_flagged(env, dec_ctx):
     torch.cuda.synchronize()
     assert ms.read_status(case.ws) & ms.STATUS_BAD_META
     assert ms.read_status(case.status) == 0  # the append itself was fine
+    # a decode whose c + d wraps in 32 bits (c = 2^31 - 1, ctx given as the wrapped sum) is refused too
+    case.batch.context_lens[len(dec_ctx) // 2] -= 1
+    case.batch.q_start_pos[0] = 2**31 - 1
+    case.batch.context_lens[0] = -2**31
+    ms.mixed_step_attention(case.q, case.k_cache, case.v_cache, case.batch.cu_seqlens_q, case.batch.q_start_pos,
+                            case.batch.context_lens, case.batch.block_tables, case.batch.context_total,
+                            case.out, case.ws)
+    torch.cuda.synchronize()
+    assert ms.read_status(case.ws) & ms.STATUS_BAD_META
 
 
 def test_append_bad_position_and_negative_slot(env):
