@@ -404,21 +404,28 @@ __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
     p.dec_rows[rank] = lane;
     p.dec_part_base[rank] = static_cast<int32_t>(static_cast<int64_t>(before) * p.H_q);
     p.dec_nsplit[rank] = items;
-    if (!dec_over) {
+    if (!dec_over)
       for (int i = 0; i < items; ++i) p.dec_items[before + i] = make_int2(rank, i);
-      for (int h = 0; h < p.H_kv; ++h) p.dec_cnt[rank * p.H_kv + h] = 0;
-    }
   }
+  if (is_ch) p.ch_rows[rank] = lane;
   const SmSplit sp = chunk_cta_split(p, static_cast<float>(tiles), static_cast<float>(dec_pages),
                                      ch_over ? 0 : static_cast<int>(n_ch_items),
                                      dec_over ? 0 : static_cast<int>(n_dec_items), static_cast<float>(chunk_keys),
                                      measured_mhz, lane);
-  if (is_ch) {
-    p.ch_rows[rank] = lane;
-    if (!ch_over)
-      for (int i = 0; i < items * p.H_kv; ++i)
-        p.ch_items[static_cast<int64_t>(before - dec_tot) * p.H_kv + i] =
-            make_int2(rank, chunk_entry(i, items, p.H_kv, sp.head_major));
+  // the chunk rows' items (pairs x H_kv of them per row), the whole warp on one row at
+  // a time; then the split counters, 16 bytes per store
+  for (unsigned pend = ch_over ? 0u : bc; pend != 0u; pend &= pend - 1u) {
+    const int src = __ffs(pend) - 1;
+    const int r_rank = __shfl_sync(0xffffffffu, rank, src), r_items = __shfl_sync(0xffffffffu, items, src);
+    const int r_before = __shfl_sync(0xffffffffu, before, src);
+    int2* out = p.ch_items + static_cast<int64_t>(r_before - dec_tot) * p.H_kv;
+    for (int i = lane; i < r_items * p.H_kv; i += 32)
+      out[i] = make_int2(r_rank, chunk_entry(i, r_items, p.H_kv, sp.head_major));
+  }
+  if (!dec_over) {
+    const int n_cnt = n_dec * p.H_kv;  // the counters start 16-byte aligned in the workspace
+    for (int i = lane; i < (n_cnt >> 2); i += 32) reinterpret_cast<int4*>(p.dec_cnt)[i] = make_int4(0, 0, 0, 0);
+    for (int i = (n_cnt & ~3) + lane; i < n_cnt; i += 32) p.dec_cnt[i] = 0;
   }
   if (lane == 0) {
     hdr[H_NDEC] = dec_over ? 0 : n_dec;
@@ -797,7 +804,8 @@ __device__ __forceinline__ void merge_splits(const AttnParams& p, int k, int h0,
 // (inlined into one kernel body the two spill).
 template <int D, int G>
 __device__ __noinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem, const CUtensorMap* tm_k,
-                                             const CUtensorMap* tm_v) {
+                                             const CUtensorMap* tm_v, const CUtensorMap* tm_kp,
+                                             const CUtensorMap* tm_vp) {
   using C = DecCfg<D, G>;
   constexpr int NST = C::NST;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -852,12 +860,15 @@ __device__ __noinline__ void decode_phase(const AttnParams& p, uint8_t* dsmem, c
       }
       const uint32_t bytes = 2 * C::PAGE_BYTES + (pi == 0 ? C::Q_BYTES : 0);
       mbar_arrive_expect_tx(full + st, bytes);
-      // 16-row x 64-column boxes, 128-byte swizzled, for conflict-free ldmatrix
-      const int row0 = (phys * p.H_kv + it.hk) * kPage;
-#pragma unroll
-      for (int s = 0; s < D / 64; ++s) {
-        tma_load_2d(stage + s * 2048, tm_k, s * 64, row0, full + st);
-        tma_load_2d(stage + C::PAGE_BYTES + s * 2048, tm_v, s * 64, row0, full + st);
+      // 16-row x 64-column slabs, 128-byte swizzled, for conflict-free ldmatrix; at
+      // D = 128 each of K and V is one box of the whole page (slab 0, then slab 1)
+      const int pg = phys * p.H_kv + it.hk;
+      if constexpr (D == 128) {
+        tma_load_4d(stage, tm_kp, 0, 0, 0, pg, full + st);
+        tma_load_4d(stage + C::PAGE_BYTES, tm_vp, 0, 0, 0, pg, full + st);
+      } else {
+        tma_load_2d(stage, tm_k, 0, pg * kPage, full + st);
+        tma_load_2d(stage + C::PAGE_BYTES, tm_v, 0, pg * kPage, full + st);
       }
       if (pi == 0)
         bulk_g2s(tail + qpar * C::Q_BYTES, p.q_rot + (static_cast<int64_t>(it.tok) * p.H_q + it.hk * G) * D,
@@ -1658,6 +1669,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vp,
+                     const __grid_constant__ CUtensorMap tm_kp,
                      AttnParams p) {
   // no static shared memory: the dynamic block starts 1024-aligned, as the
   // 128-byte-swizzled TMA tiles and MMA descriptors require
@@ -1710,7 +1722,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
       __syncthreads();
       if (aborted) break;
     } else if (!chunk && n_dec_items > 0) {
-      decode_phase<D, G>(p, smem, &tm_k, &tm_v);
+      decode_phase<D, G>(p, smem, &tm_k, &tm_v, &tm_kp, &tm_vp);
       __syncwarp();
       invalidate_phase_barriers<D, G>(smem, false);
       __syncthreads();
@@ -1908,13 +1920,13 @@ int dec_warps(int D, int G) {
 
 template <int D, int G>
 int launch_paths(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                 const CUtensorMap& tvp, int n_ctas, cudaStream_t st) {
+                 const CUtensorMap& tvp, const CUtensorMap& tkp, int n_ctas, cudaStream_t st) {
   constexpr int smem = ChCfg<D>::SMEM > DecCfg<D, G>::SMEM ? ChCfg<D>::SMEM : DecCfg<D, G>::SMEM;
   static_assert(smem <= 232448, "attention kernel exceeds the per-CTA shared-memory limit");
   const int slot = (D == 128 ? 4 : 0) + (G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3);  // one bit per instance
   if (ensure_smem_limit(attention_kernel<D, G>, slot, smem) != MS_OK) return MS_ERR_CUDA;
-  if (launch_dependent(attention_kernel<D, G>, dim3(n_ctas), dim3(kChunkThreads), smem, st, tq, tk, tv, tvp, p) !=
-      cudaSuccess)
+  if (launch_dependent(attention_kernel<D, G>, dim3(n_ctas), dim3(kChunkThreads), smem, st, tq, tk, tv, tvp, tkp,
+                       p) != cudaSuccess)
     return MS_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MS_OK : MS_ERR_CUDA;
 }
@@ -1948,7 +1960,7 @@ namespace {
 // tensor maps.
 struct AttnPlan {
   AttnParams p;
-  CUtensorMap tq, tk, tv, tvp;
+  CUtensorMap tq, tk, tv, tvp, tkp;
 };
 
 // Checks every argument of an attention call and fills *L; enqueues nothing.
@@ -1990,6 +2002,7 @@ int attention_setup(const void* q_rot, const void* k_cache, const void* v_cache,
   CUtensorMap& tk = L->tk;
   CUtensorMap& tv = L->tv;
   CUtensorMap& tvp = L->tvp;
+  CUtensorMap& tkp = L->tkp;
   {
     const cuuint64_t dq[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_q),
                               static_cast<cuuint64_t>(num_tokens)};
@@ -2001,16 +2014,19 @@ int attention_setup(const void* q_rot, const void* k_cache, const void* v_cache,
     if (!encode_bf16(enc, &tq, q_rot, 3, dq, sq, bq) || !encode_bf16(enc, &tk, k_cache, 2, dk, sk, bk) ||
         !encode_bf16(enc, &tv, v_cache, 2, dk, sk, bk))
       return MS_ERR_ARG;
-    tvp = tv;  // at D = 64 a page is one 2 KB box of tv
+    tvp = tv;  // at D = 64 a page is one 2 KB box of tv (and of tk)
+    tkp = tk;
     if (D == 128) {
-      // V by whole pages for the chunk tiles: (64 columns, 16 rows, 2 slabs, page x KV head),
-      // so that one box lands as the page's slab 0 then its slab 1
+      // K and V by whole pages (V for the chunk tiles, both for the decode ring):
+      // (64 columns, 16 rows, 2 slabs, page x KV head), so that one box lands as
+      // the page's slab 0 then its slab 1
       const cuuint64_t dv[4] = {64, static_cast<cuuint64_t>(kPage), 2,
                                 static_cast<cuuint64_t>(num_pages) * H_kv};
       const cuuint64_t sv[3] = {static_cast<cuuint64_t>(D) * 2, 128,
                                 static_cast<cuuint64_t>(kPage) * D * 2};
       const cuuint32_t bv[4] = {64, static_cast<cuuint32_t>(kPage), 2, 1};
-      if (!encode_bf16(enc, &tvp, v_cache, 4, dv, sv, bv)) return MS_ERR_ARG;
+      if (!encode_bf16(enc, &tvp, v_cache, 4, dv, sv, bv) || !encode_bf16(enc, &tkp, k_cache, 4, dv, sv, bv))
+        return MS_ERR_ARG;
     }
   }
 
@@ -2075,18 +2091,18 @@ int launch_prologue(const AttnParams& p, cudaStream_t st) {
 // The persistent attention kernel for the call's head dim and group size.
 int launch_attention(const AttnPlan& L, cudaStream_t st) {
   const AttnParams& p = L.p;
-  const CUtensorMap &tq = L.tq, &tk = L.tk, &tv = L.tv, &tvp = L.tvp;
+  const CUtensorMap &tq = L.tq, &tk = L.tk, &tv = L.tv, &tvp = L.tvp, &tkp = L.tkp;
   const int n_ctas = p.num_sms;  // one persistent CTA per SM
   int rc = MS_ERR_ARG;
   switch (p.D * 100 + p.G) {
-    case 6401: rc = launch_paths<64, 1>(p, tq, tk, tv, tvp, n_ctas, st); break;
-    case 6402: rc = launch_paths<64, 2>(p, tq, tk, tv, tvp, n_ctas, st); break;
-    case 6404: rc = launch_paths<64, 4>(p, tq, tk, tv, tvp, n_ctas, st); break;
-    case 6408: rc = launch_paths<64, 8>(p, tq, tk, tv, tvp, n_ctas, st); break;
-    case 12801: rc = launch_paths<128, 1>(p, tq, tk, tv, tvp, n_ctas, st); break;
-    case 12802: rc = launch_paths<128, 2>(p, tq, tk, tv, tvp, n_ctas, st); break;
-    case 12804: rc = launch_paths<128, 4>(p, tq, tk, tv, tvp, n_ctas, st); break;
-    case 12808: rc = launch_paths<128, 8>(p, tq, tk, tv, tvp, n_ctas, st); break;
+    case 6401: rc = launch_paths<64, 1>(p, tq, tk, tv, tvp, tkp, n_ctas, st); break;
+    case 6402: rc = launch_paths<64, 2>(p, tq, tk, tv, tvp, tkp, n_ctas, st); break;
+    case 6404: rc = launch_paths<64, 4>(p, tq, tk, tv, tvp, tkp, n_ctas, st); break;
+    case 6408: rc = launch_paths<64, 8>(p, tq, tk, tv, tvp, tkp, n_ctas, st); break;
+    case 12801: rc = launch_paths<128, 1>(p, tq, tk, tv, tvp, tkp, n_ctas, st); break;
+    case 12802: rc = launch_paths<128, 2>(p, tq, tk, tv, tvp, tkp, n_ctas, st); break;
+    case 12804: rc = launch_paths<128, 4>(p, tq, tk, tv, tvp, tkp, n_ctas, st); break;
+    case 12808: rc = launch_paths<128, 8>(p, tq, tk, tv, tvp, tkp, n_ctas, st); break;
     default: break;
   }
   return rc;
