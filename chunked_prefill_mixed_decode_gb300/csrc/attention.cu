@@ -297,13 +297,15 @@ __device__ __forceinline__ int chunk_entry(int i, int np, int H_kv, bool head_ma
 }
 
 // Decode split size: about 8 items per decode worker warp, clamped; at least 32
-// pages (64 when G >= 4, whose items carry G heads of partials to merge).
-__device__ __forceinline__ int decode_split(const AttnParams& p, int64_t dec_pages) {
+// pages (64 when G >= 4, whose items carry G heads of partials to merge, and 128
+// when chunk rows share the step: decode then runs on the SMs the chunk tiles
+// leave, where fewer, longer items cost less than a finer tail saves).
+__device__ __forceinline__ int decode_split(const AttnParams& p, int64_t dec_pages, bool with_chunks) {
   const int64_t num = dec_pages * p.H_kv, den = static_cast<int64_t>(p.dec_workers) * 8;
   int64_t split = num + den <= 0xffffffffll
                       ? static_cast<int64_t>(static_cast<uint32_t>(num + den - 1) / static_cast<uint32_t>(den))
                       : cdiv64(num, den);
-  const int64_t min_split = p.G >= 4 ? 2 * kMinSplitPages : kMinSplitPages;
+  const int64_t min_split = p.G >= 4 ? (with_chunks ? 4 : 2) * kMinSplitPages : kMinSplitPages;
   split = split < min_split ? min_split : (split > kMaxSplitPages ? kMaxSplitPages : split);
   return static_cast<int>(split);
 }
@@ -348,7 +350,7 @@ __device__ __forceinline__ void prologue_warp(const AttnParams& p) {
   }
   const bool is_dec = d == 1, is_ch = d > 1;
   const int64_t dec_pages = warp_sum31(is_dec ? (ctx + kPage - 1) / kPage : 0);
-  const int split = decode_split(p, dec_pages);
+  const int split = decode_split(p, dec_pages, __any_sync(0xffffffffu, is_ch));
   const int tpt = 128 / p.G;
   const unsigned bd = __ballot_sync(0xffffffffu, is_dec), bc = __ballot_sync(0xffffffffu, is_ch);
   const int n_dec = __popc(bd), n_ch = __popc(bc);
@@ -530,7 +532,7 @@ __device__ __forceinline__ void prologue_body(const AttnParams& p) {
     return;
   }
   // 2. decode split size
-  const int split = decode_split(p, dec_pages);
+  const int split = decode_split(p, dec_pages, n_ch > 0);
   const int tpt = 128 / p.G;
   const unsigned split32 = static_cast<unsigned>(split);
   // 3. the two lists in input order: decode rows at lst[0, n_dec), chunk rows after them
