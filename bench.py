@@ -802,26 +802,39 @@ def run_timeline(args, local):
 SPLIT_CONFIGS = ["mha7b_b512", "mha13b_b2048", "gqa8b_b8192", "long_bimodal_b4608"]
 
 
-def _timed(fn, reps: int, stream) -> float:
-    """Mean device milliseconds of fn() over reps launches (events on the launching stream)."""
+def _timed(fn, reps: int, stream, flush=None) -> float:
+    """Mean device milliseconds of fn() over reps launches (events on the launching stream).  With
+    ``flush``, each launch is timed on its own after flush() has overwritten L2 (outside the events)."""
     import torch
     for _ in range(3):
         fn()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+    pairs = []
     for _ in range(reps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
         fn()
-    e1.record(stream)
+        e1.record(stream)
+        pairs.append((e0, e1))
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps
+    return sum(a.elapsed_time(b) for a, b in pairs) / reps
 
 
 def run_split(args, local):
     """Attribute each workload's step to its two bounds: the attention call on the mixed batch, on
     its decode rows alone (HBM GB/s of their KV reads) and on its prefill chunks alone (TFLOP/s
     of their causal pairs), plus the append on the mixed batch.  Every variant reads the same KV
-    pool; each call is timed alone (back to back, CUDA events), summed over the workload's batches."""
+    pool; each call is timed alone with CUDA events after a write of twice the L2 size has evicted
+    what the previous call left there, summed over the workload's batches."""
     import torch
 
     import chunked_prefill_mixed_decode_gb300 as ms
@@ -834,6 +847,14 @@ def run_split(args, local):
     stream = torch.cuda.current_stream(device)
     peaks, peak_src = read_peaks()
     reps = max(5, args.split_reps)
+    l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (129 << 20))
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    n_flush = [0]
+
+    def flush():
+        n_flush[0] += 1
+        flush_buf.fill_(n_flush[0] & 0xFF)
+
     out = []
     for name in args.split_configs:
         wls = load_workload(name)
@@ -872,12 +893,12 @@ def run_split(args, local):
                                             b.context_lens, b.block_tables, b.context_total, o, ws, stream=stream)
 
                 append()
-                t_attn = _timed(attend, reps, stream)
+                t_attn = _timed(attend, reps, stream, flush)
                 if ms.read_status(status) or ms.read_status(ws):
                     raise RuntimeError(f"device status set in {name} {label}")
                 acc[label + "_ms"] += t_attn
                 if label == "mixed":
-                    acc["append_ms"] += _timed(append, reps, stream)
+                    acc["append_ms"] += _timed(append, reps, stream, flush)
                     acc["append_bytes"] += cnt["append_bytes"]
                     acc["mixed_bytes"] += cnt["attn_bytes"]
                     acc["mixed_flops"] += cnt["flops"]
@@ -909,8 +930,8 @@ def run_split(args, local):
         })
     line = {"split": "attention call per workload: mixed, decode rows only, prefill chunks only",
             "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"], "source": peak_src,
-                      "note": "each call timed alone, back to back: the burst tensor peak applies"},
-            "reps": reps, "configs": out}
+                      "note": "each call timed alone: the burst tensor peak applies"},
+            "reps": reps, "l2_flush_bytes": int(flush_buf.numel()), "configs": out}
     print(json.dumps(line), flush=True)
 
 
