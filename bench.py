@@ -802,21 +802,13 @@ def run_timeline(args, local):
 SPLIT_CONFIGS = ["mha7b_b512", "mha13b_b2048", "gqa8b_b8192", "long_bimodal_b4608"]
 
 
-def _timed(fn, reps: int, stream, flush=None) -> float:
-    """Mean device milliseconds of fn() over reps launches (events on the launching stream).  With
-    ``flush``, each launch is timed on its own after flush() has overwritten L2 (outside the events)."""
+def _call_times(fn, reps: int, stream, flush) -> list:
+    """Device milliseconds of each of reps launches of fn(), each timed alone with CUDA events on
+    the launching stream after flush() has overwritten L2 (outside the events); 3 warm-ups first."""
     import torch
     for _ in range(3):
         fn()
     torch.cuda.synchronize()
-    if flush is None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
     pairs = []
     for _ in range(reps):
         flush()
@@ -826,7 +818,7 @@ def _timed(fn, reps: int, stream, flush=None) -> float:
         e1.record(stream)
         pairs.append((e0, e1))
     torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in pairs) / reps
+    return [a.elapsed_time(b) for a, b in pairs]
 
 
 def run_split(args, local):
@@ -893,12 +885,16 @@ def run_split(args, local):
                                             b.context_lens, b.block_tables, b.context_total, o, ws, stream=stream)
 
                 append()
-                t_attn = _timed(attend, reps, stream, flush)
+                times = _call_times(attend, reps, stream, flush)
+                t_attn = sum(times) / len(times)
+                acc[label + "_median"] = acc.get(label + "_median", 0.0) + statistics.median(times)
+                acc[label + "_min"] = acc.get(label + "_min", 0.0) + min(times)
                 if ms.read_status(status) or ms.read_status(ws):
                     raise RuntimeError(f"device status set in {name} {label}")
                 acc[label + "_ms"] += t_attn
                 if label == "mixed":
-                    acc["append_ms"] += _timed(append, reps, stream, flush)
+                    times = _call_times(append, reps, stream, flush)
+                    acc["append_ms"] += sum(times) / len(times)
                     acc["append_bytes"] += cnt["append_bytes"]
                     acc["mixed_bytes"] += cnt["attn_bytes"]
                     acc["mixed_flops"] += cnt["flops"]
@@ -927,6 +923,11 @@ def run_split(args, local):
             "chunk_only_tflops": round(chk_tf, 1) if chk_tf else None,
             "chunk_only_tensor_frac": round(chk_tf / tf, 4) if chk_tf else None,
             "mixed_vs_sum_of_parts": round(acc["mixed_ms"] / (acc["decode_only_ms"] + acc["chunk_only_ms"]), 4),
+            # per call: median and minimum of the timed calls, summed over the workload's batches
+            "median_ms": {lab: round(acc[lab + "_median"], 4) for lab in ("mixed", "decode_only", "chunk_only")
+                          if lab + "_median" in acc},
+            "min_ms": {lab: round(acc[lab + "_min"], 4) for lab in ("mixed", "decode_only", "chunk_only")
+                       if lab + "_min" in acc},
         })
     line = {"split": "attention call per workload: mixed, decode rows only, prefill chunks only",
             "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"], "source": peak_src,
