@@ -338,8 +338,10 @@ def measure_config(name, args, ms, world, rank, device, dist) -> dict:
                       "then the persistent attention_kernel)")
     roof["peak_source"] = (f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
                            + ("; sustained bf16 (kernel timed inside a step)" if roof["bound"] == "tensor" else ""))
+    all_ms = [t for a in attn_ms for t in a]
     roof["per_launch"] = {"alg_bytes": int(grp_bytes_avg), "alg_flops": int(flops_avg),
-                          "avg_ms": round(grp_avg_ms, 4)}
+                          "avg_ms": round(grp_avg_ms, 4), "median_ms": round(statistics.median(all_ms), 4),
+                          "min_ms": round(min(all_ms), 4)}
     step_bytes = sum(s["counts"]["step_bytes"] for s in subs)
     step_flops = attn_flops
     t_roof = max(step_bytes / (peaks["hbm_gbs"] * 1e9), step_flops / (peaks["bf16_tflops_sustained"] * 1e12))
